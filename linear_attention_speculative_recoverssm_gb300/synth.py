@@ -1,0 +1,231 @@
+"""Seeded synthetic inputs for the KDA RecoverSSM step.
+
+This module draws random operands and index structure only; it holds none of
+the method's arithmetic.  Both the CUDA path (tests, bench) and the CPU oracle
+(tests) take their inputs from here, as numpy arrays:
+
+* BF16 tensors are uint16 bit patterns (rounded to nearest even from FP32
+  draws), FP32 tensors are float32, indices are int32.
+* Activations are token-major: token ``b * Q + t`` of request ``b``.
+
+Distributions (one recipe for every workload):
+
+* state S_0 ~ N(0, 0.05^2) on the slots a request uses, zero elsewhere;
+* q, k: a N(0, 1) draw per (token, head) scaled onto the unit sphere (a
+  uniform random direction), q additionally multiplied by K^-1/2;
+* v, raw_g, raw_beta ~ N(0, 1); A_log ~ U(0, 2.5) per head;
+  dt_bias ~ N(0, 0.1^2) per (head, key channel); lower_bound = -5;
+* records of the previous window: corrections u ~ N(0, 0.5^2) (FP32), keys
+  drawn like k, raw gates ~ N(0, 1);
+* slots: distinct live slots in 1..slots-1 (slot 0 is the null slot),
+  record rows a random permutation, counts uniform on their ranges.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NULL_SLOT = 0
+LOWER_BOUND = -5.0
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """FP32 draws -> BF16 bit patterns (round to nearest even; finite input)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    b = b + (((b >> 16) & 1) + 0x7FFF)
+    return (b >> 16).astype(np.uint16)
+
+
+def _normal(rng, shape, std=1.0):
+    x = rng.standard_normal(shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
+
+
+def _unit_directions(rng, shape):
+    """Random directions on the unit sphere along the last axis."""
+    x = rng.standard_normal(shape, dtype=np.float32)
+    x /= np.linalg.norm(x, axis=-1, keepdims=True)
+    return x
+
+
+def replay_verify_case(*, B, H, Q, slots, seed, RQ=None, rows=None, K=128,
+                       V=128, pending_max=None, padding_frac=0.0,
+                       no_record_frac=0.0, state_dtype="f32",
+                       boundary_frac=0.0):
+    """Operands of one RecoverSSM verify step (replay + verify).
+
+    Returns a dict with q, k, v, raw_g [B*Q, H, K|V], raw_beta [B*Q, H] (BF16
+    bits); A_log [H], dt_bias [H, K] (FP32); state [slots, H, V, K] (FP32 or
+    BF16 bits); state_slots [B]; record_rows [B]; pending [rows]; corr
+    [rows, H, RQ, V] FP32; key_gate [rows, H, RQ, 2K] BF16 bits; boundary_slots
+    and boundary_lens [B] (all null / 0 unless ``boundary_frac`` > 0); and the
+    scalars lower_bound, q_scale, null_slot, B, H, Q, RQ.
+    """
+    RQ = Q if RQ is None else RQ
+    rows = B if rows is None else rows
+    pending_max = RQ if pending_max is None else pending_max
+    assert rows >= B and Q <= RQ
+    rng = np.random.default_rng(seed)
+
+    n_pad = int(round(padding_frac * B))
+    order = rng.permutation(B)
+    padding = np.zeros(B, dtype=bool)
+    padding[order[:n_pad]] = True
+    live_idx = np.flatnonzero(~padding)
+    n_bnd = int(round(boundary_frac * len(live_idx)))
+    need = len(live_idx) + n_bnd
+    assert need <= slots - 1, "not enough distinct slots"
+    chosen = rng.choice(np.arange(1, slots, dtype=np.int64), size=need,
+                        replace=False)
+    state_slots = np.full(B, NULL_SLOT, dtype=np.int32)
+    state_slots[live_idx] = chosen[:len(live_idx)]
+
+    record_rows = rng.permutation(rows)[:B].astype(np.int32)
+    n_norec = int(round(no_record_frac * B))
+    if n_norec:
+        record_rows[rng.choice(live_idx, size=n_norec, replace=False)] = -1
+    record_rows[padding] = -1
+    pending = rng.integers(0, pending_max + 1, size=rows, dtype=np.int32)
+
+    boundary_slots = np.full(B, NULL_SLOT, dtype=np.int32)
+    boundary_lens = np.zeros(B, dtype=np.int32)
+    if n_bnd:
+        crossing = rng.choice(live_idx, size=n_bnd, replace=False)
+        boundary_slots[crossing] = chosen[len(live_idx):]
+        boundary_lens[crossing] = rng.integers(1, max(RQ, 2), size=n_bnd,
+                                               dtype=np.int32)
+
+    if state_dtype == "f32":
+        state = np.zeros((slots, H, V, K), dtype=np.float32)
+    else:
+        state = np.zeros((slots, H, V, K), dtype=np.uint16)
+    used = np.sort(state_slots[state_slots > NULL_SLOT])
+    draw = _normal(rng, (len(used), H, V, K), 0.05)
+    state[used] = draw if state_dtype == "f32" else to_bf16_bits(draw)
+    del draw
+
+    T = B * Q
+    q = _unit_directions(rng, (T, H, K)) * np.float32(K ** -0.5)
+    k = _unit_directions(rng, (T, H, K))
+    case = dict(
+        q=to_bf16_bits(q),
+        k=to_bf16_bits(k),
+        v=to_bf16_bits(_normal(rng, (T, H, V))),
+        raw_g=to_bf16_bits(_normal(rng, (T, H, K))),
+        raw_beta=to_bf16_bits(_normal(rng, (T, H))),
+        A_log=rng.uniform(0.0, 2.5, size=H).astype(np.float32),
+        dt_bias=_normal(rng, (H, K), 0.1),
+        state=state,
+        state_slots=state_slots,
+        record_rows=record_rows,
+        pending=pending,
+        corr=_normal(rng, (rows, H, RQ, V), 0.5),
+        key_gate=np.concatenate(
+            [to_bf16_bits(_unit_directions(rng, (rows, H, RQ, K))),
+             to_bf16_bits(_normal(rng, (rows, H, RQ, K)))], axis=-1),
+        boundary_slots=boundary_slots,
+        boundary_lens=boundary_lens,
+        lower_bound=LOWER_BOUND,
+        q_scale=float(K ** -0.5),
+        null_slot=NULL_SLOT,
+        B=B, H=H, Q=Q, RQ=RQ,
+    )
+    return case
+
+
+def commit_case(*, L, B, H, Q, slots, seed, K=128, V=128, state_dtype="bf16",
+                null_frac=0.10, in_place_frac=0.5, boundary_frac=0.25):
+    """Operands of the standalone commit over L layers.
+
+    Per layer: state [slots, H, V, K] (BF16 bits or FP32), corr [B, H, Q, V]
+    FP32, key_gate [B, H, Q, 2K] BF16 bits (request b's records in row b).
+    Shared across layers: sources, commit_lens, destinations, boundaries,
+    boundary_lens [B] and A_log [L, H], dt_bias [L, H, K].  A ``null_frac``
+    share of requests has source = destination = null; of the others,
+    ``in_place_frac`` commit in place and the rest to a fresh slot; a
+    ``boundary_frac`` share of all requests crosses a block boundary after
+    m ~ U{1..Q-1} tokens into a fresh boundary slot.
+    """
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(B)
+    n_null = int(round(null_frac * B))
+    null_rows = order[:n_null]
+    live_idx = np.sort(order[n_null:])
+    in_place = rng.random(len(live_idx)) < in_place_frac
+    n_fresh = int((~in_place).sum())
+    n_bnd = int(round(boundary_frac * B))
+    need = len(live_idx) + n_fresh + n_bnd
+    assert need <= slots - 1, "not enough distinct slots"
+    chosen = rng.choice(np.arange(1, slots, dtype=np.int64), size=need,
+                        replace=False)
+    sources = np.full(B, NULL_SLOT, dtype=np.int32)
+    destinations = np.full(B, NULL_SLOT, dtype=np.int32)
+    sources[live_idx] = chosen[:len(live_idx)]
+    dst = sources[live_idx].copy()
+    dst[~in_place] = chosen[len(live_idx):len(live_idx) + n_fresh]
+    destinations[live_idx] = dst
+    commit_lens = rng.integers(0, Q + 1, size=B, dtype=np.int32)
+    boundaries = np.full(B, NULL_SLOT, dtype=np.int32)
+    boundary_lens = np.zeros(B, dtype=np.int32)
+    if n_bnd:
+        crossing = rng.choice(np.arange(B), size=n_bnd, replace=False)
+        boundaries[crossing] = chosen[len(live_idx) + n_fresh:]
+        boundary_lens[crossing] = rng.integers(1, max(Q, 2), size=n_bnd,
+                                               dtype=np.int32)
+    del null_rows
+
+    layers = []
+    used = np.sort(sources[sources > NULL_SLOT])
+    for _ in range(L):
+        if state_dtype == "bf16":
+            state = np.zeros((slots, H, V, K), dtype=np.uint16)
+            state[used] = to_bf16_bits(_normal(rng, (len(used), H, V, K), 0.05))
+        else:
+            state = np.zeros((slots, H, V, K), dtype=np.float32)
+            state[used] = _normal(rng, (len(used), H, V, K), 0.05)
+        corr = _normal(rng, (B, H, Q, V), 0.5)
+        key_gate = np.concatenate(
+            [to_bf16_bits(_unit_directions(rng, (B, H, Q, K))),
+             to_bf16_bits(_normal(rng, (B, H, Q, K)))], axis=-1)
+        layers.append(dict(state=state, corr=corr, key_gate=key_gate))
+    return dict(
+        layers=layers,
+        A_log=rng.uniform(0.0, 2.5, size=(L, H)).astype(np.float32),
+        dt_bias=_normal(rng, (L, H, K), 0.1),
+        sources=sources, commit_lens=commit_lens, destinations=destinations,
+        boundaries=boundaries, boundary_lens=boundary_lens,
+        lower_bound=LOWER_BOUND, null_slot=NULL_SLOT, L=L, B=B, H=H, Q=Q,
+    )
+
+
+# The workloads of the five measured configurations, by what they are.
+WORKLOADS = {
+    "tiny-b2-h2-q2": dict(kind="replay_verify", B=2, H=2, Q=2, slots=4,
+                          seed=0),
+    "commit-bf16-l4-h32-b64-q4-align": dict(kind="commit", L=4, H=32, B=64,
+                                            Q=4, slots=256, seed=1),
+    "replay-verify-f32-h32-b128-q4": dict(kind="replay_verify", B=128, H=32,
+                                          Q=4, slots=512, seed=2,
+                                          no_record_frac=0.05),
+    "replay-verify-f32-h64-b512-q8": dict(kind="replay_verify", B=512, H=64,
+                                          Q=8, slots=1024, seed=3,
+                                          padding_frac=0.05),
+}
+
+
+def make(name, **overrides):
+    """Build a named workload (see WORKLOADS), with optional overrides."""
+    spec = dict(WORKLOADS[name])
+    spec.update(overrides)
+    kind = spec.pop("kind")
+    if kind == "commit":
+        return commit_case(**spec)
+    return replay_verify_case(**spec)
+
+
+def latency_case(*, B, Q, seed=4, H=32, slots=64):
+    """The latency sweep's small batches: H=32, B in {1, 4, 16}, Q in
+    {1, 2, 4, 8}, pending ~ U{0..Q}."""
+    return replay_verify_case(B=B, H=H, Q=Q, slots=max(slots, B + 1),
+                              seed=seed + 100 * B + Q)

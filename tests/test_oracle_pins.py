@@ -1,0 +1,449 @@
+"""Pins of the FP64 oracle to things other than itself (no GPU needed).
+
+Each test checks the oracle against what the pages or the mathematics fix:
+a hand-derived worked example, alternative formulations the pages state
+(closed-form replay, chunked WY verify), special cases that reduce to a
+textbook routine, and invariants (n = 0 leaves the checkpoint, deferred then
+flushed equals eager).  Shapes with K != V are used where a transposed
+operand would otherwise go unnoticed.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import kda_oracle as ko
+from linear_attention_speculative_recoverssm_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(x):
+    """Exactly representable FP32 values -> BF16 bits (test helper)."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0), "value not exactly representable in BF16"
+    return (b >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# conversions
+# ---------------------------------------------------------------------------
+
+def test_bf16_rounding_known_patterns():
+    cases = {
+        1.0: 0x3F80, -2.0: 0xC000, 0.0: 0x0000,
+        1.0 + 2.0 ** -8: 0x3F80,            # tie -> even (down)
+        1.0 + 3 * 2.0 ** -8: 0x3F82,        # tie -> even (up)
+        1.0 + 2.0 ** -8 + 2.0 ** -30: 0x3F81,  # just above the tie
+        2.0 ** -130: 0x0008,                 # subnormal
+        3.4e38: 0x7F80,                      # rounds past the largest -> inf
+    }
+    for value, bits in cases.items():
+        assert int(ko.f64_to_bf16(np.array([value]))[0]) == bits, value
+
+
+def test_bf16_rounding_matches_torch_on_fp32_values():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(100000) * np.exp(rng.uniform(-20, 20, 100000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ko.f64_to_bf16(x.astype(np.float64)), ref)
+    back = ko.bf16_to_f64(ref)
+    np.testing.assert_array_equal(back, torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float().numpy())
+
+
+# ---------------------------------------------------------------------------
+# per-channel operands
+# ---------------------------------------------------------------------------
+
+def test_decay_special_values():
+    # sigmoid(0) = 1/2: d = exp(lb / 2); A_log = 0 -> exp(A_log) = 1
+    d = ko.decay(np.zeros(3), 0.0, np.zeros(3), -5.0)
+    np.testing.assert_allclose(d, math.exp(-2.5), rtol=1e-15)
+    # lower bound 0: no decay at all
+    np.testing.assert_array_equal(ko.decay(np.array([-3.0, 0.0, 7.0]), 1.3, np.ones(3), 0.0), 1.0)
+    # saturated gate: sigmoid -> 1, d -> exp(lb); very negative: d -> 1
+    np.testing.assert_allclose(ko.decay(np.array([80.0]), 0.0, np.zeros(1), -5.0), math.exp(-5.0), rtol=1e-15)
+    np.testing.assert_allclose(ko.decay(np.array([-80.0]), 0.0, np.zeros(1), -5.0), 1.0, rtol=1e-15)
+    # exp(A_log) multiplies (raw_g + dt_bias): A_log = ln 2, raw_g = 1, dt = -0.5 -> sigmoid(1)
+    d = ko.decay(np.array([1.0]), math.log(2.0), np.array([-0.5]), -1.0)
+    np.testing.assert_allclose(d, math.exp(-1.0 / (1.0 + math.exp(-1.0))), rtol=1e-14)
+
+
+def test_l2norm_closed_form():
+    x = np.array([[3.0, 4.0], [0.0, 0.0], [1e-4, 0.0]])
+    y = ko.l2norm(x)
+    np.testing.assert_allclose(y[0], np.array([3.0, 4.0]) / math.sqrt(25.0 + 1e-6), rtol=1e-15)
+    np.testing.assert_array_equal(y[1], 0.0)
+    np.testing.assert_allclose(y[2, 0], 1e-4 / math.sqrt(1e-8 + 1e-6), rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# the hand-derived worked example (K = V = 2)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case_index", [0, 1])
+def test_hand_worked_example(case_index):
+    g = json.load(open(os.path.join(GOLDEN, "kda_hand_k2.json")))
+    c = g["cases"][case_index]
+    Q = len(c["q"])
+    K = V = 2
+    rec = c["records"]
+    state = np.zeros((2, 1, V, K), dtype=np.float32)
+    state[1, 0] = np.array(c["S0"], dtype=np.float32)
+    corr = np.zeros((1, 1, 2, V), dtype=np.float32)
+    key_gate = np.zeros((1, 1, 2, 2 * K), dtype=np.uint16)
+    if rec is not None:
+        corr[0, 0] = np.array(rec["u"], dtype=np.float32)
+        key_gate[0, 0, :, :K] = _bits(rec["k"])
+        key_gate[0, 0, :, K:] = _bits(rec["raw_g"])
+    out = np.zeros((Q, 1, V), dtype=np.uint16)
+    out64 = np.zeros((Q, 1, V))
+    ko.replay_verify(
+        q=_bits(c["q"]).reshape(Q, 1, K), k=_bits(c["k"]).reshape(Q, 1, K),
+        v=_bits(c["v"]).reshape(Q, 1, V), raw_g=_bits(c["raw_g"]).reshape(Q, 1, K),
+        raw_beta=_bits(c["raw_beta"]).reshape(Q, 1),
+        A_log=np.array(g["A_log"], dtype=np.float32),
+        dt_bias=np.array(g["dt_bias"], dtype=np.float32),
+        lower_bound=g["lower_bound"], q_scale=g["q_scale"], state=state,
+        state_slots=np.array([1], dtype=np.int32), record_rows=np.array([0], dtype=np.int32),
+        pending=np.array([c["pending"]], dtype=np.int32), corr=corr, key_gate=key_gate,
+        out=out, out_f64=out64, B=1, H=1, Q=Q)
+    np.testing.assert_allclose(out64[:, 0, :], np.array(c["expect_o"]), atol=1e-5, rtol=1e-5)
+    np.testing.assert_allclose(corr[0, 0, :Q], np.array(c["expect_u"]), atol=1e-5, rtol=1e-5)
+    np.testing.assert_allclose(state[1, 0], np.array(c["expect_state_after"]), atol=1e-5, rtol=1e-5)
+    # records now hold the verified window's key and raw gate, copied bit-exactly
+    np.testing.assert_array_equal(key_gate[0, 0, :Q, :K], _bits(c["k"]))
+    np.testing.assert_array_equal(key_gate[0, 0, :Q, K:], _bits(c["raw_g"]))
+
+
+# ---------------------------------------------------------------------------
+# alternative formulations stated on the pages
+# ---------------------------------------------------------------------------
+
+def _toy(rng, K, V, n, Q):
+    S0 = rng.standard_normal((V, K))
+    u = rng.standard_normal((n, V)) * 0.5
+    kr = rng.standard_normal((n, K))
+    gr = rng.standard_normal((n, K))
+    q = rng.standard_normal((Q, K))
+    k = rng.standard_normal((Q, K))
+    v = rng.standard_normal((Q, V))
+    g = rng.standard_normal((Q, K))
+    rb = rng.standard_normal(Q)
+    a_log = rng.uniform(0, 2.5)
+    dt = rng.standard_normal(K) * 0.1
+    return S0, u, kr, gr, q, k, v, g, rb, a_log, dt
+
+
+@pytest.mark.parametrize("K,V", [(2, 3), (5, 4), (128, 128)])
+def test_closed_form_replay_equals_sequential(K, V):
+    rng = np.random.default_rng(K * 31 + V)
+    for n in range(0, 9):
+        S0, u, kr, gr, *_, a_log, dt = _toy(rng, K, V, n, 1)
+        seq, _ = ko.replay_item(S0, u, kr, gr, n, a_log, dt, -5.0)
+        closed = ko.replay_closed_form(S0, u, kr, gr, n, a_log, dt, -5.0)
+        np.testing.assert_allclose(closed, seq, rtol=1e-12, atol=1e-12 * np.abs(seq).max())
+
+
+@pytest.mark.parametrize("K,V", [(2, 3), (6, 4), (128, 128)])
+def test_chunked_verify_equals_stock_recurrence(K, V):
+    rng = np.random.default_rng(K * 17 + V)
+    for Q in range(1, 9):
+        S0, _, _, _, q, k, v, g, rb, a_log, dt = _toy(rng, K, V, 0, Q)
+        u1, o1 = ko.verify_item(S0, q, k, v, g, rb, a_log, dt, -5.0, K ** -0.5)
+        u2, o2 = ko.verify_chunked(S0, q, k, v, g, rb, a_log, dt, -5.0, K ** -0.5)
+        np.testing.assert_allclose(u2, u1, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(o2, o1, rtol=1e-11, atol=1e-12)
+
+
+def test_boundary_state_is_prefix_replay():
+    rng = np.random.default_rng(3)
+    S0, u, kr, gr, *_, a_log, dt = _toy(rng, 4, 3, 6, 1)
+    S_n, _ = ko.replay_item(S0, u, kr, gr, 6, a_log, dt, -5.0)
+    for m in range(1, 9):
+        _, S_m = ko.replay_item(S0, u, kr, gr, 6, a_log, dt, -5.0, m=m)
+        ref = ko.replay_closed_form(S0, u, kr, gr, min(m, 6), a_log, dt, -5.0)
+        np.testing.assert_allclose(S_m, ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(S_m, S_n, rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# special cases reducing to textbook routines
+# ---------------------------------------------------------------------------
+
+def test_beta_zero_is_a_plain_decayed_gemv():
+    # beta = 0 (raw_beta = -inf) and no decay (lower_bound = 0): u = 0 and
+    # o_t = S qn_t, one matrix-vector product with the normalised query.
+    rng = np.random.default_rng(11)
+    K, V, Q = 5, 3, 4
+    S0, _, _, _, q, k, v, g, _, a_log, dt = _toy(rng, K, V, 0, Q)
+    rb = np.full(Q, -np.inf)
+    u, o = ko.verify_item(S0, q, k, v, g, rb, a_log, dt, 0.0, 0.7)
+    np.testing.assert_array_equal(u, 0.0)
+    qn = q / np.sqrt(np.linalg.norm(q, axis=1, keepdims=True) ** 2 + 1e-6)
+    np.testing.assert_allclose(o, 0.7 * qn @ S0.T, rtol=1e-13)
+
+
+def test_delta_rule_with_unit_step_writes_v_at_k():
+    # lower_bound = 0 and beta = 1 reduce each token to the delta rule with a
+    # unit step: afterwards S kn_t = v_t (up to the 1e-6 in the norm).  With
+    # q_t = k_t and q_scale = 1 the output is therefore v_t.
+    rng = np.random.default_rng(5)
+    K, V, Q = 7, 3, 6
+    S0, _, _, _, _, k, v, g, _, a_log, dt = _toy(rng, K, V, 0, Q)
+    u, o = ko.verify_item(S0, k, k, v, g, np.full(Q, np.inf), a_log, dt, 0.0, 1.0)
+    np.testing.assert_allclose(o, v, rtol=0, atol=1e-5 * np.abs(v).max())
+    # and the correction is exactly the residual against the current state
+    S = S0.copy()
+    kn = k / np.sqrt((k * k).sum(1, keepdims=True) + 1e-6)
+    for t in range(Q):
+        np.testing.assert_allclose(u[t], v[t] - S @ kn[t], rtol=1e-12, atol=1e-12)
+        S = S + np.outer(u[t], kn[t])
+
+
+def test_zero_state_single_token():
+    # S = 0, one token: u = beta v, o = beta v (kn . qn)
+    K, V = 4, 3
+    q = np.array([[1.0, 2.0, 0.0, -1.0]])
+    k = np.array([[0.5, -1.0, 2.0, 0.0]])
+    v = np.array([[1.0, -2.0, 3.0]])
+    u, o = ko.verify_item(np.zeros((V, K)), q, k, v, np.zeros((1, K)), np.array([0.0]),
+                          0.0, np.zeros(K), -5.0, 0.25)
+    kn = k[0] / math.sqrt(k[0] @ k[0] + 1e-6)
+    qn = q[0] / math.sqrt(q[0] @ q[0] + 1e-6) * 0.25
+    np.testing.assert_allclose(u[0], 0.5 * v[0], rtol=1e-15)
+    np.testing.assert_allclose(o[0], 0.5 * v[0] * (kn @ qn), rtol=1e-14)
+
+
+def test_q_scale_is_linear_and_inputs_are_normalised():
+    rng = np.random.default_rng(9)
+    K, V, Q = 8, 5, 3
+    S0, _, _, _, q, k, v, g, rb, a_log, dt = _toy(rng, K, V, 0, Q)
+    u1, o1 = ko.verify_item(S0, q, k, v, g, rb, a_log, dt, -5.0, 1.0)
+    u2, o2 = ko.verify_item(S0, q, k, v, g, rb, a_log, dt, -5.0, 3.0)
+    np.testing.assert_allclose(o2, 3.0 * o1, rtol=1e-13)
+    np.testing.assert_allclose(u2, u1, rtol=1e-14)
+    # scaling the raw q or k by a constant changes nothing (normalised inputs)
+    u3, o3 = ko.verify_item(S0, 4.0 * q, 2.0 * k, v, g, rb, a_log, dt, -5.0, 1.0)
+    np.testing.assert_allclose(o3, o1, rtol=1e-5, atol=1e-7)
+    np.testing.assert_allclose(u3, u1, rtol=1e-5, atol=1e-7)
+
+
+# ---------------------------------------------------------------------------
+# invariants of the protocol
+# ---------------------------------------------------------------------------
+
+def _case(**kw):
+    base = dict(B=6, H=3, Q=3, slots=16, seed=21, K=8, V=6)
+    base.update(kw)
+    return synth.replay_verify_case(**base)
+
+
+def _run(case, pending=True, **kw):
+    c = {key: (val.copy() if isinstance(val, np.ndarray) else val) for key, val in case.items()}
+    B, H, Q = c["B"], c["H"], c["Q"]
+    out = np.zeros(c["v"].shape, dtype=np.uint16)
+    ko.replay_verify(q=c["q"], k=c["k"], v=c["v"], raw_g=c["raw_g"], raw_beta=c["raw_beta"],
+                     A_log=c["A_log"], dt_bias=c["dt_bias"], lower_bound=c["lower_bound"],
+                     q_scale=c["q_scale"], state=c["state"], state_slots=c["state_slots"],
+                     record_rows=c["record_rows"], corr=c["corr"], key_gate=c["key_gate"],
+                     out=out, B=B, H=H, Q=Q, pending=c["pending"] if pending else None, **kw)
+    c["out"] = out
+    return c
+
+
+def test_n_zero_leaves_the_checkpoint_bit_identical():
+    case = _case()
+    case["pending"][:] = 0
+    after = _run(case)
+    np.testing.assert_array_equal(after["state"], case["state"])
+    # and the stock verify (no pending) never writes it
+    after = _run(_case(), pending=False)
+    np.testing.assert_array_equal(after["state"], _case()["state"])
+    # align: with n = 0 the boundary slot is not written either; with n > 0 it
+    # receives S_min(m, n)
+    case = _case(boundary_frac=0.5)
+    crossing = case["boundary_slots"] > 0
+    assert crossing.any()
+    case["pending"][:] = 0
+    after = _run(case, boundary_slots=case["boundary_slots"], boundary_lens=case["boundary_lens"])
+    np.testing.assert_array_equal(after["state"], case["state"])
+    case["pending"][:] = case["RQ"]
+    after = _run(case, boundary_slots=case["boundary_slots"], boundary_lens=case["boundary_lens"])
+    for b in np.flatnonzero(crossing & (case["record_rows"] >= 0)):
+        for h in range(case["H"]):
+            rec, m = case["record_rows"][b], min(case["boundary_lens"][b], case["RQ"])
+            K = case["q"].shape[-1]
+            ref = ko.replay_closed_form(
+                case["state"][case["state_slots"][b], h].astype(np.float64),
+                case["corr"][rec, h, :m].astype(np.float64),
+                ko.bf16_to_f64(case["key_gate"][rec, h, :m, :K]),
+                ko.bf16_to_f64(case["key_gate"][rec, h, :m, K:]), m,
+                float(case["A_log"][h]), case["dt_bias"][h].astype(np.float64), case["lower_bound"])
+            np.testing.assert_allclose(after["state"][case["boundary_slots"][b], h], ref,
+                                       rtol=1e-6, atol=1e-7)
+
+
+def test_pending_is_clamped():
+    case = _case(Q=3)
+    rows = case["record_rows"]
+    live = rows >= 0
+    case["pending"][rows[live]] = case["RQ"]
+    a = _run(case)
+    case["pending"][rows[live]] = case["RQ"] + 5
+    b = _run(case)
+    np.testing.assert_array_equal(a["state"], b["state"])
+    np.testing.assert_array_equal(a["out"], b["out"])
+    case["pending"][:] = -4
+    c = _run(case)
+    np.testing.assert_array_equal(c["state"], case["state"])
+
+
+def test_inert_and_recordless_rows():
+    case = _case(B=8, padding_frac=0.25, no_record_frac=0.25)
+    after = _run(case)
+    slots, rows = case["state_slots"], case["record_rows"]
+    Q = case["Q"]
+    for b in range(case["B"]):
+        tok = slice(b * Q, (b + 1) * Q)
+        if slots[b] <= 0:
+            np.testing.assert_array_equal(after["out"][tok], 0)
+        if rows[b] < 0 and slots[b] > 0:
+            # no record row: no replay, checkpoint untouched
+            np.testing.assert_array_equal(after["state"][slots[b]], case["state"][slots[b]])
+    # record rows not referenced by a live request are never written
+    used = set(int(r) for b, r in enumerate(rows) if r >= 0 and slots[b] > 0)
+    for r in range(case["corr"].shape[0]):
+        if r not in used:
+            np.testing.assert_array_equal(after["corr"][r], case["corr"][r])
+            np.testing.assert_array_equal(after["key_gate"][r], case["key_gate"][r])
+
+
+def test_fused_step_equals_commit_then_verify():
+    # One step of replay + verify == the commit of the pending tokens
+    # (in place, FP32) followed by the stock verify of the new window.
+    case = _case(B=5, H=2, Q=4, K=16, V=12)
+    fused = _run(case)
+    split = {key: (val.copy() if isinstance(val, np.ndarray) else val) for key, val in case.items()}
+    rows = split["record_rows"]
+    lens = np.array([split["pending"][r] if r >= 0 else 0 for r in rows], dtype=np.int32)
+    layer = dict(state=split["state"], corr=split["corr"], key_gate=split["key_gate"])
+    ko.commit(layers=[layer], A_log=split["A_log"][None], dt_bias=split["dt_bias"][None],
+              sources=split["state_slots"], commit_lens=np.minimum(lens, split["RQ"]),
+              destinations=split["state_slots"], lower_bound=split["lower_bound"],
+              Q=split["RQ"], B=split["B"], H=split["H"], record_rows=rows)
+    verified = _run(split, pending=False)
+    np.testing.assert_allclose(verified["state"], fused["state"], rtol=0, atol=1e-6)
+    np.testing.assert_allclose(ko.bf16_to_f64(verified["out"]), ko.bf16_to_f64(fused["out"]),
+                               rtol=1e-2, atol=1e-2)
+    np.testing.assert_allclose(verified["corr"], fused["corr"], rtol=1e-5, atol=1e-5)
+    np.testing.assert_array_equal(verified["key_gate"], fused["key_gate"])
+
+
+def test_deferred_then_flushed_equals_eager_commit():
+    # Step 1 verifies (records written, checkpoint kept); sampling accepts a_b
+    # tokens.  Eager: commit a_b now.  Deferred: defer (pending <- a_b), then
+    # the flush plan and the same commit in place.  The states must agree
+    # bit-exactly, the integer arrays too.
+    case = _case(B=6, H=2, Q=4, K=8, V=8, no_record_frac=0.2, padding_frac=0.2)
+    step1 = _run(case, pending=False)
+    rng = np.random.default_rng(2)
+    B, Q = case["B"], case["Q"]
+    accepted = rng.integers(0, Q + 1, size=B).astype(np.int32)
+    slots, rows = case["state_slots"], case["record_rows"]
+
+    eager_state = step1["state"].copy()
+    eager_lens = np.where((rows >= 0) & (slots > 0), accepted, 0).astype(np.int32)
+    ko.commit(layers=[dict(state=eager_state, corr=step1["corr"], key_gate=step1["key_gate"])],
+              A_log=case["A_log"][None], dt_bias=case["dt_bias"][None], sources=slots,
+              commit_lens=eager_lens, destinations=slots, lower_bound=case["lower_bound"],
+              Q=Q, B=B, H=case["H"], record_rows=rows)
+
+    pending = np.full(case["pending"].shape, 77, dtype=np.int32)
+    lens = accepted.copy()
+    ko.defer_commit(state_slots=slots, commit_lens=lens, record_rows=rows, pending=pending, B=B)
+    live = (rows >= 0) & (slots > 0)
+    np.testing.assert_array_equal(lens[live], 0)
+    np.testing.assert_array_equal(pending[rows[live]], accepted[live])
+    plan = dict(commit_lens=np.zeros(B, np.int32), final_slots=np.zeros(B, np.int32),
+                boundary_slots=np.ones(B, np.int32), boundary_lens=np.ones(B, np.int32))
+    ko.flush_plan(state_slots=slots, record_rows=rows, pending=pending, B=B, Q=Q, **plan)
+    np.testing.assert_array_equal(plan["commit_lens"], eager_lens)
+    np.testing.assert_array_equal(plan["final_slots"], slots)
+    deferred_state = step1["state"].copy()
+    ko.commit(layers=[dict(state=deferred_state, corr=step1["corr"], key_gate=step1["key_gate"])],
+              A_log=case["A_log"][None], dt_bias=case["dt_bias"][None], sources=slots,
+              commit_lens=plan["commit_lens"], destinations=plan["final_slots"],
+              boundaries=plan["boundary_slots"], boundary_lens=plan["boundary_lens"],
+              lower_bound=case["lower_bound"], Q=Q, B=B, H=case["H"], record_rows=rows)
+    np.testing.assert_array_equal(deferred_state, eager_state)
+    # ... and the fused step from the deferred checkpoint replays the same
+    nxt = dict(step1)
+    nxt["state"] = step1["state"].copy()
+    nxt["pending"] = pending
+    fused = _run(nxt)
+    for b in range(B):
+        if live[b] and accepted[b] > 0:
+            np.testing.assert_allclose(fused["state"][slots[b]], eager_state[slots[b]],
+                                       rtol=0, atol=1e-6)
+
+
+def test_commit_skips_dead_rows_and_writes_boundary():
+    c = synth.commit_case(L=2, B=12, H=2, Q=4, slots=40, seed=5, K=8, V=8,
+                          state_dtype="f32", boundary_frac=0.5)
+    layers = [{k: v.copy() for k, v in lay.items()} for lay in c["layers"]]
+    ko.commit(layers=layers, A_log=c["A_log"], dt_bias=c["dt_bias"], sources=c["sources"],
+              commit_lens=c["commit_lens"], destinations=c["destinations"],
+              boundaries=c["boundaries"], boundary_lens=c["boundary_lens"],
+              lower_bound=c["lower_bound"], Q=c["Q"], B=c["B"], H=c["H"])
+    written = set()
+    for b in range(c["B"]):
+        n, src, dst = c["commit_lens"][b], c["sources"][b], c["destinations"][b]
+        if n > 0 and src > 0 and dst > 0:
+            written.add(int(dst))
+            if c["boundary_lens"][b] > 0 and c["boundaries"][b] > 0:
+                written.add(int(c["boundaries"][b]))
+                for l, lay in enumerate(layers):
+                    for h in range(c["H"]):
+                        m = min(int(c["boundary_lens"][b]), int(n))
+                        src_page = c["layers"][l]["state"][src, h].astype(np.float64)
+                        ref = ko.replay_closed_form(
+                            src_page, c["layers"][l]["corr"][b, h, :m].astype(np.float64),
+                            ko.bf16_to_f64(c["layers"][l]["key_gate"][b, h, :m, :8]),
+                            ko.bf16_to_f64(c["layers"][l]["key_gate"][b, h, :m, 8:]), m,
+                            float(c["A_log"][l, h]), c["dt_bias"][l, h].astype(np.float64),
+                            c["lower_bound"])
+                        np.testing.assert_allclose(lay["state"][c["boundaries"][b], h], ref,
+                                                   rtol=1e-6, atol=1e-7)
+    for l, lay in enumerate(layers):
+        for s in range(lay["state"].shape[0]):
+            if s not in written:
+                np.testing.assert_array_equal(lay["state"][s], c["layers"][l]["state"][s])
+
+
+# ---------------------------------------------------------------------------
+# bookkeeping, against the hand-worked fixture
+# ---------------------------------------------------------------------------
+
+def test_bookkeeping_hand_worked():
+    g = json.load(open(os.path.join(GOLDEN, "bookkeeping_hand.json")))
+    d = g["defer"]
+    for eager, key in ((np.array(d["eager"], np.uint8), "expect_eager"), (None, "expect_no_eager")):
+        pending = np.array(d["pending"], np.int32)
+        lens = np.array(d["commit_lens"], np.int32)
+        ko.defer_commit(state_slots=np.array(d["state_slots"], np.int32), commit_lens=lens,
+                        record_rows=np.array(d["record_rows"], np.int32), pending=pending,
+                        B=len(lens), eager=eager)
+        np.testing.assert_array_equal(pending, d[key]["pending"])
+        np.testing.assert_array_equal(lens, d[key]["commit_lens"])
+    f = g["flush"]
+    B = len(f["state_slots"])
+    plan = {k: np.full(B, 99, np.int32) for k in f["expect"]}
+    ko.flush_plan(state_slots=np.array(f["state_slots"], np.int32),
+                  record_rows=np.array(f["record_rows"], np.int32),
+                  pending=np.array(f["pending"], np.int32), B=B, Q=f["Q"], **plan)
+    for k, v in f["expect"].items():
+        np.testing.assert_array_equal(plan[k], v)
