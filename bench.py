@@ -1,0 +1,409 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused KDA RecoverSSM replay + verify step on GB300.
+
+One step = one kda_replay_verify launch over the large-batch workload
+(H=64 heads, B=512 requests, Q=8 verified tokens each, FP32 state pool of
+1024 slots, pending ~ U{0..8}, 5% padding rows) with every input resident
+in HBM.  Prints one JSON line (rank 0):
+
+  value       verify tokens/s (live requests x Q per step / time), summed
+              over ranks (replicas: each GPU runs its own copy)
+  roofline    algorithmic bytes of one launch / its CUDA-event duration,
+              against the measured HBM copy bandwidth
+  e2e         the same metric through the C ABI with the step's inputs in
+              pinned host memory: per step the activations and request
+              metadata are copied in and the outputs copied out
+  cpu_baseline the FP64 oracle on a bounded sample of the same items, on
+              one host core
+
+`--impl reference` times the oracle alone (one core, a bounded sample of
+items per step) and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import os
+
+# the oracle baseline runs on exactly one core
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "replay-verify-f32-h64-b512-q8"
+METRIC = "fused replay+verify tokens/s and state HBM GB/s (% of GB300 peak), 1 GPU"
+DIM = 128
+
+
+# ---------------------------------------------------------------------------
+# algorithmic traffic of one step (bytes that must cross HBM at least once)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(case):
+    """Bytes one replay + verify launch must move, from the workload itself.
+
+    Per live item (request b with a live slot, head h): the 64 KB FP32 state
+    page read; written back iff n > 0; n recorded corrections (512 B each)
+    and key/gate records (512 B each) read; this window's q, k, v, raw_g
+    (4 x Q x 256 B) and raw_beta (2 B per token) read; the outputs (Q x 256 B)
+    written; with a record row, Q corrections and Q key/gate records
+    (512 + 512 B per token) written.  Per inert item: its outputs (zeros)
+    written.  Plus the per-request indices and the per-head gate
+    parameters, read once.
+    """
+    B, H, Q, RQ = case["B"], case["H"], case["Q"], case["RQ"]
+    slots, rows, pending = case["state_slots"], case["record_rows"], case["pending"]
+    page = DIM * DIM * 4
+    total = 0
+    state = 0
+    live_items = 0
+    for b in range(B):
+        if slots[b] <= case["null_slot"]:
+            total += H * Q * DIM * 2
+            continue
+        rec = rows[b]
+        n = min(max(int(pending[rec]), 0), RQ) if rec >= 0 else 0
+        per = page + (page if n > 0 else 0)
+        state += H * per
+        per += n * (DIM * 4 + 2 * DIM * 2)
+        per += 4 * Q * DIM * 2 + Q * 2 + Q * DIM * 2
+        if rec >= 0:
+            per += Q * (DIM * 4 + 2 * DIM * 2)
+        total += H * per
+        live_items += H
+    total += B * 4 * 2 + len(pending) * 0 + H * (4 + DIM * 4)
+    live_tokens = int((slots > case["null_slot"]).sum()) * Q
+    return dict(total=total, state=state, live_items=live_items, live_tokens=live_tokens)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                power.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_rate(case, seconds, seed=0):
+    """Times the FP64 oracle on a bounded random sample of live items; returns
+    (tokens/s equivalent of a whole step, items timed, seconds)."""
+    from oracle import kda_oracle as ko
+    B, H, Q = case["B"], case["H"], case["Q"]
+    live = np.flatnonzero(case["state_slots"] > case["null_slot"])
+    all_items = (live[:, None] * H + np.arange(H)[None, :]).ravel()
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(all_items)
+    state = case["state"]
+    corr, kg = case["corr"].copy(), case["key_gate"].copy()
+    out = np.zeros((0,), dtype=np.uint16)
+    done = 0
+    t0 = time.perf_counter()
+    chunk = 16
+    while done < len(order):
+        items = order[done:done + chunk]
+        saved = {}
+        for i in items:
+            b, h = divmod(int(i), H)
+            s = int(case["state_slots"][b])
+            saved[(s, h)] = state[s, h].copy()
+        out = np.zeros(case["v"].shape, dtype=np.uint16) if out.size == 0 else out
+        ko.replay_verify(q=case["q"], k=case["k"], v=case["v"], raw_g=case["raw_g"],
+                         raw_beta=case["raw_beta"], A_log=case["A_log"],
+                         dt_bias=case["dt_bias"], lower_bound=case["lower_bound"],
+                         q_scale=case["q_scale"], state=state, state_slots=case["state_slots"],
+                         record_rows=case["record_rows"], corr=corr, key_gate=kg, out=out,
+                         B=B, H=H, Q=Q, pending=case["pending"], items=items)
+        for (s, h), page in saved.items():  # leave the host pool as it was
+            state[s, h] = page
+        done += len(items)
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    live_tokens = len(live) * Q
+    step_equiv = dt * len(all_items) / done
+    return live_tokens / step_equiv, done, dt
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from linear_attention_speculative_recoverssm_gb300 import synth
+    case = synth.make(args.workload)
+    per_step = args.ref_step_seconds
+    for _ in range(args.warmup):
+        oracle_rate(case, per_step)
+    rates, items, secs = [], 0, 0.0
+    for i in range(args.steps):
+        r, n, dt = oracle_rate(case, per_step, seed=i + 1)
+        rates.append(r)
+        items += n
+        secs += dt
+    value = float(statistics.median(rates))
+    ab = algorithmic_bytes(case)
+    line = dict(
+        impl="reference", metric=METRIC, value=value, unit="tok/s", n_gpus=args.gpus,
+        steps=args.steps, warmup=args.warmup,
+        ms_per_step=1e3 * ab["live_tokens"] / value, higher_is_better=True,
+        scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+        config=workload_config(case, args.workload),
+        cpu_baseline=dict(value=value, unit="tok/s", cores=1, kind="oracle",
+                          sample=f"{items} random live (request, head) items over "
+                                 f"{args.steps} steps ({secs:.1f} s of FP64 numpy on one core), "
+                                 "scaled to the whole step"),
+        e2e=dict(value=value, unit="tok/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+    )
+    print(json.dumps(line))
+
+
+def workload_config(case, name):
+    return dict(workload=name, B=case["B"], H=case["H"], Q=case["Q"], RQ=case["RQ"],
+                state_slots=int(case["state"].shape[0]), state_dtype="f32", K=DIM, V=DIM,
+                padding_rows=int((case["state_slots"] <= case["null_slot"]).sum()),
+                l2="inputs larger than L2: ~2 GB of state pages touched per step vs 129 MB L2",
+                parallelism="replicas")
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from linear_attention_speculative_recoverssm_gb300 import kda_replay_verify, synth
+
+    case = synth.make(args.workload)
+    ab = algorithmic_bytes(case)
+
+    def dt(a, pin=False):
+        t = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
+             else torch.from_numpy(a))
+        return t.pin_memory() if pin else t.to(dev)
+
+    names = ("q", "k", "v", "raw_g", "raw_beta", "A_log", "dt_bias", "state", "state_slots",
+             "record_rows", "pending", "corr", "key_gate")
+    d = {n: dt(case[n]) for n in names}
+    out = torch.zeros(case["v"].shape, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    Q = case["Q"]
+
+    def step(dd):
+        kda_replay_verify(dd["q"], dd["k"], dd["v"], dd["raw_g"], dd["raw_beta"], d["A_log"],
+                          d["dt_bias"], d["state"], dd["state_slots"], dd["record_rows"],
+                          d["pending"], d["corr"], d["key_gate"], dd["out"], Q=Q,
+                          lower_bound=case["lower_bound"], q_scale=case["q_scale"], split=1,
+                          status=status, stream=stream)
+
+    dd = dict(d, out=out)
+    for _ in range(args.warmup):
+        step(dd)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    sampler.start()
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev_s[i].record(stream)
+        step(dd)
+        ev_e[i].record(stream)
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in zip(ev_s, ev_e)]
+    avg_kernel_ms = sum(kern_ms) / len(kern_ms)
+
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = ab["live_tokens"] * world * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the C ABI, inputs from pinned host memory ----
+    e2e = None
+    if not args.no_e2e:
+        host_names = ("q", "k", "v", "raw_g", "raw_beta", "state_slots", "record_rows")
+        host = {n: dt(case[n], pin=True) for n in host_names}
+        dev_in = {n: torch.empty_like(host[n], device=dev) for n in host_names}
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        de = dict(dev_in, out=out)
+
+        def e2e_step():
+            for n in host_names:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            step(de)
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = dict(value=ab["live_tokens"] * world * args.steps / (e_ms / 1e3), unit="tok/s",
+                   h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h))
+
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = ab["total"] / (avg_kernel_ms / 1e3) / 1e9
+    state_gbs = ab["state"] / (avg_kernel_ms / 1e3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, items, secs = oracle_rate(case, args.cpu_seconds)
+        cpu = dict(value=rate, unit="tok/s", cores=1, kind="oracle",
+                   sample=f"{items} random live (request, head) items of this workload "
+                          f"({secs:.1f} s of FP64 numpy on one core), scaled to the whole step")
+
+    if rank == 0:
+        line = dict(
+            metric=METRIC, value=value, unit="tok/s", n_gpus=world, steps=args.steps,
+            warmup=args.warmup, ms_per_step=total_ms / args.steps, higher_is_better=True,
+            scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
+            config=workload_config(case, args.workload),
+            state_gbs=state_gbs, algorithmic_gbs=achieved,
+            hbm_frac=achieved / peak,
+            kernel_ms=avg_kernel_ms,
+            roofline=dict(bound="hbm", achieved=achieved, peak=peak, unit="GB/s",
+                          frac=achieved / peak, traffic=args.traffic,
+                          peak_source="MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks
+                          else "fallback 6.8 TB/s",
+                          bytes_per_launch=ab["total"], state_bytes_per_launch=ab["state"]),
+            cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps, clocks=clocks,
+        )
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=1.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the current kernel, if measured")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

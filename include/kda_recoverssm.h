@@ -1,0 +1,221 @@
+/*
+ * kda_recoverssm.h -- C ABI of libkda_recoverssm.so, the GB300 (sm_103a)
+ * KDA RecoverSSM step of speculative decoding: replay the accepted tokens of
+ * the previous window into the checkpoint state, verify this window's draft
+ * tokens in chunked (WY) form, write the checkpoint back at most once and
+ * store the new records.
+ *
+ * Sources (page titles of the vLLM kimi_k3 documentation):
+ *  - "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.fused"
+ *    (module docstring: deferred RecoverSSM steps 1-3, precision and layout
+ *    notes; class KdaFused and its decay / quad_sum helpers);
+ *  - "vllm.models.kimi_k3.nvidia.recoverssm.cutedsl.commit" (module
+ *    docstring: the closed-form commit and the align boundary state; class
+ *    KdaCommit: its argument list);
+ *  - "vllm.models.kimi_k3.nvidia.specialized_decode.recoverssm.kernels"
+ *    (kda_recoverssm_verify and its argument checks; _defer_commit_kernel;
+ *    _prepare_flush_plan_kernel).
+ *
+ * Conventions shared by every entry point
+ *  - K = V = 128 (key and value channels per head).  Other sizes return
+ *    KDA_ERR_UNSUPPORTED.
+ *  - Every pointer is DEVICE memory owned by the caller.  The library never
+ *    allocates, frees or synchronises; each call enqueues its kernels on
+ *    `stream` (a cudaStream_t passed as void*, NULL = the legacy default
+ *    stream) and returns at once.
+ *  - BF16 tensors are passed as raw bit patterns (kda_bf16, uint16_t).
+ *  - Activations are token-major: token b*Q + t belongs to request b.
+ *  - A state slot is inert when slot <= null_slot (the pages use 0).  A
+ *    record row < 0 means the request has none.
+ *  - Live slots, destinations, boundary slots and record rows must be
+ *    pairwise distinct across the requests of one call (the pages leave
+ *    duplicates undefined).
+ *  - `status` (nullable) is a device int32.  The caller sets it to 0; a
+ *    kernel that meets an index outside its pool (slot >= n_slots, row >=
+ *    n_rows), a misaligned per-layer address or a device wait that gave up
+ *    writes the first such error code there (KDA_ERR_ARG, KDA_ERR_ALIGN,
+ *    KDA_ERR_TIMEOUT) and skips the offending item instead of faulting.
+ *  - Host-side checks return before anything is launched:
+ *      KDA_ERR_ARG          a required pointer is NULL, or a size / count /
+ *                           window / split is out of range;
+ *      KDA_ERR_ALIGN        a pointer is not 16-byte aligned, or a slot /
+ *                           row stride is not a multiple of 16 bytes;
+ *      KDA_ERR_UNSUPPORTED  unknown state dtype, or K / V != 128;
+ *      KDA_ERR_CUDA         the launch itself failed.
+ *  - B == 0 is a no-op that returns KDA_OK (the stock wrapper returns early
+ *    on zero tokens).
+ */
+#ifndef KDA_RECOVERSSM_H
+#define KDA_RECOVERSSM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_OK 0
+#define KDA_ERR_ARG (-1)
+#define KDA_ERR_ALIGN (-2)
+#define KDA_ERR_UNSUPPORTED (-3)
+#define KDA_ERR_CUDA (-4)
+#define KDA_ERR_TIMEOUT (-5)
+
+#define KDA_STATE_F32 0
+#define KDA_STATE_BF16 1
+
+#define KDA_HEAD_DIM 128
+#define KDA_MAX_WINDOW 8
+
+typedef uint16_t kda_bf16;
+
+/* Version of this ABI (bumped on any signature change). */
+int kda_abi_version(void);
+
+/* A static, human-readable name for a status code. */
+const char *kda_error_string(int status);
+
+/*
+ * kda_verify -- the stock RecoverSSM verify of one window, from the
+ * checkpoint, which it never writes ("Verify a KDA speculative window
+ * without modifying its checkpoint", kda_recoverssm_verify).
+ *
+ * Per (request b, head h) with slot = state_slots[b] > null_slot and
+ * S = state_pool[slot, h] ([V=128 rows, K=128 columns]), for t < Q:
+ *   d_t  = exp(lower_bound * sigmoid(exp(A_log[h]) * (raw_g_t + dt_bias[h])))
+ *   kn_t = k_t * rsqrt(sum k_t^2 + 1e-6)
+ *   qn_t = q_t * rsqrt(sum q_t^2 + 1e-6) * q_scale
+ *   S <- S diag(d_t); u_t = sigmoid(raw_beta_t) (v_t - S kn_t);
+ *   S <- S + u_t kn_t^T; o_t = S qn_t
+ * computed in the equivalent chunked form of the "kda.fused" page (step 2):
+ * the state is only read.  Writes out[b*Q + t, h, :] = BF16(o_t) and, when
+ * the record row r (record_rows[b], or b when record_rows is NULL) is >= 0,
+ * corr[r, h, t, :] = u_t (FP32), key_gate[r, h, t, 0:128] = k_t and
+ * key_gate[r, h, t, 128:256] = raw_g_t (BF16 copies).  Inert requests
+ * write zeros to `out` only.
+ *
+ *   q, k, raw_g   [B*Q, H, 128] BF16;  v [B*Q, H, 128] BF16
+ *   raw_beta      [B*Q, H] BF16
+ *   A_log [H] FP32; dt_bias [H, 128] FP32
+ *   state_pool    [n_slots, H, 128, 128] of state_dtype, slot stride
+ *                 `slot_stride` elements (>= H*128*128)
+ *   state_slots   [B] int32; record_rows [B] int32 or NULL
+ *   corr          [n_rows, H, rq, 128] FP32, row stride corr_row_stride
+ *   key_gate      [n_rows, H, rq, 256] BF16, row stride kg_row_stride
+ *   out           [B*Q, H, 128] BF16
+ *   1 <= Q <= rq <= 8; H >= 1.
+ */
+int kda_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+               const kda_bf16 *raw_g, const kda_bf16 *raw_beta,
+               const float *A_log, const float *dt_bias, float lower_bound,
+               float q_scale, const void *state_pool, int state_dtype,
+               int64_t slot_stride, int n_slots, const int32_t *state_slots,
+               const int32_t *record_rows, float *corr, kda_bf16 *key_gate,
+               int64_t corr_row_stride, int64_t kg_row_stride, int n_rows,
+               int rq, kda_bf16 *out, int B, int H, int Q, int null_slot,
+               int32_t *status, void *stream);
+
+/*
+ * kda_replay_verify -- the fused deferred RecoverSSM step ("kda.fused" page,
+ * module docstring steps 1-3; class KdaFused).  Per (request b, head h) with
+ * slot = state_slots[b] > null_slot, r = record_rows[b] and
+ * n = r >= 0 ? clamp(pending[r], 0, rq) : 0:
+ *  1. S_n = S_0 diag(D_n) + sum_{t<n} u_t (kn_t * P_t)^T from the request's
+ *     records (u_t = corr[r, h, t, :], kn_t the normalised recorded key,
+ *     d_t the decay of the recorded raw gate, D_n = prod_{s<n} d_s,
+ *     P_t = prod_{t<s<n} d_s), written back to state_pool[slot, h] iff n > 0;
+ *     with boundary_slots given and m = boundary_lens[b] > 0,
+ *     boundary_slots[b] > null_slot and n > 0, S_min(m, n) is also written
+ *     to state_pool[boundary_slots[b], h] (the commit page's align state);
+ *  2. the chunked verify of this window from S_n, exactly as kda_verify;
+ *  3. the new records, after every old record of the item has been read.
+ * `pending` is only read (the defer step after sampling writes it).
+ * `state_pool` is FP32.  split = 0 picks the launch shape; 1 is one
+ * persistent CTA per SM streaming whole items; 2 or 4 splits each item's
+ * rows across a thread-block cluster of that many CTAs (for small batches),
+ * whose key-norm and pair-product partial sums are exchanged through
+ * distributed shared memory.
+ */
+int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                      const kda_bf16 *raw_g, const kda_bf16 *raw_beta,
+                      const float *A_log, const float *dt_bias,
+                      float lower_bound, float q_scale, float *state_pool,
+                      int64_t slot_stride, int n_slots,
+                      const int32_t *state_slots, const int32_t *record_rows,
+                      const int32_t *pending, float *corr, kda_bf16 *key_gate,
+                      int64_t corr_row_stride, int64_t kg_row_stride,
+                      int n_rows, int rq, const int32_t *boundary_slots,
+                      const int32_t *boundary_lens, kda_bf16 *out, int B,
+                      int H, int Q, int null_slot, int split, int32_t *status,
+                      void *stream);
+
+/*
+ * kda_commit -- the standalone closed-form commit over L layers (commit
+ * page; KdaCommit argument list).  Per (layer l, request b, head h) with
+ * n = min(commit_lens[b], Q), src = sources[b], dst = destinations[b],
+ * r = record_rows[b] (or b when record_rows is NULL) and
+ * live = n > 0 && src > null_slot && dst > null_slot && r >= 0:
+ *   dst page <- S_n of the src page replayed from record row r (as in
+ *   kda_replay_verify step 1), rounded once to the state dtype;
+ *   with boundaries given, m = min(boundary_lens[b], Q) > 0 and
+ *   boundaries[b] > null_slot: boundary page <- S_min(m, n).
+ * Nothing is written for a request that is not live.  dst == src commits in
+ * place.
+ *
+ *   state_ptrs, corr_ptrs, kg_ptrs  [L] device tables of device addresses
+ *                 (uint64) of layer l's state pool [slots, H, 128, 128],
+ *                 corrections [rows, H, Q, 128] FP32 and key/gate records
+ *                 [rows, H, Q, 256] BF16; each address 16-byte aligned
+ *   state_strides, corr_strides, kg_strides  [L] device int64 tables:
+ *                 elements per slot / per record row
+ *   A_log [L, H], dt_bias [L, H, 128] FP32
+ *   sources, commit_lens, destinations [B] int32
+ *   boundaries, boundary_lens [B] int32 or both NULL (align off)
+ *   record_rows [B] int32 or NULL
+ *   state_dtype KDA_STATE_BF16 or KDA_STATE_F32; 1 <= Q <= 8.
+ */
+int kda_commit(const uint64_t *state_ptrs, const uint64_t *corr_ptrs,
+               const uint64_t *kg_ptrs, const int64_t *state_strides,
+               const int64_t *corr_strides, const int64_t *kg_strides,
+               const float *A_log, const float *dt_bias,
+               const int32_t *sources, const int32_t *commit_lens,
+               const int32_t *destinations, const int32_t *boundaries,
+               const int32_t *boundary_lens, const int32_t *record_rows,
+               int state_dtype, float lower_bound, int null_slot, int L, int H,
+               int B, int Q, int n_slots, int n_rows, int32_t *status,
+               void *stream);
+
+/*
+ * kda_defer_commit -- after sampling, per request b (_defer_commit_kernel):
+ * if record_rows[b] < 0 or state_slots[b] <= null_slot nothing changes;
+ * else if eager && eager[b] != 0: pending[record_rows[b]] = 0 and the
+ * commit length is kept (the row is committed now); otherwise
+ * pending[record_rows[b]] = commit_lens[b] and commit_lens[b] = 0.
+ * eager [B] uint8 or NULL.  Record rows >= n_rows are reported in status
+ * and skipped.
+ */
+int kda_defer_commit(const int32_t *state_slots, int32_t *commit_lens,
+                     const int32_t *record_rows, int32_t *pending,
+                     const uint8_t *eager, int B, int null_slot, int n_rows,
+                     int32_t *status, void *stream);
+
+/*
+ * kda_flush_plan -- the in-place commit plan of the pending replays
+ * (_prepare_flush_plan_kernel), per request b:
+ *   len = record_rows[b] >= 0 ? pending[record_rows[b]] : 0, clamped to
+ *   [0, Q]; commit_lens[b] = (state_slots[b] > null_slot && len > 0) ? len
+ *   : 0; final_slots[b] = state_slots[b]; boundary_slots[b] = null_slot;
+ *   boundary_lens[b] = 0.
+ * `pending` is only read.
+ */
+int kda_flush_plan(const int32_t *state_slots, const int32_t *record_rows,
+                   const int32_t *pending, int32_t *commit_lens,
+                   int32_t *final_slots, int32_t *boundary_slots,
+                   int32_t *boundary_lens, int B, int Q, int null_slot,
+                   int n_rows, int32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_RECOVERSSM_H */

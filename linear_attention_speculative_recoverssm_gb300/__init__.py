@@ -1,0 +1,27 @@
+"""GB300-native (sm_103a) KDA RecoverSSM step for speculative decoding.
+
+The compute lives in libkda_recoverssm.so (hand-written CUDA kernels behind a
+C ABI, declared in include/kda_recoverssm.h).  This package holds the build
+script (``_build``), the thin ctypes binding (``_lib``) and the seeded
+synthetic-input generator (``synth``).  Calling any entry point without the
+built library raises ImportError; there is no CPU fallback.
+"""
+from ._lib import (  # noqa: F401
+    EXPORTS,
+    KDA_ERR_ALIGN,
+    KDA_ERR_ARG,
+    KDA_ERR_CUDA,
+    KDA_ERR_TIMEOUT,
+    KDA_ERR_UNSUPPORTED,
+    KDA_OK,
+    KDA_STATE_BF16,
+    KDA_STATE_F32,
+    KdaError,
+    kda_commit,
+    kda_defer_commit,
+    kda_flush_plan,
+    kda_replay_verify,
+    kda_verify,
+    layer_tables,
+    load,
+)

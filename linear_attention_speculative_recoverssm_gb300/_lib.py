@@ -1,0 +1,199 @@
+"""ctypes binding of libkda_recoverssm.so (argument marshalling only).
+
+Every function here takes torch tensors on the GPU, reads their data
+pointers, sizes and strides, and calls the C entry point of the same name on
+the current CUDA stream (or the given one).  All compute runs in the
+library's kernels; there is no fallback: if the library is missing, import
+fails with an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkda_recoverssm.so")
+
+# status codes (include/kda_recoverssm.h)
+KDA_OK = 0
+KDA_ERR_ARG = -1
+KDA_ERR_ALIGN = -2
+KDA_ERR_UNSUPPORTED = -3
+KDA_ERR_CUDA = -4
+KDA_ERR_TIMEOUT = -5
+KDA_STATE_F32 = 0
+KDA_STATE_BF16 = 1
+
+EXPORTS = ("kda_abi_version", "kda_error_string", "kda_verify", "kda_replay_verify",
+           "kda_commit", "kda_defer_commit", "kda_flush_plan")
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+
+_SIGS = {
+    "kda_abi_version": ([], _I),
+    "kda_error_string": ([_I], ctypes.c_char_p),
+    "kda_verify": ([_P] * 7 + [_F, _F, _P, _I, _I64, _I, _P, _P, _P, _P, _I64, _I64, _I, _I,
+                    _P, _I, _I, _I, _I, _P, _P], _I),
+    "kda_replay_verify": ([_P] * 7 + [_F, _F, _P, _I64, _I, _P, _P, _P, _P, _P, _I64, _I64,
+                           _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "kda_commit": ([_P] * 14 + [_I, _F, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "kda_defer_commit": ([_P] * 5 + [_I, _I, _I, _P, _P], _I),
+    "kda_flush_plan": ([_P] * 7 + [_I, _I, _I, _I, _P, _P], _I),
+}
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library once; raise ImportError if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(
+            f"{p} is missing: build it with `python -m "
+            "linear_attention_speculative_recoverssm_gb300._build` "
+            "(or __graft_entry__.build())")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn, code):
+        msg = load().kda_error_string(code).decode()
+        super().__init__(f"{fn} returned {code} ({msg})")
+        self.code = code
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, code, raise_on_error):
+    if code != KDA_OK and raise_on_error:
+        raise KdaError(fn, code)
+    return code
+
+
+def _expect(t, dtype, name):
+    if t is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check_step_dtypes(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_slots, record_rows,
+                       corr, key_gate, out):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("raw_g", raw_g), ("raw_beta", raw_beta),
+                    ("key_gate", key_gate), ("out", out)):
+        _expect(t, torch.bfloat16, name)
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias), ("corr", corr)):
+        _expect(t, torch.float32, name)
+    for name, t in (("state_slots", state_slots), ("record_rows", record_rows)):
+        _expect(t, torch.int32, name)
+
+
+def kda_verify(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, state_slots, corr,
+               key_gate, out, *, Q, lower_bound, q_scale, record_rows=None, null_slot=0,
+               status=None, stream=None, raise_on_error=True):
+    """Stock verify of one window (state read only).  Shapes as in
+    include/kda_recoverssm.h; state_pool is float32 or bfloat16."""
+    import torch
+    _check_step_dtypes(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_slots, record_rows,
+                       corr, key_gate, out)
+    dtype = KDA_STATE_F32 if state_pool.dtype == torch.float32 else KDA_STATE_BF16
+    if state_pool.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("state_pool must be float32 or bfloat16")
+    B = state_slots.shape[0]
+    H = q.shape[1]
+    rc = load().kda_verify(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(raw_g), _ptr(raw_beta), _ptr(A_log), _ptr(dt_bias),
+        lower_bound, q_scale, _ptr(state_pool), dtype, state_pool.stride(0),
+        state_pool.shape[0], _ptr(state_slots), _ptr(record_rows), _ptr(corr), _ptr(key_gate),
+        corr.stride(0), key_gate.stride(0), corr.shape[0], corr.shape[2], _ptr(out), B, H, Q,
+        null_slot, _ptr(status), _stream(stream))
+    return _check("kda_verify", rc, raise_on_error)
+
+
+def kda_replay_verify(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, state_slots,
+                      record_rows, pending, corr, key_gate, out, *, Q, lower_bound, q_scale,
+                      boundary_slots=None, boundary_lens=None, null_slot=0, split=0,
+                      status=None, stream=None, raise_on_error=True):
+    """Fused replay + verify (FP32 state pool, written in place)."""
+    import torch
+    _check_step_dtypes(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_slots, record_rows,
+                       corr, key_gate, out)
+    _expect(state_pool, torch.float32, "state_pool")
+    _expect(pending, torch.int32, "pending")
+    B = state_slots.shape[0]
+    H = q.shape[1]
+    rc = load().kda_replay_verify(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(raw_g), _ptr(raw_beta), _ptr(A_log), _ptr(dt_bias),
+        lower_bound, q_scale, _ptr(state_pool), state_pool.stride(0), state_pool.shape[0],
+        _ptr(state_slots), _ptr(record_rows), _ptr(pending), _ptr(corr), _ptr(key_gate),
+        corr.stride(0), key_gate.stride(0), corr.shape[0], corr.shape[2],
+        _ptr(boundary_slots), _ptr(boundary_lens), _ptr(out), B, H, Q, null_slot, split,
+        _ptr(status), _stream(stream))
+    return _check("kda_replay_verify", rc, raise_on_error)
+
+
+def kda_commit(state_ptrs, corr_ptrs, kg_ptrs, state_strides, corr_strides, kg_strides, A_log,
+               dt_bias, sources, commit_lens, destinations, *, state_dtype, lower_bound, L, H,
+               B, Q, n_slots, n_rows, boundaries=None, boundary_lens=None, record_rows=None,
+               null_slot=0, status=None, stream=None, raise_on_error=True):
+    """Standalone commit over L layers; the six tables are device int64
+    tensors of [L] addresses / strides (see layer_tables)."""
+    rc = load().kda_commit(
+        _ptr(state_ptrs), _ptr(corr_ptrs), _ptr(kg_ptrs), _ptr(state_strides),
+        _ptr(corr_strides), _ptr(kg_strides), _ptr(A_log), _ptr(dt_bias), _ptr(sources),
+        _ptr(commit_lens), _ptr(destinations), _ptr(boundaries), _ptr(boundary_lens),
+        _ptr(record_rows), state_dtype, lower_bound, null_slot, L, H, B, Q, n_slots, n_rows,
+        _ptr(status), _stream(stream))
+    return _check("kda_commit", rc, raise_on_error)
+
+
+def layer_tables(states, corrs, key_gates, device):
+    """The per-layer address and stride tables kda_commit reads, as device
+    int64 tensors: (state_ptrs, corr_ptrs, kg_ptrs, state_strides,
+    corr_strides, kg_strides)."""
+    import torch
+    mk = lambda xs: torch.tensor(xs, dtype=torch.int64, device=device)
+    return (mk([s.data_ptr() for s in states]), mk([c.data_ptr() for c in corrs]),
+            mk([g.data_ptr() for g in key_gates]), mk([s.stride(0) for s in states]),
+            mk([c.stride(0) for c in corrs]), mk([g.stride(0) for g in key_gates]))
+
+
+def kda_defer_commit(state_slots, commit_lens, record_rows, pending, *, eager=None, null_slot=0,
+                     status=None, stream=None, raise_on_error=True):
+    rc = load().kda_defer_commit(
+        _ptr(state_slots), _ptr(commit_lens), _ptr(record_rows), _ptr(pending), _ptr(eager),
+        state_slots.shape[0], null_slot, pending.shape[0], _ptr(status), _stream(stream))
+    return _check("kda_defer_commit", rc, raise_on_error)
+
+
+def kda_flush_plan(state_slots, record_rows, pending, commit_lens, final_slots, boundary_slots,
+                   boundary_lens, *, Q, null_slot=0, status=None, stream=None,
+                   raise_on_error=True):
+    rc = load().kda_flush_plan(
+        _ptr(state_slots), _ptr(record_rows), _ptr(pending), _ptr(commit_lens),
+        _ptr(final_slots), _ptr(boundary_slots), _ptr(boundary_lens), state_slots.shape[0], Q,
+        null_slot, pending.shape[0], _ptr(status), _stream(stream))
+    return _check("kda_flush_plan", rc, raise_on_error)

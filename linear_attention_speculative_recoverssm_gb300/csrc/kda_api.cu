@@ -1,0 +1,253 @@
+// C ABI of libkda_recoverssm.so: argument checks (after the stock wrapper
+// kda_recoverssm_verify on page "vllm.models.kimi_k3.nvidia.
+// specialized_decode.recoverssm.kernels"), launch-shape choice, dispatch to
+// the kernels.  No allocation, no synchronisation, no CPU fallback.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "../../include/kda_recoverssm.h"
+#include "kda_launch.h"
+#include "kda_step.cuh"
+
+namespace kda {
+
+int launch_step_q1(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_q2(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_q3(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_q4(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_q5(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_q6(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_q7(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_q8(const StepParams &, int, int, int, cudaStream_t);
+
+namespace {
+std::atomic<int> g_sm_count[64];
+}
+
+int device_sm_count(int dev) {
+  const int slot = dev & 63;
+  int v = g_sm_count[slot].load();
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 1;
+    g_sm_count[slot].store(v);
+  }
+  return v;
+}
+
+int launch_step(const StepParams &p, int n_items, int Q, int variant, int split,
+                cudaStream_t stream) {
+  switch (Q) {
+    case 1: return launch_step_q1(p, n_items, variant, split, stream);
+    case 2: return launch_step_q2(p, n_items, variant, split, stream);
+    case 3: return launch_step_q3(p, n_items, variant, split, stream);
+    case 4: return launch_step_q4(p, n_items, variant, split, stream);
+    case 5: return launch_step_q5(p, n_items, variant, split, stream);
+    case 6: return launch_step_q6(p, n_items, variant, split, stream);
+    case 7: return launch_step_q7(p, n_items, variant, split, stream);
+    case 8: return launch_step_q8(p, n_items, variant, split, stream);
+    default: return KDA_ERR_ARG;
+  }
+}
+
+}  // namespace kda
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by kda_verify and kda_replay_verify.
+int check_step_args(const void *q, const void *k, const void *v, const void *g,
+                    const void *beta, const void *A_log, const void *dt_bias,
+                    const void *state_pool, int state_bytes, int64_t slot_stride, int n_slots,
+                    const void *state_slots, const void *corr, const void *key_gate,
+                    int64_t corr_row_stride, int64_t kg_row_stride, int n_rows, int rq,
+                    const void *out, int B, int H, int Q) {
+  if (B < 0 || H < 1 || Q < 1 || Q > KDA_MAX_WINDOW || rq < Q || rq > KDA_MAX_WINDOW)
+    return KDA_ERR_ARG;
+  if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !state_pool || !state_slots ||
+      !corr || !key_gate || !out)
+    return KDA_ERR_ARG;
+  if (n_slots < 1 || n_rows < 0) return KDA_ERR_ARG;
+  if (slot_stride < (int64_t)H * KDA_HEAD_DIM * KDA_HEAD_DIM) return KDA_ERR_ARG;
+  if (corr_row_stride < (int64_t)H * rq * KDA_HEAD_DIM ||
+      kg_row_stride < (int64_t)H * rq * 2 * KDA_HEAD_DIM)
+    return KDA_ERR_ARG;
+  if ((long long)B * H > 0x7fffffffLL) return KDA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) ||
+      !aligned16(state_pool) || !aligned16(corr) || !aligned16(key_gate) || !aligned16(out) ||
+      !aligned16(dt_bias))
+    return KDA_ERR_ALIGN;
+  if (((slot_stride * state_bytes) & 15) != 0 || ((corr_row_stride * 4) & 15) != 0 ||
+      ((kg_row_stride * 2) & 15) != 0)
+    return KDA_ERR_ALIGN;
+  return KDA_OK;
+}
+
+kda::StepParams make_params(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                            const kda_bf16 *raw_g, const kda_bf16 *raw_beta, const float *A_log,
+                            const float *dt_bias, float lower_bound, float q_scale, void *state,
+                            int64_t slot_stride, int n_slots, const int32_t *state_slots,
+                            const int32_t *record_rows, const int32_t *pending, float *corr,
+                            kda_bf16 *key_gate, int64_t corr_row_stride, int64_t kg_row_stride,
+                            int n_rows, int rq, const int32_t *boundary_slots,
+                            const int32_t *boundary_lens, kda_bf16 *out, int B, int H,
+                            int null_slot, int32_t *status) {
+  kda::StepParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.g = raw_g;
+  p.beta = raw_beta;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.lower_bound = lower_bound;
+  p.q_scale = q_scale;
+  p.state = state;
+  p.slot_stride = slot_stride;
+  p.n_slots = n_slots;
+  p.state_slots = state_slots;
+  p.record_rows = record_rows;
+  p.pending = pending;
+  p.bnd_slots = boundary_slots;
+  p.bnd_lens = boundary_lens;
+  p.corr = corr;
+  p.kg = key_gate;
+  p.corr_row_stride = corr_row_stride;
+  p.kg_row_stride = kg_row_stride;
+  p.n_rows = n_rows;
+  p.rq = rq;
+  p.out = out;
+  p.B = B;
+  p.H = H;
+  p.null_slot = null_slot;
+  p.status = status;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return 1; }
+
+const char *kda_error_string(int status) {
+  switch (status) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_ARG: return "invalid argument";
+    case KDA_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case KDA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KDA_ERR_CUDA: return "CUDA launch failed";
+    case KDA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int kda_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *raw_g,
+               const kda_bf16 *raw_beta, const float *A_log, const float *dt_bias,
+               float lower_bound, float q_scale, const void *state_pool, int state_dtype,
+               int64_t slot_stride, int n_slots, const int32_t *state_slots,
+               const int32_t *record_rows, float *corr, kda_bf16 *key_gate,
+               int64_t corr_row_stride, int64_t kg_row_stride, int n_rows, int rq,
+               kda_bf16 *out, int B, int H, int Q, int null_slot, int32_t *status,
+               void *stream) {
+  if (state_dtype != KDA_STATE_F32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_UNSUPPORTED;
+  const int sb = state_dtype == KDA_STATE_F32 ? 4 : 2;
+  int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, sb,
+                           slot_stride, n_slots, state_slots, corr, key_gate, corr_row_stride,
+                           kg_row_stride, n_rows, rq, out, B, H, Q);
+  if (rc != KDA_OK) return rc;
+  if (B == 0) return KDA_OK;
+  const kda::StepParams p = make_params(
+      q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound, q_scale,
+      const_cast<void *>(state_pool), slot_stride, n_slots, state_slots, record_rows, nullptr,
+      corr, key_gate, corr_row_stride, kg_row_stride, n_rows, rq, nullptr, nullptr, out, B, H,
+      null_slot, status);
+  return kda::launch_step(p, B * H, Q, state_dtype == KDA_STATE_F32 ? 0 : 1, 1,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                      const kda_bf16 *raw_g, const kda_bf16 *raw_beta, const float *A_log,
+                      const float *dt_bias, float lower_bound, float q_scale, float *state_pool,
+                      int64_t slot_stride, int n_slots, const int32_t *state_slots,
+                      const int32_t *record_rows, const int32_t *pending, float *corr,
+                      kda_bf16 *key_gate, int64_t corr_row_stride, int64_t kg_row_stride,
+                      int n_rows, int rq, const int32_t *boundary_slots,
+                      const int32_t *boundary_lens, kda_bf16 *out, int B, int H, int Q,
+                      int null_slot, int split, int32_t *status, void *stream) {
+  int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, 4, slot_stride,
+                           n_slots, state_slots, corr, key_gate, corr_row_stride, kg_row_stride,
+                           n_rows, rq, out, B, H, Q);
+  if (rc != KDA_OK) return rc;
+  if (!record_rows || !pending) return KDA_ERR_ARG;
+  if ((boundary_slots == nullptr) != (boundary_lens == nullptr)) return KDA_ERR_ARG;
+  if (split != 0 && split != 1 && split != 2 && split != 4) return KDA_ERR_ARG;
+  if (B == 0) return KDA_OK;
+  const int items = B * H;
+  if (split == 0) {
+    // Whole items on persistent CTAs when they fill the GPU; otherwise split
+    // each item's rows over a cluster so more SMs share the latency.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    const int sms = kda::device_sm_count(dev);
+    split = items >= sms ? 1 : (items * 4 <= 2 * sms ? 4 : 2);
+  }
+  if (split > 1 && items > 65535) split = 1;
+  const kda::StepParams p = make_params(
+      q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound, q_scale, state_pool, slot_stride,
+      n_slots, state_slots, record_rows, pending, corr, key_gate, corr_row_stride, kg_row_stride,
+      n_rows, rq, boundary_slots, boundary_lens, out, B, H, null_slot, status);
+  return kda::launch_step(p, items, Q, boundary_slots ? 3 : 2, split,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int kda_commit(const uint64_t *state_ptrs, const uint64_t *corr_ptrs, const uint64_t *kg_ptrs,
+               const int64_t *state_strides, const int64_t *corr_strides,
+               const int64_t *kg_strides, const float *A_log, const float *dt_bias,
+               const int32_t *sources, const int32_t *commit_lens, const int32_t *destinations,
+               const int32_t *boundaries, const int32_t *boundary_lens,
+               const int32_t *record_rows, int state_dtype, float lower_bound, int null_slot,
+               int L, int H, int B, int Q, int n_slots, int n_rows, int32_t *status,
+               void *stream) {
+  if (state_dtype != KDA_STATE_F32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_UNSUPPORTED;
+  if (L < 0 || H < 1 || B < 0 || Q < 1 || Q > KDA_MAX_WINDOW || n_slots < 1 || n_rows < 0)
+    return KDA_ERR_ARG;
+  if (!state_ptrs || !corr_ptrs || !kg_ptrs || !state_strides || !corr_strides || !kg_strides ||
+      !A_log || !dt_bias || !sources || !commit_lens || !destinations)
+    return KDA_ERR_ARG;
+  if ((boundaries == nullptr) != (boundary_lens == nullptr)) return KDA_ERR_ARG;
+  if (L == 0 || B == 0) return KDA_OK;
+  return kda::launch_commit(state_ptrs, corr_ptrs, kg_ptrs, state_strides, corr_strides,
+                            kg_strides, A_log, dt_bias, sources, commit_lens, destinations,
+                            boundaries, boundary_lens, record_rows, state_dtype, lower_bound,
+                            null_slot, L, H, B, Q, n_slots, n_rows, status,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int kda_defer_commit(const int32_t *state_slots, int32_t *commit_lens, const int32_t *record_rows,
+                     int32_t *pending, const uint8_t *eager, int B, int null_slot, int n_rows,
+                     int32_t *status, void *stream) {
+  if (B < 0 || n_rows < 0) return KDA_ERR_ARG;
+  if (!state_slots || !commit_lens || !record_rows || !pending) return KDA_ERR_ARG;
+  if (B == 0) return KDA_OK;
+  return kda::launch_defer_commit(state_slots, commit_lens, record_rows, pending, eager, B,
+                                  null_slot, n_rows, status, static_cast<cudaStream_t>(stream));
+}
+
+int kda_flush_plan(const int32_t *state_slots, const int32_t *record_rows, const int32_t *pending,
+                   int32_t *commit_lens, int32_t *final_slots, int32_t *boundary_slots,
+                   int32_t *boundary_lens, int B, int Q, int null_slot, int n_rows,
+                   int32_t *status, void *stream) {
+  if (B < 0 || Q < 1 || Q > KDA_MAX_WINDOW || n_rows < 0) return KDA_ERR_ARG;
+  if (!state_slots || !record_rows || !pending || !commit_lens || !final_slots ||
+      !boundary_slots || !boundary_lens)
+    return KDA_ERR_ARG;
+  if (B == 0) return KDA_OK;
+  return kda::launch_flush_plan(state_slots, record_rows, pending, commit_lens, final_slots,
+                                boundary_slots, boundary_lens, B, Q, null_slot, n_rows, status,
+                                static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

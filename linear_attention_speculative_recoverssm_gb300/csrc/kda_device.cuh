@@ -1,0 +1,201 @@
+// Device building blocks of the KDA RecoverSSM kernels (sm_103a).
+//
+// Hand-written PTX for the async-proxy bulk copies and mbarriers, bounded
+// waits (every spin ends after a fixed time and reports KDA_ERR_TIMEOUT),
+// warp reduce-scatter, BF16 bit conversions and the gate decay.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kda_recoverssm.h"
+
+namespace kda {
+
+constexpr int kDim = KDA_HEAD_DIM;  // K = V = 128
+constexpr int kMaxQ = KDA_MAX_WINDOW;
+constexpr float kNormEps = 1e-6f;   // inside the rsqrt of the L2 norms
+// Upper bound on any device-side wait (ns of %globaltimer).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// ---------------------------------------------------------------------------
+// status reporting
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void report(int32_t *status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// BF16 bit patterns
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits) {
+  return __uint_as_float(bits << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// gate math (KdaFused.decay): exp(lb * sigmoid(exp(A_log) * (raw_g + dt)))
+// `a` is exp(A_log) of the head, computed once per item.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float sigmoidf_fast(float z) {
+  return __fdividef(1.0f, 1.0f + __expf(-z));
+}
+
+__device__ __forceinline__ float gate_decay(float a, float raw_g, float dt,
+                                            float lower_bound) {
+  return __expf(lower_bound * sigmoidf_fast(a * (raw_g + dt)));
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses, mbarriers and the bulk-copy engine
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(count)
+               : "memory");
+}
+
+// Make initialised barriers visible to the async proxy (and the cluster).
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete; gives up
+// after kWaitLimitNs and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar,
+                                                  uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long start = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - start > kWaitLimitNs) return false;
+  }
+}
+
+// One bulk (non-tensor) copy global -> this CTA's shared memory, completing
+// `bytes` of transaction count on `bar`.  Addresses 16-byte aligned, size a
+// multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src,
+                                         uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority hint (policy from createpolicy).
+__device__ __forceinline__ void bulk_g2s_hint(void *smem_dst,
+                                              const void *gmem_src,
+                                              uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes."
+      "L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
+               : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// vector shared / global accesses
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float4 lds4(const float *p) {
+  return *reinterpret_cast<const float4 *>(p);
+}
+
+__device__ __forceinline__ void stg4(float *p, float4 v) {
+  *reinterpret_cast<float4 *>(p) = v;
+}
+
+// ---------------------------------------------------------------------------
+// warp reduce-scatter
+// ---------------------------------------------------------------------------
+//
+// `v` holds N partial values per lane; the LANES consecutive lanes of a
+// group (LANES a power of two dividing 32, N a multiple of LANES) add them up
+// so that afterwards lane l of the group holds the totals of indices
+// [l * N / LANES, (l + 1) * N / LANES) in v[0 .. N / LANES).  It takes
+// N/2 + N/4 + ... + N/LANES shuffles instead of N * log2(LANES).
+template <int N, int LANES>
+__device__ __forceinline__ void reduce_scatter(float (&v)[N], int lane) {
+  static_assert(N % LANES == 0, "N must be a multiple of the group size");
+#pragma unroll
+  for (int o = LANES / 2, cnt = N; o >= 1; o >>= 1, cnt >>= 1) {
+    const bool upper = (lane & o) != 0;
+    const int half = cnt / 2;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[half + i];
+      const float keep = upper ? v[half + i] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+}  // namespace kda

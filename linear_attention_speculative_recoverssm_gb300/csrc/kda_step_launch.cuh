@@ -1,0 +1,89 @@
+// Host-side launch of the step kernels for one window size Q; included by
+// the per-Q translation units kda_step_q<Q>.cu so they compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "kda_launch.h"
+#include "kda_step.cuh"
+#include "kda_step_cluster.cuh"
+
+namespace kda {
+
+template <int Q, typename ST, bool REPLAY, bool BOUNDARY>
+int launch_persistent(const StepParams &p, int n_items, cudaStream_t stream) {
+  auto kern = kda_step_persistent<Q, ST, REPLAY, BOUNDARY>;
+  constexpr size_t smem = sizeof(StepSmem<Q, ST, default_stages<ST>(), BOUNDARY>);
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return KDA_ERR_CUDA;
+    configured.fetch_or(bit);
+  }
+  const int sms = device_sm_count(dev);
+  const int grid = n_items < sms ? n_items : sms;
+  kern<<<grid, kThreads, smem, stream>>>(p, n_items);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+template <int Q, int SPLIT, bool BOUNDARY>
+int launch_cluster(const StepParams &p, int n_items, cudaStream_t stream) {
+  auto kern = kda_step_cluster<Q, SPLIT, BOUNDARY>;
+  constexpr size_t smem = sizeof(ClusterSmem<Q, SPLIT, BOUNDARY>);
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return KDA_ERR_CUDA;
+    configured.fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(SPLIT, (unsigned)n_items, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = SPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return KDA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+template <int Q>
+int launch_step_q(const StepParams &p, int n_items, int variant, int split,
+                  cudaStream_t stream) {
+  if (split == 1) {
+    switch (variant) {
+      case 0: return launch_persistent<Q, float, false, false>(p, n_items, stream);
+      case 1: return launch_persistent<Q, uint16_t, false, false>(p, n_items, stream);
+      case 2: return launch_persistent<Q, float, true, false>(p, n_items, stream);
+      case 3: return launch_persistent<Q, float, true, true>(p, n_items, stream);
+      default: return KDA_ERR_ARG;
+    }
+  }
+  // the cluster split serves the fused FP32 replay + verify
+  if (variant != 2 && variant != 3) return KDA_ERR_UNSUPPORTED;
+  const bool bnd = variant == 3;
+  if (split == 2)
+    return bnd ? launch_cluster<Q, 2, true>(p, n_items, stream)
+               : launch_cluster<Q, 2, false>(p, n_items, stream);
+  if (split == 4)
+    return bnd ? launch_cluster<Q, 4, true>(p, n_items, stream)
+               : launch_cluster<Q, 4, false>(p, n_items, stream);
+  return KDA_ERR_ARG;
+}
+
+}  // namespace kda

@@ -1,0 +1,9 @@
+// Step kernels for a window of 5 token(s).
+#include "kda_step_launch.cuh"
+
+namespace kda {
+int launch_step_q5(const StepParams &p, int n_items, int variant, int split,
+                    cudaStream_t stream) {
+  return launch_step_q<5>(p, n_items, variant, split, stream);
+}
+}  // namespace kda

@@ -1,0 +1,9 @@
+// Step kernels for a window of 6 token(s).
+#include "kda_step_launch.cuh"
+
+namespace kda {
+int launch_step_q6(const StepParams &p, int n_items, int variant, int split,
+                    cudaStream_t stream) {
+  return launch_step_q<6>(p, n_items, variant, split, stream);
+}
+}  // namespace kda

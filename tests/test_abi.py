@@ -1,0 +1,101 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and its host-side argument checks reject bad calls before
+anything is launched (so these calls are safe on any machine)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_speculative_recoverssm_gb300 import _build, _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return _lib.load()
+
+
+def _declared():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            names += re.findall(r"^(?:int|const char \*)\s*(kda_\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert set(_lib.EXPORTS) <= set(declared)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_error_strings(lib):
+    assert lib.kda_abi_version() == 1
+    assert lib.kda_error_string(0) == b"ok"
+    assert lib.kda_error_string(-2).startswith(b"pointer")
+    assert lib.kda_error_string(123) == b"unknown status"
+
+
+A = 0x10000  # a 16-byte aligned stand-in address: never dereferenced below
+
+
+def _verify_args(**over):
+    args = dict(q=A, k=A, v=A, g=A, beta=A, A_log=A, dt_bias=A, lb=-5.0, qs=0.088,
+                state=A, dtype=0, slot_stride=2 * 128 * 128, n_slots=4, slots=A, rows=A,
+                corr=A, kg=A, crs=2 * 2 * 128, krs=2 * 2 * 256, n_rows=2, rq=2, out=A,
+                B=2, H=2, Q=2, null=0, status=None, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Q=0), _lib.KDA_ERR_ARG), (dict(Q=9), _lib.KDA_ERR_ARG),
+    (dict(rq=1), _lib.KDA_ERR_ARG), (dict(H=0), _lib.KDA_ERR_ARG),
+    (dict(B=-1), _lib.KDA_ERR_ARG), (dict(q=None), _lib.KDA_ERR_ARG),
+    (dict(state=None), _lib.KDA_ERR_ARG), (dict(slot_stride=100), _lib.KDA_ERR_ARG),
+    (dict(q=A + 2), _lib.KDA_ERR_ALIGN), (dict(state=A + 4), _lib.KDA_ERR_ALIGN),
+    (dict(slot_stride=2 * 128 * 128 + 1), _lib.KDA_ERR_ALIGN),
+    (dict(dtype=7), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(B=0), _lib.KDA_OK),
+])
+def test_verify_host_checks(lib, over, code):
+    assert lib.kda_verify(*_verify_args(**over)) == code
+
+
+def test_replay_verify_host_checks(lib):
+    base = dict(q=A, k=A, v=A, g=A, beta=A, A_log=A, dt_bias=A, lb=-5.0, qs=0.088, state=A,
+                slot_stride=2 * 128 * 128, n_slots=4, slots=A, rows=A, pending=A, corr=A,
+                kg=A, crs=2 * 2 * 128, krs=2 * 2 * 256, n_rows=2, rq=2, bslots=None,
+                blens=None, out=A, B=2, H=2, Q=2, null=0, split=1, status=None, stream=None)
+
+    def call(**over):
+        a = dict(base)
+        a.update(over)
+        return lib.kda_replay_verify(*a.values())
+
+    assert call(split=3) == _lib.KDA_ERR_ARG
+    assert call(pending=None) == _lib.KDA_ERR_ARG
+    assert call(rows=None) == _lib.KDA_ERR_ARG
+    assert call(bslots=A) == _lib.KDA_ERR_ARG  # boundary lengths missing
+    assert call(corr=A + 8) == _lib.KDA_ERR_ALIGN
+    assert call(B=0) == _lib.KDA_OK
+
+
+def test_commit_and_bookkeeping_host_checks(lib):
+    P = [A] * 14
+    assert lib.kda_commit(*P, 5, -5.0, 0, 1, 2, 2, 2, 4, 2, None, None) == _lib.KDA_ERR_UNSUPPORTED
+    assert lib.kda_commit(*P, 1, -5.0, 0, 1, 2, 2, 0, 4, 2, None, None) == _lib.KDA_ERR_ARG
+    P2 = list(P)
+    P2[12] = None  # boundaries given without lengths
+    assert lib.kda_commit(*P2, 1, -5.0, 0, 1, 2, 2, 2, 4, 2, None, None) == _lib.KDA_ERR_ARG
+    assert lib.kda_commit(*P, 1, -5.0, 0, 1, 2, 0, 2, 4, 2, None, None) == _lib.KDA_OK
+    assert lib.kda_defer_commit(A, A, None, A, None, 2, 0, 2, None, None) == _lib.KDA_ERR_ARG
+    assert lib.kda_defer_commit(A, A, A, A, None, 0, 0, 2, None, None) == _lib.KDA_OK
+    assert lib.kda_flush_plan(A, A, A, A, A, A, A, 2, 9, 0, 2, None, None) == _lib.KDA_ERR_ARG
+    assert lib.kda_flush_plan(A, A, A, A, A, A, A, 0, 4, 0, 2, None, None) == _lib.KDA_OK
