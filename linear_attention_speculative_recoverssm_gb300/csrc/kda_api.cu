@@ -55,6 +55,9 @@ int launch_step(const StepParams &p, int n_items, int Q, int variant, int split,
 
 namespace {
 
+// check_step_args: the call is valid but has no work (B == 0).
+constexpr int kNothingToDo = 1;
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks shared by kda_verify and kda_replay_verify.
@@ -66,6 +69,7 @@ int check_step_args(const void *q, const void *k, const void *v, const void *g,
                     const void *out, int B, int H, int Q) {
   if (B < 0 || H < 1 || Q < 1 || Q > KDA_MAX_WINDOW || rq < Q || rq > KDA_MAX_WINDOW)
     return KDA_ERR_ARG;
+  if (B == 0) return kNothingToDo;  // zero tokens: empty buffers may be NULL
   if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !state_pool || !state_slots ||
       !corr || !key_gate || !out)
     return KDA_ERR_ARG;
@@ -157,8 +161,8 @@ int kda_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kd
   int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, sb,
                            slot_stride, n_slots, state_slots, corr, key_gate, corr_row_stride,
                            kg_row_stride, n_rows, rq, out, B, H, Q);
+  if (rc == kNothingToDo) return KDA_OK;
   if (rc != KDA_OK) return rc;
-  if (B == 0) return KDA_OK;
   const kda::StepParams p = make_params(
       q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound, q_scale,
       const_cast<void *>(state_pool), slot_stride, n_slots, state_slots, record_rows, nullptr,
@@ -180,11 +184,11 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, 4, slot_stride,
                            n_slots, state_slots, corr, key_gate, corr_row_stride, kg_row_stride,
                            n_rows, rq, out, B, H, Q);
+  if (split != 0 && split != 1 && split != 2 && split != 4) return KDA_ERR_ARG;
+  if (rc == kNothingToDo) return KDA_OK;
   if (rc != KDA_OK) return rc;
   if (!record_rows || !pending) return KDA_ERR_ARG;
   if ((boundary_slots == nullptr) != (boundary_lens == nullptr)) return KDA_ERR_ARG;
-  if (split != 0 && split != 1 && split != 2 && split != 4) return KDA_ERR_ARG;
-  if (B == 0) return KDA_OK;
   const int items = B * H;
   if (split == 0) {
     // Whole items on persistent CTAs when they fill the GPU; otherwise split
