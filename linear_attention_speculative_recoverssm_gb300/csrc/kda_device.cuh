@@ -165,6 +165,92 @@ __device__ __forceinline__ void stg4(float *p, float4 v) {
   *reinterpret_cast<float4 *>(p) = v;
 }
 
+__device__ __forceinline__ void sts4(float *p, float4 v) {
+  *reinterpret_cast<float4 *>(p) = v;
+}
+
+// ---------------------------------------------------------------------------
+// packed FP32 pairs (fma.rn.f32x2 / mul / add on sm_100+): one instruction
+// for two lanes of FP32 arithmetic, each rounded like the scalar op.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long f2_bits(float2 v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 bits_f2(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+
+// (a.x * b.x + c.x, a.y * b.y + c.y)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+
+// s (4 floats) <- s * d, elementwise, as two packed multiplies
+__device__ __forceinline__ float4 fmul4(float4 s, float4 d) {
+  const float2 lo = fmul2(make_float2(s.x, s.y), make_float2(d.x, d.y));
+  const float2 hi = fmul2(make_float2(s.z, s.w), make_float2(d.z, d.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// s <- u * k + s (u scalar), as two packed FMAs
+__device__ __forceinline__ float4 ffma4s(float u, float4 k, float4 s) {
+  const float2 uu = make_float2(u, u);
+  const float2 lo = ffma2(uu, make_float2(k.x, k.y), make_float2(s.x, s.y));
+  const float2 hi = ffma2(uu, make_float2(k.z, k.w), make_float2(s.z, s.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// acc (even-key, odd-key partial sums) += s . x over 4 keys
+__device__ __forceinline__ float2 dot4_acc(float4 s, float4 x, float2 acc) {
+  acc = ffma2(make_float2(s.x, s.y), make_float2(x.x, x.y), acc);
+  return ffma2(make_float2(s.z, s.w), make_float2(x.z, x.w), acc);
+}
+
+// ---------------------------------------------------------------------------
+// named barriers (a warpgroup's own barrier, not the whole CTA's)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Barrier that also ORs a predicate over the participating threads, so a
+// decision taken after a bounded wait is the same for all of them.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // warp reduce-scatter
 // ---------------------------------------------------------------------------

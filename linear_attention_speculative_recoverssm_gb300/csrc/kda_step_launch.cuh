@@ -9,6 +9,7 @@
 #include "kda_launch.h"
 #include "kda_step.cuh"
 #include "kda_step_cluster.cuh"
+#include "kda_step_ws.cuh"
 
 namespace kda {
 
@@ -29,6 +30,26 @@ int launch_persistent(const StepParams &p, int n_items, cudaStream_t stream) {
   const int sms = device_sm_count(dev);
   const int grid = n_items < sms ? n_items : sms;
   kern<<<grid, kThreads, smem, stream>>>(p, n_items);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+template <int Q, typename ST, bool REPLAY, bool BOUNDARY>
+int launch_ws(const StepParams &p, int n_items, cudaStream_t stream) {
+  auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY>;
+  constexpr size_t smem = sizeof(WsSmem<Q, ST, BOUNDARY>);
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return KDA_ERR_CUDA;
+    configured.fetch_or(bit);
+  }
+  const int sms = device_sm_count(dev);
+  const int grid = n_items < sms ? n_items : sms;
+  kern<<<grid, kWsThreads, smem, stream>>>(p, n_items);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -67,10 +88,10 @@ int launch_step_q(const StepParams &p, int n_items, int variant, int split,
                   cudaStream_t stream) {
   if (split == 1) {
     switch (variant) {
-      case 0: return launch_persistent<Q, float, false, false>(p, n_items, stream);
-      case 1: return launch_persistent<Q, uint16_t, false, false>(p, n_items, stream);
-      case 2: return launch_persistent<Q, float, true, false>(p, n_items, stream);
-      case 3: return launch_persistent<Q, float, true, true>(p, n_items, stream);
+      case 0: return launch_ws<Q, float, false, false>(p, n_items, stream);
+      case 1: return launch_ws<Q, uint16_t, false, false>(p, n_items, stream);
+      case 2: return launch_ws<Q, float, true, false>(p, n_items, stream);
+      case 3: return launch_ws<Q, float, true, true>(p, n_items, stream);
       default: return KDA_ERR_ARG;
     }
   }

@@ -211,6 +211,11 @@ WORKLOADS = {
     "replay-verify-f32-h64-b512-q8": dict(kind="replay_verify", B=512, H=64,
                                           Q=8, slots=1024, seed=3,
                                           padding_frac=0.05),
+    # the large-batch shape at a quarter of the requests (the same kernel
+    # instance, ~0.6 GB of state): small enough for a full profiler capture
+    "replay-verify-f32-h64-b128-q8": dict(kind="replay_verify", B=128, H=64,
+                                          Q=8, slots=160, seed=5,
+                                          padding_frac=0.05),
 }
 
 
