@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstddef>
 
 #include "kda_device.cuh"
 #include "kda_launch.h"
@@ -49,6 +50,17 @@ struct CommitSmem {
   float red[4][kMaxQ];
   uint64_t full[NS];
 };
+
+template <typename ST>
+struct CommitLayoutCheck {
+  using S = CommitSmem<ST>;
+  static_assert(offsetof(S, stage) % 128 == 0 && offsetof(S, kp) % 16 == 0 &&
+                offsetof(S, dn) % 16 == 0 && offsetof(S, kpb) % 16 == 0 &&
+                offsetof(S, db) % 16 == 0 && offsetof(S, full) % 8 == 0,
+                "float4-read members / barrier alignment");
+  static constexpr bool ok = true;
+};
+static_assert(CommitLayoutCheck<float>::ok && CommitLayoutCheck<uint16_t>::ok, "layout");
 
 struct CommitItem {
   int l, b, h;

@@ -18,6 +18,8 @@
 // item has passed that barrier, i.e. after every old record was read.
 #pragma once
 
+#include <cstddef>
+
 #include "kda_step.cuh"
 
 namespace kda {
@@ -43,6 +45,17 @@ struct ClusterSmem {
   float scal[Red<Q>::kN];
   float rsrec[kMaxQ];
   uint64_t full;
+};
+
+template <int Q, int SPLIT, bool BOUNDARY>
+struct ClusterLayoutCheck {
+  using S = ClusterSmem<Q, SPLIT, BOUNDARY>;
+  static_assert(offsetof(S, stage) % 128 == 0 && offsetof(S, xk) % 16 == 0 &&
+                offsetof(S, xq) % 16 == 0 && offsetof(S, kp) % 16 == 0 &&
+                offsetof(S, dn) % 16 == 0 && offsetof(S, kpb) % 16 == 0 &&
+                offsetof(S, db) % 16 == 0 && offsetof(S, full) % 8 == 0,
+                "float4-read members / barrier alignment");
+  static constexpr bool ok = true;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -76,6 +89,7 @@ template <int Q, int SPLIT, bool BOUNDARY>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_step_cluster(const StepParams p) {
   using Smem = ClusterSmem<Q, SPLIT, BOUNDARY>;
+  static_assert(ClusterLayoutCheck<Q, SPLIT, BOUNDARY>::ok, "layout");
   constexpr int ROWS = Smem::kRows;           // state rows of this CTA
   constexpr int L = kThreads / ROWS;          // lanes per row (4 or 8)
   constexpr int NCH = kDim / (4 * L);         // 4-key chunks per lane

@@ -34,6 +34,8 @@
 //    timeout is reported in the status word instead of hanging.
 #pragma once
 
+#include <cstddef>
+
 #include "kda_step.cuh"
 
 namespace kda {
@@ -52,8 +54,9 @@ struct WsRed {
   static constexpr int kPad = round_up(kN, 32);
 };
 
+// 16-byte aligned so that ops[1] (and every float4 member) stays aligned.
 template <int Q, bool BOUNDARY>
-struct WsOps {
+struct alignas(16) WsOps {
   float xk[Q][kDim];  // Gamma_t * k_t (unnormalised)
   float xq[Q][kDim];  // Gamma_t * q_t (unnormalised)
   float kp[kMaxQ][kDim];
@@ -83,6 +86,23 @@ struct WsSmem {
   uint64_t full[NS];
   uint64_t opfull[2];
   uint64_t opempty[2];
+};
+
+// Every member read or written as float4 (or as a bulk-copy target) must sit
+// on a 16-byte boundary; the barriers on 8.
+template <int Q, typename ST, bool BOUNDARY>
+struct WsLayoutCheck {
+  using S = WsSmem<Q, ST, BOUNDARY>;
+  using O = WsOps<Q, BOUNDARY>;
+  static_assert(sizeof(O) % 16 == 0, "ops buffers must stay 16-byte aligned");
+  static_assert(offsetof(S, stage) % 128 == 0 && offsetof(S, ops) % 16 == 0, "stage / ops");
+  static_assert(offsetof(O, xk) % 16 == 0 && offsetof(O, xq) % 16 == 0 &&
+                offsetof(O, kp) % 16 == 0 && offsetof(O, dn) % 16 == 0 &&
+                offsetof(O, kpb) % 16 == 0 && offsetof(O, db) % 16 == 0,
+                "float4-read ops members");
+  static_assert(offsetof(S, full) % 8 == 0 && offsetof(S, opfull) % 8 == 0 &&
+                offsetof(S, opempty) % 8 == 0, "mbarriers");
+  static constexpr bool ok = true;
 };
 
 // The 8 keys of lane l (0..15) in a state row, as two groups of 4: FP32 rows
@@ -124,6 +144,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     kda_step_ws(const StepParams p, int n_items) {
   using Smem = WsSmem<Q, ST, BOUNDARY>;
   using Ops = WsOps<Q, BOUNDARY>;
+  static_assert(WsLayoutCheck<Q, ST, BOUNDARY>::ok, "layout");
   constexpr int NS = Smem::NS;
   constexpr uint32_t kPageBytes = kDim * kDim * sizeof(ST);
   constexpr int NR = WsRed<Q>::kN;
