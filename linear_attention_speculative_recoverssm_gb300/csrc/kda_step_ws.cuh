@@ -71,6 +71,15 @@ struct alignas(16) WsOps {
   int meta[8];  // b, h, slot, rec, n, bslot, m
 };
 
+// One item's inputs, staged by bulk copies one item ahead of the prologue.
+template <int Q>
+struct alignas(16) WsIn {
+  uint16_t tok[4][Q][kDim];      // q, k, raw_g, v rows of this window (BF16)
+  uint16_t kg[kMaxQ][2 * kDim];  // recorded key / raw gate rows (first n)
+  float corr[kMaxQ][kDim];       // recorded corrections (first n)
+  int meta[8];                   // b, h, slot, rec, n, bslot, m
+};
+
 template <typename ST>
 __host__ __device__ constexpr int ws_stages() {
   return sizeof(ST) == 4 ? 2 : 4;
@@ -81,11 +90,14 @@ struct WsSmem {
   static constexpr int NS = ws_stages<ST>();
   ST stage[NS][kDim * kDim];
   WsOps<Q, BOUNDARY> ops[2];
+  WsIn<Q> in[2];
   float dots[kDim][2 * Q + 1];  // [row][w_0..w_Q-1, y_0..y_Q-1] (odd pitch)
   float red[4][WsRed<Q>::kPad];
   uint64_t full[NS];
   uint64_t opfull[2];
   uint64_t opempty[2];
+  uint64_t infull[2];
+  int next_meta[8];  // resolved index chain of the next item to request
 };
 
 // Every member read or written as float4 (or as a bulk-copy target) must sit
@@ -100,8 +112,12 @@ struct WsLayoutCheck {
                 offsetof(O, kp) % 16 == 0 && offsetof(O, dn) % 16 == 0 &&
                 offsetof(O, kpb) % 16 == 0 && offsetof(O, db) % 16 == 0,
                 "float4-read ops members");
+  static_assert(sizeof(WsIn<Q>) % 16 == 0 && offsetof(S, in) % 16 == 0 &&
+                offsetof(WsIn<Q>, tok) % 16 == 0 && offsetof(WsIn<Q>, kg) % 16 == 0 &&
+                offsetof(WsIn<Q>, corr) % 16 == 0, "bulk-copy targets");
   static_assert(offsetof(S, full) % 8 == 0 && offsetof(S, opfull) % 8 == 0 &&
-                offsetof(S, opempty) % 8 == 0, "mbarriers");
+                offsetof(S, opempty) % 8 == 0 && offsetof(S, infull) % 8 == 0, "mbarriers");
+  static_assert(sizeof(S) <= 232448, "shared memory per CTA");
   static constexpr bool ok = true;
 };
 
@@ -182,6 +198,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     mbar_init(&sm.opfull[1], 1);
     mbar_init(&sm.opempty[0], 1);
     mbar_init(&sm.opempty[1], 1);
+    mbar_init(&sm.infull[0], 1);
+    mbar_init(&sm.infull[1], 1);
     mbar_init_fence();
   }
   __syncthreads();
@@ -191,51 +209,187 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // prologue warpgroup: thread c owns key channel c
     // =====================================================================
     const int c = tid;
+    // The index chain slot / record row -> pending count -> records runs two
+    // items ahead in thread 0; warp 0 requests item j + 1's inputs while
+    // item j is built, so the warpgroup itself never waits on HBM latency.
+    int rs_slot = -1, rs_rec = -1, rs_bslot = -1, rs_blen = 0, rs_pend = 0;  // item j + 2
+    auto publish_next = [&](const ItemMeta &m) {  // item j + 1, read by warp 0
+      sm.next_meta[0] = m.b;
+      sm.next_meta[1] = m.h;
+      sm.next_meta[2] = m.slot;
+      sm.next_meta[3] = m.rec;
+      sm.next_meta[4] = m.n;
+      sm.next_meta[5] = m.bslot;
+      sm.next_meta[6] = m.m;
+    };
+    auto load_raw = [&](int i) {
+      const int b = (first + i * stride) / p.H;
+      rs_slot = p.state_slots[b];
+      rs_rec = p.record_rows != nullptr ? p.record_rows[b] : b;
+      rs_bslot = -1;
+      rs_blen = 0;
+      if (BOUNDARY && p.bnd_slots != nullptr) {
+        rs_bslot = p.bnd_slots[b];
+        rs_blen = p.bnd_lens[b];
+      }
+    };
+    auto load_pending = [&]() {
+      rs_pend = 0;
+      if (REPLAY && rs_rec >= 0 && rs_rec < p.n_rows && rs_slot > p.null_slot &&
+          rs_slot < p.n_slots)
+        rs_pend = p.pending[rs_rec];
+    };
+    auto resolve = [&](int i) {  // item_meta from the loaded raw values
+      ItemMeta it;
+      it.b = (first + i * stride) / p.H;
+      it.h = (first + i * stride) - it.b * p.H;
+      int slot = rs_slot;
+      if (slot >= p.n_slots) {
+        report(p.status, KDA_ERR_ARG);
+        slot = -1;
+      }
+      it.slot = slot > p.null_slot ? slot : -1;
+      int rec = rs_rec;
+      if (rec >= p.n_rows) {
+        if (it.slot >= 0) report(p.status, KDA_ERR_ARG);
+        rec = -1;
+      }
+      it.rec = rec;
+      it.n = (REPLAY && rec >= 0) ? (rs_pend < 0 ? 0 : (rs_pend > p.rq ? p.rq : rs_pend)) : 0;
+      it.bslot = -1;
+      it.m = 0;
+      if (BOUNDARY && it.n > 0 && p.bnd_slots != nullptr) {
+        if (rs_bslot >= p.n_slots) {
+          report(p.status, KDA_ERR_ARG);
+        } else if (rs_blen > 0 && rs_bslot > p.null_slot) {
+          it.bslot = rs_bslot;
+          it.m = rs_blen < it.n ? rs_blen : it.n;
+        }
+      }
+      return it;
+    };
+    // Warp 0: the bulk copies of item i's inputs into in[i & 1].
+    auto request_inputs = [&](int i) {
+      __syncwarp();
+      ItemMeta m;
+      m.b = sm.next_meta[0];
+      m.h = sm.next_meta[1];
+      m.slot = sm.next_meta[2];
+      m.rec = sm.next_meta[3];
+      m.n = sm.next_meta[4];
+      m.bslot = sm.next_meta[5];
+      m.m = sm.next_meta[6];
+      __syncwarp();  // thread 0 republishes next_meta after this
+      WsIn<Q> &in = sm.in[i & 1];
+      uint64_t *bar = &sm.infull[i & 1];
+      const int nrec = (m.rec >= 0) ? m.n : 0;
+      if (lane == 0) {
+        in.meta[0] = m.b;
+        in.meta[1] = m.h;
+        in.meta[2] = m.slot;
+        in.meta[3] = m.rec;
+        in.meta[4] = m.n;
+        in.meta[5] = m.bslot;
+        in.meta[6] = m.m;
+        if (m.slot >= 0)
+          mbar_arrive_expect_tx(bar, 4u * Q * kDim * 2u + (uint32_t)nrec * 2u * kDim * 4u);
+        else
+          mbar_arrive(bar);
+      }
+      __syncwarp();
+      if (m.slot < 0) return;
+      const long long tok0 = (long long)m.b * Q;
+      for (int idx = lane; idx < 4 * Q + 2; idx += 32) {
+        if (idx < 4 * Q) {
+          const int x = idx / Q, t = idx - (idx / Q) * Q;
+          const uint16_t *src = x == 0 ? p.q : (x == 1 ? p.k : (x == 2 ? p.g : p.v));
+          bulk_g2s(in.tok[x][t], src + ((tok0 + t) * p.H + m.h) * kDim, kDim * 2, bar);
+        } else if (nrec > 0 && idx == 4 * Q) {
+          bulk_g2s(in.kg, p.kg + (long long)m.rec * p.kg_row_stride +
+                              (long long)m.h * p.rq * (2 * kDim),
+                   (uint32_t)nrec * 2 * kDim * 2, bar);
+        } else if (nrec > 0) {
+          bulk_g2s(in.corr, p.corr + (long long)m.rec * p.corr_row_stride +
+                                (long long)m.h * p.rq * kDim,
+                   (uint32_t)nrec * kDim * 4, bar);
+        }
+      }
+    };
+    // per-head / per-token scalars of an item, prefetched one item ahead
+    float dt_n = 0.f, alog_n = 0.f, beta_n = 0.f;
+    auto load_small = [&](int i) {
+      const int b = (first + i * stride) / p.H;
+      const int h = (first + i * stride) - b * p.H;
+      dt_n = p.dt_bias[h * kDim + c];
+      alog_n = p.A_log[h];
+      beta_n = c < Q ? bf16_bits_to_f32(p.beta[((long long)b * Q + c) * p.H + h]) : 0.f;
+    };
+
+    int requested = 0;  // items whose inputs were requested (warp 0)
+    int taken = 0;      // items whose inputs were waited for
+    if (count > 0) {
+      requested = 1;
+      if (c == 0) {
+        load_raw(0);
+        load_pending();
+        publish_next(resolve(0));
+      }
+      if (warp == 0) request_inputs(0);
+      if (c == 0 && count > 1) {
+        load_raw(1);
+        load_pending();
+        publish_next(resolve(1));
+        if (count > 2) load_raw(2);
+      }
+      load_small(0);
+    }
+
     for (int j = 0; j < count; ++j) {
-      const int item = first + j * stride;
-      const ItemMeta it = item_meta<REPLAY, BOUNDARY>(p, item, c == 0);
       Ops &op = sm.ops[j & 1];
-      const long long tok0 = (long long)it.b * Q;
+      const WsIn<Q> &in = sm.in[j & 1];
+      const float dt = dt_n, a = __expf(alog_n), braw = beta_n;
+      if (j + 1 < count) {
+        if (warp == 0) request_inputs(j + 1);
+        requested = j + 2;
+        load_small(j + 1);
+      }
+      if (c == 0 && j + 2 < count) load_pending();  // item j + 2 (its row is loaded)
+
+      bool ok = mbar_wait_bounded(&sm.infull[j & 1], (uint32_t)((j >> 1) & 1));
+      if (named_bar_or(kBarPro, 128, !ok)) {
+        if (c == 0) report(p.status, KDA_ERR_TIMEOUT);
+        break;
+      }
+      taken = j + 1;
+      ItemMeta it;
+      it.b = in.meta[0];
+      it.h = in.meta[1];
+      it.slot = in.meta[2];
+      it.rec = in.meta[3];
+      it.n = in.meta[4];
+      it.bslot = in.meta[5];
+      it.m = in.meta[6];
       const bool live = it.slot >= 0;
 
-      float kk[Q], qq[Q], vq[Q], gam[Q], inv[Q];
-      uint16_t kbits[Q], gbits[Q];
-      float kr[kMaxQ], ur[kMaxQ], dr[kMaxQ];
-      float braw = 0.f;
+      // (inputs are re-read from the stage where needed: fewer live registers)
+      float kk[Q], qq[Q], gam[Q], inv[Q];
+      float kr[kMaxQ], dr[kMaxQ];
       if (live) {
-        // ---- global loads of this item (independent, issued together) ----
-        const float a = __expf(p.A_log[it.h]);
-        const float dt = p.dt_bias[it.h * kDim + c];
-#pragma unroll
-        for (int t = 0; t < Q; ++t) {
-          const long long off = ((tok0 + t) * p.H + it.h) * kDim + c;
-          kbits[t] = p.k[off];
-          gbits[t] = p.g[off];
-          qq[t] = bf16_bits_to_f32(p.q[off]);
-          vq[t] = bf16_bits_to_f32(p.v[off]);
-        }
-        if (c < Q) braw = bf16_bits_to_f32(p.beta[(tok0 + c) * p.H + it.h]);
-        const long long cbase = (long long)it.rec * p.corr_row_stride +
-                                (long long)it.h * p.rq * kDim + c;
-        const long long kbase = (long long)it.rec * p.kg_row_stride +
-                                (long long)it.h * p.rq * (2 * kDim) + c;
 #pragma unroll
         for (int t = 0; t < kMaxQ; ++t) {
           kr[t] = 0.f;
-          ur[t] = 0.f;
           dr[t] = 1.f;
           if (REPLAY && t < it.n) {
-            ur[t] = p.corr[cbase + t * kDim];
-            kr[t] = bf16_bits_to_f32(p.kg[kbase + t * 2 * kDim]);
-            dr[t] = gate_decay(a, bf16_bits_to_f32(p.kg[kbase + t * 2 * kDim + kDim]), dt,
-                               p.lower_bound);
+            kr[t] = bf16_bits_to_f32(in.kg[t][c]);
+            dr[t] = gate_decay(a, bf16_bits_to_f32(in.kg[t][kDim + c]), dt, p.lower_bound);
           }
         }
         float g = 1.f;
 #pragma unroll
         for (int t = 0; t < Q; ++t) {
-          kk[t] = bf16_bits_to_f32(kbits[t]);
-          g *= gate_decay(a, bf16_bits_to_f32(gbits[t]), dt, p.lower_bound);
+          qq[t] = bf16_bits_to_f32(in.tok[0][t][c]);
+          kk[t] = bf16_bits_to_f32(in.tok[1][t][c]);
+          g *= gate_decay(a, bf16_bits_to_f32(in.tok[2][t][c]), dt, p.lower_bound);
           gam[t] = g;
           inv[t] = __fdividef(1.f, g);
         }
@@ -268,10 +422,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           sm.red[warp][ch * 32 + lane] = v[0];
         }
       }
+      // thread 0: the index chain of item j + 2, then the row of item j + 3
+      if (c == 0 && j + 2 < count) {
+        publish_next(resolve(j + 2));
+        if (j + 3 < count) load_raw(j + 3);
+      }
 
       // ---- the ops buffer of item j - 2 must have been consumed ----
       if (j >= 2) {
-        const bool ok = mbar_wait_bounded(&sm.opempty[j & 1], (uint32_t)(((j >> 1) - 1) & 1));
+        ok = mbar_wait_bounded(&sm.opempty[j & 1], (uint32_t)(((j >> 1) - 1) & 1));
         if (named_bar_or(kBarPro, 128, !ok)) {
           if (c == 0) report(p.status, KDA_ERR_TIMEOUT);
           break;
@@ -291,7 +450,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         for (int t = 0; t < Q; ++t) {
           op.xk[t][c] = gam[t] * kk[t];
           op.xq[t][c] = gam[t] * qq[t];
-          op.vv[t][c] = vq[t];
+          op.vv[t][c] = bf16_bits_to_f32(in.tok[3][t][c]);
         }
         if (c < Q) op.beta[c] = sigmoidf_fast(braw);
         if (REPLAY && it.n > 0) {
@@ -347,7 +506,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (REPLAY) {
 #pragma unroll
           for (int t = 0; t < kMaxQ; ++t)
-            if (t < it.n) op.u[t][c] = ur[t] * op.scal[WsRed<Q>::kRec + t];
+            if (t < it.n) op.u[t][c] = in.corr[t][c] * op.scal[WsRed<Q>::kRec + t];
         }
         // New key / gate records: the old ones were read above.
         if (it.rec >= 0) {
@@ -355,13 +514,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                                   (long long)it.h * p.rq * (2 * kDim) + c;
 #pragma unroll
           for (int t = 0; t < Q; ++t) {
-            p.kg[kbase + t * 2 * kDim] = kbits[t];
-            p.kg[kbase + t * 2 * kDim + kDim] = gbits[t];
+            p.kg[kbase + t * 2 * kDim] = in.tok[1][t][c];
+            p.kg[kbase + t * 2 * kDim + kDim] = in.tok[2][t][c];
           }
         }
       }
-      named_bar(kBarPro, 128);
+      named_bar(kBarPro, 128);  // in[j & 1] read, ops[j & 1] complete
       if (c == 0) mbar_arrive(&sm.opfull[j & 1]);
+    }
+    // After a timeout: input copies requested but never waited for must
+    // land (bounded) before this CTA's shared memory goes.
+    if (c == 0) {
+      for (int i = taken; i < requested; ++i)
+        mbar_wait_bounded(&sm.infull[i & 1], (uint32_t)((i >> 1) & 1));
     }
     return;
   }
@@ -428,54 +593,43 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (BOUNDARY && bslot >= 0)
           gbnd = reinterpret_cast<float *>(p.state) + (long long)bslot * p.slot_stride +
                  (long long)h * (kDim * kDim);
-        float4 kpa[kMaxQ], kpb4[kMaxQ];
-#pragma unroll
-        for (int t = 0; t < kMaxQ; ++t) {
-          if (t < n) {
-            kpa[t] = lds4(&op.kp[t][ka]);
-            kpb4[t] = lds4(&op.kp[t][kb]);
-          }
-        }
-        const float4 da = lds4(&op.dn[ka]), dbv = lds4(&op.dn[kb]);
         float *fpage = reinterpret_cast<float *>(page);
-#pragma unroll 2
-        for (int i = 0; i < 8; ++i) {
-          const int row = rg + 16 * i;
-          const float4 s0a = lds4(fpage + row * kDim + ka);
-          const float4 s0b = lds4(fpage + row * kDim + kb);
-          if constexpr (BOUNDARY) {
-            if (gbnd != nullptr) {
-              float4 ba = fmul4(s0a, lds4(&op.db[ka]));
-              float4 bb = fmul4(s0b, lds4(&op.db[kb]));
+        // the lane's two 4-key groups one after the other (half the
+        // coefficient registers live at a time)
+#pragma unroll 1
+        for (int grp = 0; grp < 2; ++grp) {
+          const int key = grp == 0 ? ka : kb;
+          float4 kpr[kMaxQ];
 #pragma unroll
-              for (int t = 0; t < kMaxQ; ++t) {
-                if (t < m) {
-                  const float u = op.u[t][row];
-                  ba = ffma4s(u, lds4(&op.kpb[t][ka]), ba);
-                  bb = ffma4s(u, lds4(&op.kpb[t][kb]), bb);
-                }
+          for (int t = 0; t < kMaxQ; ++t)
+            if (t < n) kpr[t] = lds4(&op.kp[t][key]);
+          const float4 d4 = lds4(&op.dn[key]);
+#pragma unroll 1
+          for (int i = 0; i < 8; ++i) {
+            const int row = rg + 16 * i;
+            const float4 s0 = lds4(fpage + row * kDim + key);
+            if constexpr (BOUNDARY) {
+              if (gbnd != nullptr) {
+                float4 bq = fmul4(s0, lds4(&op.db[key]));
+#pragma unroll
+                for (int t = 0; t < kMaxQ; ++t)
+                  if (t < m) bq = ffma4s(op.u[t][row], lds4(&op.kpb[t][key]), bq);
+                stg4(gbnd + row * kDim + key, bq);
               }
-              stg4(gbnd + row * kDim + ka, ba);
-              stg4(gbnd + row * kDim + kb, bb);
             }
-          }
-          float4 sa = fmul4(s0a, da), sb = fmul4(s0b, dbv);
+            float4 sn = fmul4(s0, d4);
 #pragma unroll
-          for (int t = 0; t < kMaxQ; ++t) {
-            if (t < n) {
-              const float u = op.u[t][row];
-              sa = ffma4s(u, kpa[t], sa);
-              sb = ffma4s(u, kpb4[t], sb);
-            }
+            for (int t = 0; t < kMaxQ; ++t)
+              if (t < n) sn = ffma4s(op.u[t][row], kpr[t], sn);
+            stg4(gpage + row * kDim + key, sn);
+            sts4(fpage + row * kDim + key, sn);
           }
-          stg4(gpage + row * kDim + ka, sa);
-          stg4(gpage + row * kDim + kb, sb);
-          sts4(fpage + row * kDim + ka, sa);
-          sts4(fpage + row * kDim + kb, sb);
         }
       }
     }
 
+    // keep pass B's vector loads from being hoisted into pass A (registers)
+    asm volatile("" ::: "memory");
     // ---------------- pass B: 2Q dots per row, Q vectors at a time -------
     constexpr int RB = WsGroup<Q>::kRows;
     constexpr int NV = WsGroup<Q>::kVals;
