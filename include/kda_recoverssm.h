@@ -103,7 +103,9 @@ const char *kda_error_string(int status);
  *   corr          [n_rows, H, rq, 128] FP32, row stride corr_row_stride
  *   key_gate      [n_rows, H, rq, 256] BF16, row stride kg_row_stride
  *   out           [B*Q, H, 128] BF16
- *   1 <= Q <= rq <= 8; H >= 1.
+ *   1 <= Q <= rq <= 8; H >= 1; -10 <= lower_bound <= 10 (a bounded gate:
+ *   the chunked form divides by prod_{r<=t} d_r, which must stay inside
+ *   FP32; KDA_ERR_UNSUPPORTED otherwise).
  */
 int kda_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                const kda_bf16 *raw_g, const kda_bf16 *raw_beta,

@@ -60,6 +60,13 @@ constexpr int kNothingToDo = 1;
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The step kernels divide by Gamma_s = prod_{r<=s} d_r >= e^{Q * lower_bound}
+// (the pair-product rows k_s / Gamma_s); a gate bound of at most 10 in size
+// keeps that and its inverse inside FP32 for Q <= 8.
+inline bool gate_bound_ok(float lower_bound) {
+  return lower_bound >= -10.0f && lower_bound <= 10.0f;  // false for NaN
+}
+
 // Checks shared by kda_verify and kda_replay_verify.
 int check_step_args(const void *q, const void *k, const void *v, const void *g,
                     const void *beta, const void *A_log, const void *dt_bias,
@@ -157,6 +164,7 @@ int kda_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kd
                kda_bf16 *out, int B, int H, int Q, int null_slot, int32_t *status,
                void *stream) {
   if (state_dtype != KDA_STATE_F32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_UNSUPPORTED;
+  if (!gate_bound_ok(lower_bound)) return KDA_ERR_UNSUPPORTED;
   const int sb = state_dtype == KDA_STATE_F32 ? 4 : 2;
   int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, sb,
                            slot_stride, n_slots, state_slots, corr, key_gate, corr_row_stride,
@@ -181,6 +189,7 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                       int n_rows, int rq, const int32_t *boundary_slots,
                       const int32_t *boundary_lens, kda_bf16 *out, int B, int H, int Q,
                       int null_slot, int split, int32_t *status, void *stream) {
+  if (!gate_bound_ok(lower_bound)) return KDA_ERR_UNSUPPORTED;
   int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, 4, slot_stride,
                            n_slots, state_slots, corr, key_gate, corr_row_stride, kg_row_stride,
                            n_rows, rq, out, B, H, Q);

@@ -10,11 +10,11 @@
 //    item's operands into one of two shared "ops" buffers, one item ahead of
 //    the main warpgroups: the decays of this window and of the recorded
 //    tokens, Gamma_t * k_t and Gamma_t * q_t, the replay coefficients
-//    k_t * P_t and D_n, the sums of squares and raw A / B pair products
-//    reduced over the 128 channels (warp reduce-scatter), the rsqrt norms and
-//    normalised pair products, beta, v, and the recorded corrections scaled
-//    by their key's rsqrt norm.  It also writes the new key / gate records,
-//    after reading the old ones.  Its global loads overlap the main work.
+//    k_t * P_t and D_n, the rows k_s / Gamma_s, the squared norms of q_t and
+//    of the recorded keys reduced over the 128 channels, beta, v, and the
+//    recorded corrections scaled by their key's rsqrt norm.  It also writes
+//    the new key / gate records, after reading the old ones.  Its inputs
+//    arrive by bulk copies one item ahead, so it never waits on HBM.
 //  * Main warpgroups (warps 4-11): a bulk copy (cp.async.bulk + mbarrier)
 //    has brought the item's 64 KB state page into one of NS stages.  Thread
 //    (row group rg = 0..15, lane l = 0..15) owns 8 keys of rows rg + 16 i:
@@ -23,7 +23,13 @@
 //      pass B: the 2Q dot products of every row with Gamma_t k_t and
 //        Gamma_t q_t, the dot vectors held in registers (Q at a time) so the
 //        state is the only operand streamed from shared memory; packed FP32
-//        FMAs; a reduce-scatter over the 16 lanes of a row;
+//        FMAs; a reduce-scatter over the 16 lanes of a row.  The same pass
+//        runs Q extra rows k_s / Gamma_s: their dots are the raw pair
+//        products, A_ts = (k_s / Gamma_s) . (Gamma_t k_t) (s < t) and
+//        B_ts = (k_s / Gamma_s) . (Gamma_t q_t) (s <= t), and the diagonal
+//        (k_s / Gamma_s) . (Gamma_s k_s) is |k_s|^2.  Lanes load their
+//        vectors and rows in a lane-XOR-permuted order so the reduce-scatter
+//        needs no selects (one shuffle and one add per pair);
 //      row solve (threads of warpgroup 1, one row each): the forward
 //        substitution u_t = beta_t (v_t - w_t - sum_s A_ts u_s), the outputs
 //        o_t = y_t + sum_s B_ts u_s (BF16) and the corrections u_t (FP32).
@@ -44,30 +50,26 @@ constexpr int kWsThreads = 384;
 constexpr int kBarPro = 1;   // named barrier of the prologue warpgroup
 constexpr int kBarMain = 2;  // named barrier of the two main warpgroups
 
-template <int Q>
-struct WsRed {
-  // reduced per item: sum k_t^2 (Q), sum q_t^2 (Q), sum of the recorded
-  // keys' squares (8), then the Q*Q raw pair products
-  static constexpr int kRec = 2 * Q;
-  static constexpr int kPair = 2 * Q + kMaxQ;
-  static constexpr int kN = kPair + Q * Q;
-  static constexpr int kPad = round_up(kN, 32);
-};
+// Reduced over channels by the prologue per item: sum q_t^2 (Q values),
+// then the recorded keys' sums of squares (8 values).
+constexpr int kWsRed = 16;
 
 // 16-byte aligned so that ops[1] (and every float4 member) stays aligned.
 template <int Q, bool BOUNDARY>
 struct alignas(16) WsOps {
   float xk[Q][kDim];  // Gamma_t * k_t (unnormalised)
   float xq[Q][kDim];  // Gamma_t * q_t (unnormalised)
+  float ex[Q][kDim];  // k_s / Gamma_s (unnormalised): the pair-product rows
   float kp[kMaxQ][kDim];
   float dn[kDim];
-  float kpb[BOUNDARY ? kMaxQ : 1][kDim];
-  float db[BOUNDARY ? kDim : 4];
+  // boundary: 1 / prod_{m <= s < n} d_s, turning the first m replay terms
+  // of S_n's sum into S_m
+  float ir[BOUNDARY ? kDim : 4];
   float u[kMaxQ][kDim];  // recorded u_t[row] * rsqrt norm of its key
   float vv[Q][kDim];
   float beta[kMaxQ];
-  // [rsk Q][rsq * q_scale Q][rs of recorded keys 8][pairs Q*Q]
-  float scal[WsRed<Q>::kN];
+  float rsq[Q];          // rsqrt(|q_t|^2 + eps) * q_scale
+  float rsrec[kMaxQ];    // rsqrt(|recorded k_t|^2 + eps)
   int meta[8];  // b, h, slot, rec, n, bslot, m
 };
 
@@ -92,7 +94,11 @@ struct WsSmem {
   WsOps<Q, BOUNDARY> ops[2];
   WsIn<Q> in[2];
   float dots[kDim][2 * Q + 1];  // [row][w_0..w_Q-1, y_0..y_Q-1] (odd pitch)
-  float red[4][WsRed<Q>::kPad];
+  float dots_ex[Q][2 * Q + 1];  // the pair-product rows' dots
+  float fin_a[Q][Q];            // normalised A_ts (s < t)
+  float fin_b[Q][Q];            // normalised B_ts (s <= t)
+  float rsk[Q];                 // rsqrt(|k_t|^2 + eps)
+  float red[4][kWsRed];
   uint64_t full[NS];
   uint64_t opfull[2];
   uint64_t opempty[2];
@@ -110,7 +116,7 @@ struct WsLayoutCheck {
   static_assert(offsetof(S, stage) % 128 == 0 && offsetof(S, ops) % 16 == 0, "stage / ops");
   static_assert(offsetof(O, xk) % 16 == 0 && offsetof(O, xq) % 16 == 0 &&
                 offsetof(O, kp) % 16 == 0 && offsetof(O, dn) % 16 == 0 &&
-                offsetof(O, kpb) % 16 == 0 && offsetof(O, db) % 16 == 0,
+                offsetof(O, ex) % 16 == 0 && offsetof(O, ir) % 16 == 0,
                 "float4-read ops members");
   static_assert(sizeof(WsIn<Q>) % 16 == 0 && offsetof(S, in) % 16 == 0 &&
                 offsetof(WsIn<Q>, tok) % 16 == 0 && offsetof(WsIn<Q>, kg) % 16 == 0 &&
@@ -163,8 +169,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   static_assert(WsLayoutCheck<Q, ST, BOUNDARY>::ok, "layout");
   constexpr int NS = Smem::NS;
   constexpr uint32_t kPageBytes = kDim * kDim * sizeof(ST);
-  constexpr int NR = WsRed<Q>::kN;
-  constexpr int NRP = WsRed<Q>::kPad;
+  constexpr int kBarSolve = 3;  // named barrier of warpgroup 1 (row solve)
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
@@ -393,33 +398,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           gam[t] = g;
           inv[t] = __fdividef(1.f, g);
         }
-        // ---- channel reductions, 32 values at a time ----
+        // ---- channel reductions: |q_t|^2 and |recorded k_t|^2 ----
+        {
+          float v[kWsRed];
 #pragma unroll
-        for (int ch = 0; ch < NRP / 32; ++ch) {
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int idx = ch * 32 + i;
+          for (int i = 0; i < kWsRed; ++i) {
             float val = 0.f;
-            if (idx < Q) {
-              val = kk[idx] * kk[idx];
-            } else if (idx < 2 * Q) {
-              val = qq[idx - Q] * qq[idx - Q];
-            } else if (idx < WsRed<Q>::kPair) {
-              val = kr[idx - 2 * Q] * kr[idx - 2 * Q];
-            } else if (idx < NR) {
-              const int pi = idx - WsRed<Q>::kPair;
-              const int ra = pi / Q, rb = pi - (pi / Q) * Q;
-              if (rb <= ra) {  // B(t = ra, s = rb) = k_s . P(s, t) q_t
-                val = kk[rb] * (gam[ra] * inv[rb]) * qq[ra];
-              } else {         // A(t = rb, s = ra) = k_s . P(s, t) k_t
-                val = kk[ra] * (gam[rb] * inv[ra]) * kk[rb];
-              }
-            }
+            if (i < Q) val = qq[i] * qq[i];
+            else if (i < Q + kMaxQ) val = kr[i - Q] * kr[i - Q];
             v[i] = val;
           }
-          reduce_scatter<32, 32>(v, lane);
-          sm.red[warp][ch * 32 + lane] = v[0];
+          reduce_scatter<kWsRed, 16>(v, lane & 15);
+          v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
+          if (lane < kWsRed) sm.red[warp][lane] = v[0];
         }
       }
       // thread 0: the index chain of item j + 2, then the row of item j + 3
@@ -450,6 +441,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         for (int t = 0; t < Q; ++t) {
           op.xk[t][c] = gam[t] * kk[t];
           op.xq[t][c] = gam[t] * qq[t];
+          op.ex[t][c] = kk[t] * inv[t];
           op.vv[t][c] = bf16_bits_to_f32(in.tok[3][t][c]);
         }
         if (c < Q) op.beta[c] = sigmoidf_fast(braw);
@@ -465,48 +457,26 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           op.dn[c] = fd;
           if constexpr (BOUNDARY) {
             if (it.bslot >= 0) {
-              float fb = 1.f;
+              float rm = 1.f;  // prod_{m <= s < n} d_s
 #pragma unroll
-              for (int t = kMaxQ - 1; t >= 0; --t) {
-                if (t < it.m) {
-                  op.kpb[t][c] = kr[t] * fb;
-                  fb *= dr[t];
-                }
-              }
-              op.db[c] = fb;
+              for (int t = kMaxQ - 1; t >= 0; --t)
+                if (t >= it.m && t < it.n) rm *= dr[t];
+              op.ir[c] = __fdividef(1.f, rm);
             }
           }
         }
         named_bar(kBarPro, 128);
         // ---- final scalars ----
-        if (c < NR) {
-          auto tot = [&](int i) {
-            return (sm.red[0][i] + sm.red[2][i]) + (sm.red[1][i] + sm.red[3][i]);
-          };
-          const float x = tot(c);
-          float val;
-          if (c < Q) {
-            val = rsqrtf(x + kNormEps);
-          } else if (c < 2 * Q) {
-            val = rsqrtf(x + kNormEps) * p.q_scale;
-          } else if (c < WsRed<Q>::kPair) {
-            val = rsqrtf(x + kNormEps);
-          } else {
-            const int pi = c - WsRed<Q>::kPair;
-            const int ra = pi / Q, rb = pi - (pi / Q) * Q;
-            if (rb <= ra) {  // B(t = ra, s = rb)
-              val = x * rsqrtf(tot(rb) + kNormEps) * (rsqrtf(tot(Q + ra) + kNormEps) * p.q_scale);
-            } else {         // A(t = rb, s = ra)
-              val = x * rsqrtf(tot(ra) + kNormEps) * rsqrtf(tot(rb) + kNormEps);
-            }
-          }
-          op.scal[c] = val;
+        if (c < Q + kMaxQ) {
+          const float x = (sm.red[0][c] + sm.red[2][c]) + (sm.red[1][c] + sm.red[3][c]);
+          if (c < Q) op.rsq[c] = rsqrtf(x + kNormEps) * p.q_scale;
+          else op.rsrec[c - Q] = rsqrtf(x + kNormEps);
         }
         named_bar(kBarPro, 128);
         if (REPLAY) {
 #pragma unroll
           for (int t = 0; t < kMaxQ; ++t)
-            if (t < it.n) op.u[t][c] = in.corr[t][c] * op.scal[WsRed<Q>::kRec + t];
+            if (t < it.n) op.u[t][c] = in.corr[t][c] * op.rsrec[t];
         }
         // New key / gate records: the old ones were read above.
         if (it.rec >= 0) {
@@ -604,23 +574,21 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           for (int t = 0; t < kMaxQ; ++t)
             if (t < n) kpr[t] = lds4(&op.kp[t][key]);
           const float4 d4 = lds4(&op.dn[key]);
+          float4 ir4 = make_float4(1.f, 1.f, 1.f, 1.f);
+          if (BOUNDARY && gbnd != nullptr) ir4 = lds4(&op.ir[key]);
 #pragma unroll 1
           for (int i = 0; i < 8; ++i) {
             const int row = rg + 16 * i;
-            const float4 s0 = lds4(fpage + row * kDim + key);
-            if constexpr (BOUNDARY) {
-              if (gbnd != nullptr) {
-                float4 bq = fmul4(s0, lds4(&op.db[key]));
+            float4 sn = fmul4(lds4(fpage + row * kDim + key), d4);
 #pragma unroll
-                for (int t = 0; t < kMaxQ; ++t)
-                  if (t < m) bq = ffma4s(op.u[t][row], lds4(&op.kpb[t][key]), bq);
-                stg4(gbnd + row * kDim + key, bq);
+            for (int t = 0; t < kMaxQ; ++t) {
+              if (t < n) {
+                sn = ffma4s(op.u[t][row], kpr[t], sn);
+                // S_m = (S_0 D_n + sum_{t<m} u_t kp_t) / prod_{m<=s<n} d_s
+                if (BOUNDARY && gbnd != nullptr && t == m - 1)
+                  stg4(gbnd + row * kDim + key, fmul4(sn, ir4));
               }
             }
-            float4 sn = fmul4(s0, d4);
-#pragma unroll
-            for (int t = 0; t < kMaxQ; ++t)
-              if (t < n) sn = ffma4s(op.u[t][row], kpr[t], sn);
             stg4(gpage + row * kDim + key, sn);
             sts4(fpage + row * kDim + key, sn);
           }
@@ -633,25 +601,42 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // ---------------- pass B: 2Q dots per row, Q vectors at a time -------
     constexpr int RB = WsGroup<Q>::kRows;
     constexpr int NV = WsGroup<Q>::kVals;
+    // Lane-XOR order (Q = 2, 4, 8: RB * Q = 16 values for the 16 lanes): lane
+    // l computes value index p ^ l into position p, so each reduction step is
+    // a shuffle of the upper half and an add, with no per-lane select.
+    constexpr bool kXor = (RB * Q == 16) && (Q == 2 || Q == 4 || Q == 8);
+    constexpr int NXG = (Q + RB - 1) / RB;  // groups of pair-product rows
+    const int xperm = kXor ? (l & (Q - 1)) : 0;
+    const int rperm = kXor ? (l / Q) : 0;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float4 xa[Q], xb[Q];
 #pragma unroll
       for (int jj = 0; jj < Q; ++jj) {
-        const float *x = half == 0 ? op.xk[jj] : op.xq[jj];
+        const float *x = half == 0 ? op.xk[jj ^ xperm] : op.xq[jj ^ xperm];
         xa[jj] = lds4(x + ka);
         xb[jj] = lds4(x + kb);
       }
+      // The two row groups of a warp run the same trip count (full-warp
+      // shuffles); a row group past the pair-product rows carries zeros.
+      const int n_groups = 8 / RB + ((rg >> 1) < ((NXG + 1) >> 1) ? 1 : 0);
 #pragma unroll 1
-      for (int i0 = 0; i0 < 8; i0 += RB) {
+      for (int gi = 0; gi < n_groups; ++gi) {
+        const bool extra = gi == 8 / RB;  // the pair-product rows
+        const int base = extra ? rg * RB : gi * RB;
         float vals[NV];
 #pragma unroll
         for (int e = 0; e < NV; ++e) vals[e] = 0.f;
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
-          const int row = rg + 16 * (i0 + r);
-          float4 sa, sb;
-          WsKeys<ST>::load(page, row, l, sa, sb);
+          const int rr = r ^ rperm;  // the row this slot holds
+          float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
+          if (!extra) {
+            WsKeys<ST>::load(page, rg + 16 * (base + rr), l, sa, sb);
+          } else if (base + rr < Q) {
+            sa = lds4(&op.ex[base + rr][ka]);
+            sb = lds4(&op.ex[base + rr][kb]);
+          }
 #pragma unroll
           for (int jj = 0; jj < Q; ++jj) {
             float2 acc = make_float2(0.f, 0.f);
@@ -660,13 +645,26 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             vals[r * Q + jj] = acc.x + acc.y;
           }
         }
-        reduce_scatter<NV, 16>(vals, l);
+        if constexpr (kXor) {
 #pragma unroll
-        for (int e = 0; e < NV / 16; ++e) {
-          const int idx = l * (NV / 16) + e;
-          if (idx < RB * Q) {
-            const int r = idx / Q, jj = idx - (idx / Q) * Q;
-            sm.dots[rg + 16 * (i0 + r)][half * Q + jj] = vals[e];
+          for (int o = 8; o >= 1; o >>= 1) {
+#pragma unroll
+            for (int i = 0; i < o; ++i) vals[i] += __shfl_xor_sync(0xffffffffu, vals[i + o], o);
+          }
+          // vals[0] is the total of value l: row l / Q, dot l % Q
+          const int r = l / Q, jj = l & (Q - 1);
+          if (!extra) sm.dots[rg + 16 * (base + r)][half * Q + jj] = vals[0];
+          else if (base + r < Q) sm.dots_ex[base + r][half * Q + jj] = vals[0];
+        } else {
+          reduce_scatter<NV, 16>(vals, l);
+#pragma unroll
+          for (int e = 0; e < NV / 16; ++e) {
+            const int idx = l * (NV / 16) + e;
+            if (idx < RB * Q) {
+              const int r = idx / Q, jj = idx - (idx / Q) * Q;
+              if (!extra) sm.dots[rg + 16 * (base + r)][half * Q + jj] = vals[e];
+              else if (base + r < Q) sm.dots_ex[base + r][half * Q + jj] = vals[e];
+            }
           }
         }
       }
@@ -680,21 +678,30 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     // ---------------- row solve: warpgroup 1, one state row each --------
     if (mt < kDim) {
+      // normalised pair products from the pair-product rows' dots
+      if (mt < Q * Q) {
+        const int t = mt / Q, s2 = mt - (mt / Q) * Q;
+        const float rks = rsqrtf(sm.dots_ex[s2][s2] + kNormEps);
+        if (s2 < t)
+          sm.fin_a[t][s2] = sm.dots_ex[s2][t] * rks * rsqrtf(sm.dots_ex[t][t] + kNormEps);
+        if (s2 <= t) sm.fin_b[t][s2] = sm.dots_ex[s2][Q + t] * rks * op.rsq[t];
+      }
+      if (mt < Q) sm.rsk[mt] = rsqrtf(sm.dots_ex[mt][mt] + kNormEps);
+      named_bar(kBarSolve, 128);
       const int row = mt;
       float u[Q];
 #pragma unroll
       for (int t = 0; t < Q; ++t) {
-        float a_t = op.vv[t][row] - sm.dots[row][t] * op.scal[t];
+        float a_t = op.vv[t][row] - sm.dots[row][t] * sm.rsk[t];
 #pragma unroll
-        for (int s = 0; s < t; ++s)
-          a_t = fmaf(-op.scal[WsRed<Q>::kPair + s * Q + t], u[s], a_t);
+        for (int s2 = 0; s2 < t; ++s2) a_t = fmaf(-sm.fin_a[t][s2], u[s2], a_t);
         u[t] = op.beta[t] * a_t;
       }
 #pragma unroll
       for (int t = 0; t < Q; ++t) {
-        float o = sm.dots[row][Q + t] * op.scal[Q + t];
+        float o = sm.dots[row][Q + t] * op.rsq[t];
 #pragma unroll
-        for (int s = 0; s <= t; ++s) o = fmaf(op.scal[WsRed<Q>::kPair + t * Q + s], u[s], o);
+        for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sm.fin_b[t][s2], u[s2], o);
         p.out[((tok0 + t) * p.H + h) * kDim + row] = f32_to_bf16_bits(o);
       }
       if (rec >= 0) {

@@ -62,6 +62,7 @@ def _verify_args(**over):
     (dict(q=A + 2), _lib.KDA_ERR_ALIGN), (dict(state=A + 4), _lib.KDA_ERR_ALIGN),
     (dict(slot_stride=2 * 128 * 128 + 1), _lib.KDA_ERR_ALIGN),
     (dict(dtype=7), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(lb=-20.0), _lib.KDA_ERR_UNSUPPORTED), (dict(lb=float("nan")), _lib.KDA_ERR_UNSUPPORTED),
     (dict(B=0), _lib.KDA_OK),
 ])
 def test_verify_host_checks(lib, over, code):
