@@ -110,6 +110,22 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about `hint_ns` passed, instead of spinning (a spinning
+// warp takes issue slots from the warps doing the work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete; gives up
 // after kWaitLimitNs and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar,
@@ -117,7 +133,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar,
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long start = global_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     if (global_ns() - start > kWaitLimitNs) return false;
   }
 }
@@ -170,36 +186,16 @@ __device__ __forceinline__ void sts4(float *p, float4 v) {
 }
 
 // ---------------------------------------------------------------------------
-// packed FP32 pairs (fma.rn.f32x2 / mul / add on sm_100+): one instruction
+// packed FP32 pairs (the float2 FMA / multiply of sm_100+): one instruction
 // for two lanes of FP32 arithmetic, each rounded like the scalar op.
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ unsigned long long f2_bits(float2 v) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
-  return r;
-}
-
-__device__ __forceinline__ float2 bits_f2(unsigned long long r) {
-  float2 v;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
-  return v;
-}
-
-// (a.x * b.x + c.x, a.y * b.y + c.y)
+// (a.x * b.x + c.x, a.y * b.y + c.y), each rounded like the scalar FMA
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(d)
-      : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-  return bits_f2(d);
+  return __ffma2_rn(a, b, c);
 }
 
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(d);
-}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // s (4 floats) <- s * d, elementwise, as two packed multiplies
 __device__ __forceinline__ float4 fmul4(float4 s, float4 d) {

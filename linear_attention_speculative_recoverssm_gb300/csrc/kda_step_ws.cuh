@@ -10,9 +10,13 @@
 //    item's operands into one of two shared "ops" buffers, one item ahead of
 //    the main warpgroups: the decays of this window and of the recorded
 //    tokens, Gamma_t * k_t and Gamma_t * q_t, the replay coefficients
-//    k_t * P_t and D_n, the rows k_s / Gamma_s, the squared norms of q_t and
-//    of the recorded keys reduced over the 128 channels, beta, v, and the
-//    recorded corrections scaled by their key's rsqrt norm.  It also writes
+//    k_t * P_t and D_n, the squared norms of q_t and of the recorded keys
+//    reduced over the 128 channels, beta, v, and the recorded corrections
+//    scaled by their key's rsqrt norm.  The pair products come from Q rows
+//    k_s / Gamma_s dotted with the same vectors as the state rows:
+//    A_ts = (k_s / Gamma_s) . (Gamma_t k_t) (s < t), B_ts = (k_s / Gamma_s)
+//    . (Gamma_t q_t) (s <= t), and the diagonal (k_s / Gamma_s) . (Gamma_s
+//    k_s) is |k_s|^2; the warpgroup normalises them itself.  It also writes
 //    the new key / gate records, after reading the old ones.  Its inputs
 //    arrive by bulk copies one item ahead, so it never waits on HBM.
 //  * Main warpgroups (warps 4-11): a bulk copy (cp.async.bulk + mbarrier)
@@ -23,13 +27,9 @@
 //      pass B: the 2Q dot products of every row with Gamma_t k_t and
 //        Gamma_t q_t, the dot vectors held in registers (Q at a time) so the
 //        state is the only operand streamed from shared memory; packed FP32
-//        FMAs; a reduce-scatter over the 16 lanes of a row.  The same pass
-//        runs Q extra rows k_s / Gamma_s: their dots are the raw pair
-//        products, A_ts = (k_s / Gamma_s) . (Gamma_t k_t) (s < t) and
-//        B_ts = (k_s / Gamma_s) . (Gamma_t q_t) (s <= t), and the diagonal
-//        (k_s / Gamma_s) . (Gamma_s k_s) is |k_s|^2.  Lanes load their
-//        vectors and rows in a lane-XOR-permuted order so the reduce-scatter
-//        needs no selects (one shuffle and one add per pair);
+//        FMAs; a reduce-scatter over the 16 lanes of a row.  Lanes load
+//        their vectors and rows in a lane-XOR-permuted order so the
+//        reduce-scatter needs no selects (one shuffle and one add per pair);
 //      row solve (threads of warpgroup 1, one row each): the forward
 //        substitution u_t = beta_t (v_t - w_t - sum_s A_ts u_s), the outputs
 //        o_t = y_t + sum_s B_ts u_s (BF16) and the corrections u_t (FP32).
@@ -70,6 +70,9 @@ struct alignas(16) WsOps {
   float beta[kMaxQ];
   float rsq[Q];          // rsqrt(|q_t|^2 + eps) * q_scale
   float rsrec[kMaxQ];    // rsqrt(|recorded k_t|^2 + eps)
+  float rsk[Q];          // rsqrt(|k_t|^2 + eps)
+  float fin_a[Q][Q];     // normalised A_ts (s < t)
+  float fin_b[Q][Q];     // normalised B_ts (s <= t)
   int meta[8];  // b, h, slot, rec, n, bslot, m
 };
 
@@ -94,10 +97,7 @@ struct WsSmem {
   WsOps<Q, BOUNDARY> ops[2];
   WsIn<Q> in[2];
   float dots[kDim][2 * Q + 1];  // [row][w_0..w_Q-1, y_0..y_Q-1] (odd pitch)
-  float dots_ex[Q][2 * Q + 1];  // the pair-product rows' dots
-  float fin_a[Q][Q];            // normalised A_ts (s < t)
-  float fin_b[Q][Q];            // normalised B_ts (s <= t)
-  float rsk[Q];                 // rsqrt(|k_t|^2 + eps)
+  float dots_ex[Q][2 * Q + 1];  // prologue: the pair-product rows' dots
   float red[4][kWsRed];
   uint64_t full[NS];
   uint64_t opfull[2];
@@ -154,12 +154,111 @@ struct WsKeys<uint16_t> {
   }
 };
 
-// Rows whose dot products are reduced together: enough for the 16 lanes.
+// Rows whose dot products are reduced together.  For Q = 8 a group holds
+// 32 values (two per lane after the reduction), for Q = 2 and 4 sixteen:
+// then lane l computes value v at position v ^ (l << kShift) and every
+// reduction step is a plain shuffle-and-add (kXor).  Other Q reduce with
+// per-lane selects.
 template <int Q>
 struct WsGroup {
-  static constexpr int kRows = Q >= 8 ? 2 : (Q >= 4 ? 4 : 8);
+  static constexpr int kRows = Q >= 4 ? 4 : 8;
   static constexpr int kVals = round_up(kRows * Q, 16);
+  static constexpr bool kXor = (Q == 2 || Q == 4 || Q == 8) && (kRows * Q == 16 || kRows * Q == 32);
+  static constexpr int kShift = kRows * Q == 32 ? 1 : 0;
 };
+
+// The dots of `rows` state-like rows (RB of them, in the lane-permuted
+// order) with Q vectors held in registers, reduced over the 16 lanes of a
+// row; `emit(r, jj, value)` receives each finished dot.
+template <int Q, typename Load, typename Emit>
+__device__ __forceinline__ void ws_dot_group(const float4 (&xa)[Q], const float4 (&xb)[Q],
+                                             int l, Load load, Emit emit) {
+  using G = WsGroup<Q>;
+  constexpr int RB = G::kRows;
+  constexpr int NV = G::kVals;
+  const int lp = G::kXor ? (l << G::kShift) : 0;
+  const int rperm = lp / Q;         // slot r holds row r ^ rperm
+  const int xperm = lp & (Q - 1);   // x slot jj holds vector jj ^ xperm (set by the caller)
+  (void)xperm;
+  float vals[NV];
+#pragma unroll
+  for (int e = 0; e < NV; ++e) vals[e] = 0.f;
+#pragma unroll
+  for (int r = 0; r < RB; ++r) {
+    float4 sa, sb;
+    load(r ^ rperm, sa, sb);
+#pragma unroll
+    for (int jj = 0; jj < Q; ++jj) {
+      float2 acc = make_float2(0.f, 0.f);
+      acc = dot4_acc(sa, xa[jj], acc);
+      acc = dot4_acc(sb, xb[jj], acc);
+      vals[r * Q + jj] = acc.x + acc.y;
+    }
+  }
+  if constexpr (G::kXor) {
+    constexpr int W = 1 << G::kShift;  // values left per lane
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+#pragma unroll
+      for (int i = 0; i < o * W; ++i) vals[i] += __shfl_xor_sync(0xffffffffu, vals[o * W + i], o);
+    }
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
+      const int v = lp + e;  // value index: row v / Q, dot v % Q
+      emit(v / Q, v & (Q - 1), vals[e]);
+    }
+  } else {
+    reduce_scatter<NV, 16>(vals, l);
+#pragma unroll
+    for (int e = 0; e < NV / 16; ++e) {
+      const int idx = l * (NV / 16) + e;
+      if (idx < RB * Q) emit(idx / Q, idx - (idx / Q) * Q, vals[e]);
+    }
+  }
+}
+
+// The x-register permutation that goes with ws_dot_group.
+template <int Q>
+__device__ __forceinline__ int ws_xperm(int l) {
+  using G = WsGroup<Q>;
+  return G::kXor ? ((l << G::kShift) & (Q - 1)) : 0;
+}
+
+// Pass A for NT pending tokens: S_n = S_0 diag(D_n) + sum_{t<NT} u_t kp_t^T
+// on this thread's 8 rows x 8 keys, stored to HBM and back into the stage;
+// with a boundary slot, S_m (= the partial sum after m terms times
+// 1 / prod_{m<=s<n} d_s) is stored too.  Fully unrolled: no per-token tests.
+template <int NT, bool BOUNDARY, typename Ops>
+__device__ __forceinline__ void ws_replay_rows(const Ops &op, float *fpage, float *gpage,
+                                               float *gbnd, int m, int rg, int ka, int kb) {
+#pragma unroll 1
+  for (int grp = 0; grp < 2; ++grp) {
+    const int key = grp == 0 ? ka : kb;
+    float4 kpr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) kpr[t] = lds4(&op.kp[t][key]);
+    const float4 d4 = lds4(&op.dn[key]);
+    float4 ir4 = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (BOUNDARY && gbnd != nullptr) ir4 = lds4(&op.ir[key]);
+#pragma unroll 2
+    for (int i = 0; i < 8; ++i) {
+      const int row = rg + 16 * i;
+      float u[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) u[t] = op.u[t][row];
+      float4 sn = fmul4(lds4(fpage + row * kDim + key), d4);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        sn = ffma4s(u[t], kpr[t], sn);
+        if constexpr (BOUNDARY) {
+          if (gbnd != nullptr && t == m - 1) stg4(gbnd + row * kDim + key, fmul4(sn, ir4));
+        }
+      }
+      stg4(gpage + row * kDim + key, sn);
+      sts4(fpage + row * kDim + key, sn);
+    }
+  }
+}
 
 template <int Q, typename ST, bool REPLAY, bool BOUNDARY>
 __global__ void __launch_bounds__(kWsThreads, 1)
@@ -169,7 +268,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   static_assert(WsLayoutCheck<Q, ST, BOUNDARY>::ok, "layout");
   constexpr int NS = Smem::NS;
   constexpr uint32_t kPageBytes = kDim * kDim * sizeof(ST);
-  constexpr int kBarSolve = 3;  // named barrier of warpgroup 1 (row solve)
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
@@ -321,13 +419,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
     };
     // per-head / per-token scalars of an item, prefetched one item ahead
-    float dt_n = 0.f, alog_n = 0.f, beta_n = 0.f;
+    // (kept raw: converting here would wait for the loads at once)
+    float dt_n = 0.f, alog_n = 0.f;
+    uint32_t beta_n = 0;
     auto load_small = [&](int i) {
       const int b = (first + i * stride) / p.H;
       const int h = (first + i * stride) - b * p.H;
       dt_n = p.dt_bias[h * kDim + c];
       alog_n = p.A_log[h];
-      beta_n = c < Q ? bf16_bits_to_f32(p.beta[((long long)b * Q + c) * p.H + h]) : 0.f;
+      if (c < Q) beta_n = p.beta[((long long)b * Q + c) * p.H + h];
     };
 
     int requested = 0;  // items whose inputs were requested (warp 0)
@@ -352,7 +452,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     for (int j = 0; j < count; ++j) {
       Ops &op = sm.ops[j & 1];
       const WsIn<Q> &in = sm.in[j & 1];
-      const float dt = dt_n, a = __expf(alog_n), braw = beta_n;
+      const float dt = dt_n, a_log_h = alog_n;
+      const uint32_t braw_bits = beta_n;
       if (j + 1 < count) {
         if (warp == 0) request_inputs(j + 1);
         requested = j + 2;
@@ -379,6 +480,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       // (inputs are re-read from the stage where needed: fewer live registers)
       float kk[Q], qq[Q], gam[Q], inv[Q];
       float kr[kMaxQ], dr[kMaxQ];
+      const float a = __expf(a_log_h);
       if (live) {
 #pragma unroll
         for (int t = 0; t < kMaxQ; ++t) {
@@ -444,7 +546,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           op.ex[t][c] = kk[t] * inv[t];
           op.vv[t][c] = bf16_bits_to_f32(in.tok[3][t][c]);
         }
-        if (c < Q) op.beta[c] = sigmoidf_fast(braw);
+        if (c < Q) op.beta[c] = sigmoidf_fast(bf16_bits_to_f32(braw_bits));
         if (REPLAY && it.n > 0) {
           float fd = 1.f;
 #pragma unroll
@@ -466,17 +568,63 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           }
         }
         named_bar(kBarPro, 128);
-        // ---- final scalars ----
+        // ---- norms of q and of the recorded keys ----
         if (c < Q + kMaxQ) {
           const float x = (sm.red[0][c] + sm.red[2][c]) + (sm.red[1][c] + sm.red[3][c]);
           if (c < Q) op.rsq[c] = rsqrtf(x + kNormEps) * p.q_scale;
           else op.rsrec[c - Q] = rsqrtf(x + kNormEps);
+        }
+        // ---- raw pair products: rows k_s / Gamma_s dotted with the vectors,
+        // QV vectors at a time (fewer live registers than the main pass) ----
+        {
+          constexpr int QV = Q == 8 ? 4 : Q;
+          constexpr int RB = WsGroup<QV>::kRows;
+          const int prg = c >> 4, pl = c & 15;
+          const int pka = WsKeys<float>::a(pl), pkb = WsKeys<float>::b(pl);
+          const int xp = ws_xperm<QV>(pl);
+          const int base = prg * RB;  // rows base .. base + RB - 1 of this row group
+          if ((prg >> 1) * 2 * RB < Q) {  // warp-uniform: a warp holding any of the rows
+#pragma unroll 1
+            for (int chunk = 0; chunk < 2 * (Q / QV); ++chunk) {
+              const int half = chunk / (Q / QV);
+              const int v0 = (chunk - half * (Q / QV)) * QV;  // first vector of the chunk
+              float4 xa[QV], xb[QV];
+#pragma unroll
+              for (int jj = 0; jj < QV; ++jj) {
+                const float *x = half == 0 ? op.xk[v0 + (jj ^ xp)] : op.xq[v0 + (jj ^ xp)];
+                xa[jj] = lds4(x + pka);
+                xb[jj] = lds4(x + pkb);
+              }
+              ws_dot_group<QV>(
+                  xa, xb, pl,
+                  [&](int rr, float4 &sa, float4 &sb) {
+                    const int srow = base + rr;
+                    if (srow < Q) {
+                      sa = lds4(&op.ex[srow][pka]);
+                      sb = lds4(&op.ex[srow][pkb]);
+                    } else {
+                      sa = sb = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                  },
+                  [&](int r, int jj, float v) {
+                    if (base + r < Q) sm.dots_ex[base + r][half * Q + v0 + jj] = v;
+                  });
+            }
+          }
         }
         named_bar(kBarPro, 128);
         if (REPLAY) {
 #pragma unroll
           for (int t = 0; t < kMaxQ; ++t)
             if (t < it.n) op.u[t][c] = in.corr[t][c] * op.rsrec[t];
+        }
+        if (c < Q * Q) {
+          const int t = c / Q, s2 = c - (c / Q) * Q;
+          const float rks = rsqrtf(sm.dots_ex[s2][s2] + kNormEps);
+          if (s2 < t)
+            op.fin_a[t][s2] = sm.dots_ex[s2][t] * rks * rsqrtf(sm.dots_ex[t][t] + kNormEps);
+          if (s2 <= t) op.fin_b[t][s2] = sm.dots_ex[s2][Q + t] * rks * op.rsq[t];
+          if (s2 == t) op.rsk[t] = rks;
         }
         // New key / gate records: the old ones were read above.
         if (it.rec >= 0) {
@@ -563,35 +711,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (BOUNDARY && bslot >= 0)
           gbnd = reinterpret_cast<float *>(p.state) + (long long)bslot * p.slot_stride +
                  (long long)h * (kDim * kDim);
+        // disjoint shared arrays: the stage (read S_0, write S_n in place) and
+        // the corrections; saying so lets the loads run ahead of the stores
         float *fpage = reinterpret_cast<float *>(page);
-        // the lane's two 4-key groups one after the other (half the
-        // coefficient registers live at a time)
-#pragma unroll 1
-        for (int grp = 0; grp < 2; ++grp) {
-          const int key = grp == 0 ? ka : kb;
-          float4 kpr[kMaxQ];
-#pragma unroll
-          for (int t = 0; t < kMaxQ; ++t)
-            if (t < n) kpr[t] = lds4(&op.kp[t][key]);
-          const float4 d4 = lds4(&op.dn[key]);
-          float4 ir4 = make_float4(1.f, 1.f, 1.f, 1.f);
-          if (BOUNDARY && gbnd != nullptr) ir4 = lds4(&op.ir[key]);
-#pragma unroll 1
-          for (int i = 0; i < 8; ++i) {
-            const int row = rg + 16 * i;
-            float4 sn = fmul4(lds4(fpage + row * kDim + key), d4);
-#pragma unroll
-            for (int t = 0; t < kMaxQ; ++t) {
-              if (t < n) {
-                sn = ffma4s(op.u[t][row], kpr[t], sn);
-                // S_m = (S_0 D_n + sum_{t<m} u_t kp_t) / prod_{m<=s<n} d_s
-                if (BOUNDARY && gbnd != nullptr && t == m - 1)
-                  stg4(gbnd + row * kDim + key, fmul4(sn, ir4));
-              }
-            }
-            stg4(gpage + row * kDim + key, sn);
-            sts4(fpage + row * kDim + key, sn);
-          }
+        // n is uniform per item: one predicate-free instance per count
+        switch (n) {
+          case 1: ws_replay_rows<1, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
+          case 2: ws_replay_rows<2, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
+          case 3: ws_replay_rows<3, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
+          case 4: ws_replay_rows<4, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
+          case 5: ws_replay_rows<5, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
+          case 6: ws_replay_rows<6, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
+          case 7: ws_replay_rows<7, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
+          default: ws_replay_rows<8, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
         }
       }
     }
@@ -599,73 +731,30 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // keep pass B's vector loads from being hoisted into pass A (registers)
     asm volatile("" ::: "memory");
     // ---------------- pass B: 2Q dots per row, Q vectors at a time -------
-    constexpr int RB = WsGroup<Q>::kRows;
-    constexpr int NV = WsGroup<Q>::kVals;
-    // Lane-XOR order (Q = 2, 4, 8: RB * Q = 16 values for the 16 lanes): lane
-    // l computes value index p ^ l into position p, so each reduction step is
-    // a shuffle of the upper half and an add, with no per-lane select.
-    constexpr bool kXor = (RB * Q == 16) && (Q == 2 || Q == 4 || Q == 8);
-    constexpr int NXG = (Q + RB - 1) / RB;  // groups of pair-product rows
-    const int xperm = kXor ? (l & (Q - 1)) : 0;
-    const int rperm = kXor ? (l / Q) : 0;
+    {
+      constexpr int RB = WsGroup<Q>::kRows;
+      const int xp = ws_xperm<Q>(l);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float4 xa[Q], xb[Q];
+      for (int half = 0; half < 2; ++half) {
+        float4 xa[Q], xb[Q];
 #pragma unroll
-      for (int jj = 0; jj < Q; ++jj) {
-        const float *x = half == 0 ? op.xk[jj ^ xperm] : op.xq[jj ^ xperm];
-        xa[jj] = lds4(x + ka);
-        xb[jj] = lds4(x + kb);
-      }
-      // The two row groups of a warp run the same trip count (full-warp
-      // shuffles); a row group past the pair-product rows carries zeros.
-      const int n_groups = 8 / RB + ((rg >> 1) < ((NXG + 1) >> 1) ? 1 : 0);
-#pragma unroll 1
-      for (int gi = 0; gi < n_groups; ++gi) {
-        const bool extra = gi == 8 / RB;  // the pair-product rows
-        const int base = extra ? rg * RB : gi * RB;
-        float vals[NV];
-#pragma unroll
-        for (int e = 0; e < NV; ++e) vals[e] = 0.f;
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          const int rr = r ^ rperm;  // the row this slot holds
-          float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
-          if (!extra) {
-            WsKeys<ST>::load(page, rg + 16 * (base + rr), l, sa, sb);
-          } else if (base + rr < Q) {
-            sa = lds4(&op.ex[base + rr][ka]);
-            sb = lds4(&op.ex[base + rr][kb]);
-          }
-#pragma unroll
-          for (int jj = 0; jj < Q; ++jj) {
-            float2 acc = make_float2(0.f, 0.f);
-            acc = dot4_acc(sa, xa[jj], acc);
-            acc = dot4_acc(sb, xb[jj], acc);
-            vals[r * Q + jj] = acc.x + acc.y;
-          }
+        for (int jj = 0; jj < Q; ++jj) {
+          const float *x = half == 0 ? op.xk[jj ^ xp] : op.xq[jj ^ xp];
+          xa[jj] = lds4(x + ka);
+          xb[jj] = lds4(x + kb);
         }
-        if constexpr (kXor) {
-#pragma unroll
-          for (int o = 8; o >= 1; o >>= 1) {
-#pragma unroll
-            for (int i = 0; i < o; ++i) vals[i] += __shfl_xor_sync(0xffffffffu, vals[i + o], o);
-          }
-          // vals[0] is the total of value l: row l / Q, dot l % Q
-          const int r = l / Q, jj = l & (Q - 1);
-          if (!extra) sm.dots[rg + 16 * (base + r)][half * Q + jj] = vals[0];
-          else if (base + r < Q) sm.dots_ex[base + r][half * Q + jj] = vals[0];
-        } else {
-          reduce_scatter<NV, 16>(vals, l);
-#pragma unroll
-          for (int e = 0; e < NV / 16; ++e) {
-            const int idx = l * (NV / 16) + e;
-            if (idx < RB * Q) {
-              const int r = idx / Q, jj = idx - (idx / Q) * Q;
-              if (!extra) sm.dots[rg + 16 * (base + r)][half * Q + jj] = vals[e];
-              else if (base + r < Q) sm.dots_ex[base + r][half * Q + jj] = vals[e];
-            }
-          }
+        const ST *__restrict__ pg = page;                // disjoint from dots
+        float *__restrict__ dp = &sm.dots[0][0];
+#pragma unroll 1
+        for (int i0 = 0; i0 < 8; i0 += RB) {
+          ws_dot_group<Q>(
+              xa, xb, l,
+              [&](int rr, float4 &sa, float4 &sb) {
+                WsKeys<ST>::load(pg, rg + 16 * (i0 + rr), l, sa, sb);
+              },
+              [&](int r, int jj, float v) {
+                dp[(rg + 16 * (i0 + r)) * (2 * Q + 1) + half * Q + jj] = v;
+              });
         }
       }
     }
@@ -678,30 +767,20 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     // ---------------- row solve: warpgroup 1, one state row each --------
     if (mt < kDim) {
-      // normalised pair products from the pair-product rows' dots
-      if (mt < Q * Q) {
-        const int t = mt / Q, s2 = mt - (mt / Q) * Q;
-        const float rks = rsqrtf(sm.dots_ex[s2][s2] + kNormEps);
-        if (s2 < t)
-          sm.fin_a[t][s2] = sm.dots_ex[s2][t] * rks * rsqrtf(sm.dots_ex[t][t] + kNormEps);
-        if (s2 <= t) sm.fin_b[t][s2] = sm.dots_ex[s2][Q + t] * rks * op.rsq[t];
-      }
-      if (mt < Q) sm.rsk[mt] = rsqrtf(sm.dots_ex[mt][mt] + kNormEps);
-      named_bar(kBarSolve, 128);
       const int row = mt;
       float u[Q];
 #pragma unroll
       for (int t = 0; t < Q; ++t) {
-        float a_t = op.vv[t][row] - sm.dots[row][t] * sm.rsk[t];
+        float a_t = op.vv[t][row] - sm.dots[row][t] * op.rsk[t];
 #pragma unroll
-        for (int s2 = 0; s2 < t; ++s2) a_t = fmaf(-sm.fin_a[t][s2], u[s2], a_t);
+        for (int s2 = 0; s2 < t; ++s2) a_t = fmaf(-op.fin_a[t][s2], u[s2], a_t);
         u[t] = op.beta[t] * a_t;
       }
 #pragma unroll
       for (int t = 0; t < Q; ++t) {
         float o = sm.dots[row][Q + t] * op.rsq[t];
 #pragma unroll
-        for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sm.fin_b[t][s2], u[s2], o);
+        for (int s2 = 0; s2 <= t; ++s2) o = fmaf(op.fin_b[t][s2], u[s2], o);
         p.out[((tok0 + t) * p.H + h) * kDim + row] = f32_to_bf16_bits(o);
       }
       if (rec >= 0) {
