@@ -301,8 +301,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     mbar_init(&sm.opfull[1], 1);
     mbar_init(&sm.opempty[0], 1);
     mbar_init(&sm.opempty[1], 1);
-    mbar_init(&sm.infull[0], 1);
-    mbar_init(&sm.infull[1], 1);
+    mbar_init(&sm.infull[0], 128);  // one asynchronous arrival per prologue thread
+    mbar_init(&sm.infull[1], 128);
     mbar_init_fence();
   }
   __syncthreads();
@@ -371,9 +371,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       return it;
     };
-    // Warp 0: the bulk copies of item i's inputs into in[i & 1].
+    // All prologue threads: item i's inputs into in[i & 1] with 16-byte
+    // cp.async copies (the load/store path: they do not queue behind the state
+    // pages in the bulk-copy engine); each thread then arrives on infull once
+    // its own copies have landed.
     auto request_inputs = [&](int i) {
-      __syncwarp();
       ItemMeta m;
       m.b = sm.next_meta[0];
       m.h = sm.next_meta[1];
@@ -382,11 +384,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       m.n = sm.next_meta[4];
       m.bslot = sm.next_meta[5];
       m.m = sm.next_meta[6];
-      __syncwarp();  // thread 0 republishes next_meta after this
       WsIn<Q> &in = sm.in[i & 1];
-      uint64_t *bar = &sm.infull[i & 1];
-      const int nrec = (m.rec >= 0) ? m.n : 0;
-      if (lane == 0) {
+      if (c == 0) {
         in.meta[0] = m.b;
         in.meta[1] = m.h;
         in.meta[2] = m.slot;
@@ -394,29 +393,31 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         in.meta[4] = m.n;
         in.meta[5] = m.bslot;
         in.meta[6] = m.m;
-        if (m.slot >= 0)
-          mbar_arrive_expect_tx(bar, 4u * Q * kDim * 2u + (uint32_t)nrec * 2u * kDim * 4u);
-        else
-          mbar_arrive(bar);
       }
-      __syncwarp();
-      if (m.slot < 0) return;
-      const long long tok0 = (long long)m.b * Q;
-      for (int idx = lane; idx < 4 * Q + 2; idx += 32) {
-        if (idx < 4 * Q) {
-          const int x = idx / Q, t = idx - (idx / Q) * Q;
-          const uint16_t *src = x == 0 ? p.q : (x == 1 ? p.k : (x == 2 ? p.g : p.v));
-          bulk_g2s(in.tok[x][t], src + ((tok0 + t) * p.H + m.h) * kDim, kDim * 2, bar);
-        } else if (nrec > 0 && idx == 4 * Q) {
-          bulk_g2s(in.kg, p.kg + (long long)m.rec * p.kg_row_stride +
-                              (long long)m.h * p.rq * (2 * kDim),
-                   (uint32_t)nrec * 2 * kDim * 2, bar);
-        } else if (nrec > 0) {
-          bulk_g2s(in.corr, p.corr + (long long)m.rec * p.corr_row_stride +
-                                (long long)m.h * p.rq * kDim,
-                   (uint32_t)nrec * kDim * 4, bar);
+      if (m.slot >= 0) {
+        const long long tok0 = (long long)m.b * Q;
+        const int nrec = (m.rec >= 0) ? m.n : 0;
+        constexpr int kTok = 4 * Q * 16;  // 16-byte chunks of the token rows
+        const int total = kTok + nrec * 64;
+        for (int e = c; e < total; e += 128) {
+          if (e < kTok) {
+            const int x = e / (Q * 16), t = (e / 16) % Q, part = e & 15;
+            const uint16_t *src = x == 0 ? p.q : (x == 1 ? p.k : (x == 2 ? p.g : p.v));
+            cp_async16(&in.tok[x][t][part * 8], src + ((tok0 + t) * p.H + m.h) * kDim + part * 8);
+          } else if (e < kTok + nrec * 32) {
+            const int f = e - kTok;  // key / gate rows: 32 chunks each
+            cp_async16(&in.kg[f >> 5][(f & 31) * 8],
+                       p.kg + (long long)m.rec * p.kg_row_stride +
+                           (long long)m.h * p.rq * (2 * kDim) + (long long)f * 8);
+          } else {
+            const int f = e - kTok - nrec * 32;  // corrections: 32 chunks each
+            cp_async16(&in.corr[f >> 5][(f & 31) * 4],
+                       p.corr + (long long)m.rec * p.corr_row_stride +
+                           (long long)m.h * p.rq * kDim + (long long)f * 4);
+          }
         }
       }
+      cp_async_arrive(&sm.infull[i & 1]);
     };
     // per-head / per-token scalars of an item, prefetched one item ahead
     // (kept raw: converting here would wait for the loads at once)
@@ -439,13 +440,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         load_pending();
         publish_next(resolve(0));
       }
-      if (warp == 0) request_inputs(0);
+      named_bar(kBarPro, 128);  // next_meta published
+      request_inputs(0);
+      named_bar(kBarPro, 128);  // next_meta read by every thread
       if (c == 0 && count > 1) {
         load_raw(1);
         load_pending();
         publish_next(resolve(1));
         if (count > 2) load_raw(2);
       }
+      named_bar(kBarPro, 128);  // next_meta published
       load_small(0);
     }
 
@@ -455,7 +459,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const float dt = dt_n, a_log_h = alog_n;
       const uint32_t braw_bits = beta_n;
       if (j + 1 < count) {
-        if (warp == 0) request_inputs(j + 1);
+        request_inputs(j + 1);
         requested = j + 2;
         load_small(j + 1);
       }
@@ -574,27 +578,32 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           if (c < Q) op.rsq[c] = rsqrtf(x + kNormEps) * p.q_scale;
           else op.rsrec[c - Q] = rsqrtf(x + kNormEps);
         }
-        // ---- raw pair products: rows k_s / Gamma_s dotted with the vectors,
-        // QV vectors at a time (fewer live registers than the main pass) ----
+        // ---- raw pair products: rows k_s / Gamma_s dotted with the vectors.
+        // The (half, vector chunk) combinations are spread over the four
+        // warps; each warp's two row groups hold the Q rows. ----
         {
-          constexpr int QV = Q == 8 ? 4 : Q;
+          constexpr int QV = Q == 8 ? 4 : Q;  // vectors per dot call
           constexpr int RB = WsGroup<QV>::kRows;
-          const int prg = c >> 4, pl = c & 15;
+          constexpr int NCHUNK = 2 * (Q / QV);  // (half, chunk) combinations
+          const int prg = (c >> 4) & 1, pl = c & 15;
           const int pka = WsKeys<float>::a(pl), pkb = WsKeys<float>::b(pl);
           const int xp = ws_xperm<QV>(pl);
-          const int base = prg * RB;  // rows base .. base + RB - 1 of this row group
-          if ((prg >> 1) * 2 * RB < Q) {  // warp-uniform: a warp holding any of the rows
 #pragma unroll 1
-            for (int chunk = 0; chunk < 2 * (Q / QV); ++chunk) {
-              const int half = chunk / (Q / QV);
-              const int v0 = (chunk - half * (Q / QV)) * QV;  // first vector of the chunk
-              float4 xa[QV], xb[QV];
+          for (int chunk = warp; chunk < NCHUNK; chunk += 4) {
+            const int half = chunk / (Q / QV);
+            const int v0 = (chunk - half * (Q / QV)) * QV;  // first vector of the chunk
+            float4 xa[QV], xb[QV];
 #pragma unroll
-              for (int jj = 0; jj < QV; ++jj) {
-                const float *x = half == 0 ? op.xk[v0 + (jj ^ xp)] : op.xq[v0 + (jj ^ xp)];
-                xa[jj] = lds4(x + pka);
-                xb[jj] = lds4(x + pkb);
-              }
+            for (int jj = 0; jj < QV; ++jj) {
+              const float *x = half == 0 ? op.xk[v0 + (jj ^ xp)] : op.xq[v0 + (jj ^ xp)];
+              xa[jj] = lds4(x + pka);
+              xb[jj] = lds4(x + pkb);
+            }
+            // both row groups of the warp run every trip (full-warp shuffles);
+            // rows past Q are zeros
+#pragma unroll 1
+            for (int b2 = 0; b2 < Q; b2 += 2 * RB) {
+              const int base = b2 + prg * RB;
               ws_dot_group<QV>(
                   xa, xb, pl,
                   [&](int rr, float4 &sa, float4 &sb) {
@@ -745,7 +754,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         const ST *__restrict__ pg = page;                // disjoint from dots
         float *__restrict__ dp = &sm.dots[0][0];
-#pragma unroll 1
+        // unrolled: one group's loads and FMAs overlap the previous group's
+        // shuffle chain
+#pragma unroll
         for (int i0 = 0; i0 < 8; i0 += RB) {
           ws_dot_group<Q>(
               xa, xb, l,
