@@ -162,6 +162,19 @@ __device__ __forceinline__ void bulk_g2s_hint(void *smem_dst,
       : "memory");
 }
 
+// One tiled tensor copy (3-D box) global -> this CTA's shared memory through
+// the tensor map at `tmap` (a kernel-parameter address), completing its bytes
+// on `bar`.  The innermost coordinate x times the element size must be a
+// multiple of 16 bytes; the shared destination 128-byte aligned.
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, int x, int y, int z,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared through the load/store path
 // (not the bulk-copy engine).  Both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
@@ -260,6 +273,31 @@ __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
 // async-proxy (bulk copy) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory counter increment with acquire-release ordering at CTA
+// scope; returns the prior value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_smem(uint32_t *p, uint32_t v) {
+  uint32_t prior;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(prior)
+               : "r"(smem_u32(p)), "r"(v)
+               : "memory");
+  return prior;
+}
+
+// Hand registers between warpgroups: every thread of the warpgroup executes
+// the same instruction.  The decreases and increases of one CTA must add up
+// to at most the registers it was launched with (threads x registers).
+template <int N>
+__device__ __forceinline__ void warpgroup_reg_dealloc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void warpgroup_reg_alloc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------------------

@@ -2,6 +2,8 @@
 // the per-Q translation units kda_step_q<Q>.cu so they compile in parallel.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -33,6 +35,42 @@ int launch_persistent(const StepParams &p, int n_items, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// The four token-major inputs [B*Q, H, 128] (BF16) as 3-D tensors (128, H,
+// B*Q) with a (128, 1, Q) box: one item's window rows per copy.
+template <int Q>
+int encode_token_maps(const StepParams &p, WsMaps &maps) {
+  const auto encode = tensor_map_encoder();
+  if (encode == nullptr) return KDA_ERR_CUDA;
+  const uint16_t *src[4] = {p.q, p.k, p.g, p.v};
+  const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)p.H, (cuuint64_t)p.B * Q};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)p.H * kDim * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kDim, 1, (cuuint32_t)Q};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  for (int x = 0; x < 4; ++x) {
+    if (encode(&maps.tok[x], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<uint16_t *>(src[x]), dims, strides, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
 template <int Q, typename ST, bool REPLAY, bool BOUNDARY>
 int launch_ws(const StepParams &p, int n_items, cudaStream_t stream) {
   auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY>;
@@ -49,7 +87,10 @@ int launch_ws(const StepParams &p, int n_items, cudaStream_t stream) {
   }
   const int sms = device_sm_count(dev);
   const int grid = n_items < sms ? n_items : sms;
-  kern<<<grid, kWsThreads, smem, stream>>>(p, n_items);
+  WsMaps maps;
+  const int st = encode_token_maps<Q>(p, maps);
+  if (st != KDA_OK) return st;
+  kern<<<grid, kWsThreads, smem, stream>>>(p, maps, n_items);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

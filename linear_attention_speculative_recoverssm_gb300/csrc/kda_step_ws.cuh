@@ -20,25 +20,32 @@
 //    the new key / gate records, after reading the old ones.  Its inputs
 //    arrive by bulk copies one item ahead, so it never waits on HBM.
 //  * Main warpgroups (warps 4-11): a bulk copy (cp.async.bulk + mbarrier)
-//    has brought the item's 64 KB state page into one of NS stages.  Thread
-//    (row group rg = 0..15, lane l = 0..15) owns 8 keys of rows rg + 16 i:
-//      pass A (n > 0): S_n = S_0 diag(D_n) + sum_t u_t (k_t P_t)^T, stored
-//        to HBM and back into the stage in place;
+//    has brought the item's state page into one of NS stages.  Thread (main
+//    warp w, lane 8 rs + c) owns rows 16 w + 4 rs .. + 3 and keys 32 i + 4 c
+//    .. + 3 (i = 0..3) of them, and reads those 64 values into registers;
+//    the last warp to do so requests the next page into the stage.
+//      pass A (n > 0): S_n = S_0 diag(D_n) + sum_t u_t (k_t P_t)^T in
+//        registers, stored to HBM (and the boundary state S_m);
 //      pass B: the 2Q dot products of every row with Gamma_t k_t and
-//        Gamma_t q_t, the dot vectors held in registers (Q at a time) so the
-//        state is the only operand streamed from shared memory; packed FP32
-//        FMAs; a reduce-scatter over the 16 lanes of a row.  Lanes load
-//        their vectors and rows in a lane-XOR-permuted order so the
-//        reduce-scatter needs no selects (one shuffle and one add per pair);
-//      row solve (threads of warpgroup 1, one row each): the forward
-//        substitution u_t = beta_t (v_t - w_t - sum_s A_ts u_s), the outputs
-//        o_t = y_t + sum_s B_ts u_s (BF16) and the corrections u_t (FP32).
-//    When a stage is done the next page is requested into it (NS ahead).
+//        Gamma_t q_t straight from those registers, the vectors read from
+//        shared memory 8 at a time; packed FP32 FMAs; a reduce-scatter over
+//        the 8 lanes of a row group, each lane reading its vectors in a
+//        lane-XOR-permuted order so every step is one shuffle and one add;
+//      row solve, in registers: the forward substitution u_t = beta_t (v_t -
+//        w_t - sum_s A_ts u_s) with u_s broadcast by shuffles within the row
+//        group, the outputs o_t = y_t + sum_s B_ts u_s (BF16) and the
+//        corrections u_t (FP32).
+//    Main warps synchronise only through mbarriers, never a CTA barrier.
 //  * Hand-offs: mbarriers full[stage] (bulk copy landed), opfull[buf] (ops
-//    ready), opempty[buf] (ops consumed).  Every wait is bounded; its
-//    outcome is made uniform across the warpgroup with bar.red.or, and a
-//    timeout is reported in the status word instead of hanging.
+//    ready), opempty[buf] (ops consumed by every main warp), and a counter
+//    per stage whose eighth reader requests the next page into it.  Every
+//    wait is bounded; its outcome is
+//    made uniform across the warp (main) or warpgroup (prologue, with
+//    bar.red.or), and a timeout is reported in the status word instead of
+//    hanging.
 #pragma once
+
+#include <cuda.h>
 
 #include <cstddef>
 
@@ -47,18 +54,33 @@
 namespace kda {
 
 constexpr int kWsThreads = 384;
+// Registers per thread: launched with 168 (the most 384 threads can have);
+// the prologue warpgroup gives some up to the two main warpgroups, whose
+// state tile, partial dots and vectors live in registers.  The split adds up
+// to the launch total: 128 x 136 + 256 x 184 = 384 x 168.
+constexpr int kWsRegsLaunch = 168;
+constexpr int kWsRegsProlog = 136;
+constexpr int kWsRegsMain = 184;
+static_assert(128 * kWsRegsProlog + 256 * kWsRegsMain <= kWsThreads * kWsRegsLaunch,
+              "register split exceeds the launch allocation");
 constexpr int kBarPro = 1;   // named barrier of the prologue warpgroup
-constexpr int kBarMain = 2;  // named barrier of the two main warpgroups
 
 // Reduced over channels by the prologue per item: sum q_t^2 (Q values),
 // then the recorded keys' sums of squares (8 values).
 constexpr int kWsRed = 16;
 
+// Dot vectors of the verify, padded to whole groups of 8 (zeros).
+template <int Q>
+__host__ __device__ constexpr int ws_vectors() {
+  return (2 * Q + 7) / 8 * 8;
+}
+
 // 16-byte aligned so that ops[1] (and every float4 member) stays aligned.
 template <int Q, bool BOUNDARY>
 struct alignas(16) WsOps {
-  float xk[Q][kDim];  // Gamma_t * k_t (unnormalised)
-  float xq[Q][kDim];  // Gamma_t * q_t (unnormalised)
+  // x[t] = Gamma_t * k_t and x[Q + t] = Gamma_t * q_t (unnormalised), then
+  // zero rows up to a multiple of 8 (written once, at kernel start)
+  float x[ws_vectors<Q>()][kDim];
   float ex[Q][kDim];  // k_s / Gamma_s (unnormalised): the pair-product rows
   float kp[kMaxQ][kDim];
   float dn[kDim];
@@ -71,14 +93,22 @@ struct alignas(16) WsOps {
   float rsq[Q];          // rsqrt(|q_t|^2 + eps) * q_scale
   float rsrec[kMaxQ];    // rsqrt(|recorded k_t|^2 + eps)
   float rsk[Q];          // rsqrt(|k_t|^2 + eps)
-  float fin_a[Q][Q];     // normalised A_ts (s < t)
-  float fin_b[Q][Q];     // normalised B_ts (s <= t)
+  float fin_a[Q][Q];     // normalised A_ts (s < t), 0 for s >= t
+  float fin_b[Q][Q];     // normalised B_ts (s <= t), 0 for s > t
   int meta[8];  // b, h, slot, rec, n, bslot, m
 };
 
-// One item's inputs, staged by bulk copies one item ahead of the prologue.
+// Tensor maps of the four token-major BF16 inputs [B*Q, H, 128], in the
+// order q, k, raw_g, v, each as a 3-D tensor (128 channels, H heads, B*Q
+// tokens) whose (128, 1, Q) box is one item's rows of the window.
+struct WsMaps {
+  CUtensorMap tok[4];
+};
+
+// One item's inputs, staged by tensor / bulk copies one item ahead of the
+// prologue (128-byte aligned: tensor-copy destinations).
 template <int Q>
-struct alignas(16) WsIn {
+struct alignas(128) WsIn {
   uint16_t tok[4][Q][kDim];      // q, k, raw_g, v rows of this window (BF16)
   uint16_t kg[kMaxQ][2 * kDim];  // recorded key / raw gate rows (first n)
   float corr[kMaxQ][kDim];       // recorded corrections (first n)
@@ -96,10 +126,10 @@ struct WsSmem {
   ST stage[NS][kDim * kDim];
   WsOps<Q, BOUNDARY> ops[2];
   WsIn<Q> in[2];
-  float dots[kDim][2 * Q + 1];  // [row][w_0..w_Q-1, y_0..y_Q-1] (odd pitch)
   float dots_ex[Q][2 * Q + 1];  // prologue: the pair-product rows' dots
   float red[4][kWsRed];
   uint64_t full[NS];
+  uint32_t sreads[NS];  // main-warp reads of each stage (8 per use)
   uint64_t opfull[2];
   uint64_t opempty[2];
   uint64_t infull[2];
@@ -114,11 +144,12 @@ struct WsLayoutCheck {
   using O = WsOps<Q, BOUNDARY>;
   static_assert(sizeof(O) % 16 == 0, "ops buffers must stay 16-byte aligned");
   static_assert(offsetof(S, stage) % 128 == 0 && offsetof(S, ops) % 16 == 0, "stage / ops");
-  static_assert(offsetof(O, xk) % 16 == 0 && offsetof(O, xq) % 16 == 0 &&
+  static_assert(offsetof(O, x) % 16 == 0 && offsetof(O, u) % 16 == 0 &&
+                offsetof(O, vv) % 16 == 0 &&
                 offsetof(O, kp) % 16 == 0 && offsetof(O, dn) % 16 == 0 &&
                 offsetof(O, ex) % 16 == 0 && offsetof(O, ir) % 16 == 0,
                 "float4-read ops members");
-  static_assert(sizeof(WsIn<Q>) % 16 == 0 && offsetof(S, in) % 16 == 0 &&
+  static_assert(sizeof(WsIn<Q>) % 128 == 0 && offsetof(S, in) % 128 == 0 &&
                 offsetof(WsIn<Q>, tok) % 16 == 0 && offsetof(WsIn<Q>, kg) % 16 == 0 &&
                 offsetof(WsIn<Q>, corr) % 16 == 0, "bulk-copy targets");
   static_assert(offsetof(S, full) % 8 == 0 && offsetof(S, opfull) % 8 == 0 &&
@@ -127,31 +158,12 @@ struct WsLayoutCheck {
   static constexpr bool ok = true;
 };
 
-// The 8 keys of lane l (0..15) in a state row, as two groups of 4: FP32 rows
-// are read as 16 B at 4l and at 64 + 4l (each quarter-warp reads 128
-// contiguous bytes); BF16 rows as 16 B holding keys 8l .. 8l + 7.
-template <typename ST>
-struct WsKeys;
-template <>
-struct WsKeys<float> {
+// The prologue's pair-product dots: lane l (0..15) of a row takes the 8 keys
+// 4l .. 4l + 3 and 64 + 4l .. 64 + 4l + 3 (each quarter-warp reads 128
+// contiguous bytes).
+struct WsKeys {
   __device__ static int a(int l) { return 4 * l; }
   __device__ static int b(int l) { return 64 + 4 * l; }
-  __device__ static void load(const float *page, int row, int l, float4 &sa, float4 &sb) {
-    sa = lds4(page + row * kDim + 4 * l);
-    sb = lds4(page + row * kDim + 64 + 4 * l);
-  }
-};
-template <>
-struct WsKeys<uint16_t> {
-  __device__ static int a(int l) { return 8 * l; }
-  __device__ static int b(int l) { return 8 * l + 4; }
-  __device__ static void load(const uint16_t *page, int row, int l, float4 &sa, float4 &sb) {
-    const uint4 w = *reinterpret_cast<const uint4 *>(page + row * kDim + 8 * l);
-    sa = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-    sb = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
-                     __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
-  }
 };
 
 // Rows whose dot products are reduced together.  For Q = 8 a group holds
@@ -224,45 +236,180 @@ __device__ __forceinline__ int ws_xperm(int l) {
   return G::kXor ? ((l << G::kShift) & (Q - 1)) : 0;
 }
 
-// Pass A for NT pending tokens: S_n = S_0 diag(D_n) + sum_{t<NT} u_t kp_t^T
-// on this thread's 8 rows x 8 keys, stored to HBM and back into the stage;
-// with a boundary slot, S_m (= the partial sum after m terms times
-// 1 / prod_{m<=s<n} d_s) is stored too.  Fully unrolled: no per-token tests.
+// ---------------------------------------------------------------------------
+// Main warpgroups.  Thread (main warp w = 0..7, lane = 8 rs + c) owns state
+// rows R0 .. R0 + 3 with R0 = 16 w + 4 rs, and the 16 keys 32 i + 4 c .. + 3
+// (i = 0..3) of each: every warp access to a key chunk covers 128 contiguous
+// bytes per row, and the 8 lanes c of a row group split the 128 keys.
+// ---------------------------------------------------------------------------
+
+// The thread's 4 x 16 state values from a stage (FP32 or BF16 page).
+template <typename ST>
+struct WsTile;
+template <>
+struct WsTile<float> {
+  __device__ static void load(const float *page, int R0, int c, float4 (&s)[4][4]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[r][i] = lds4(page + (R0 + r) * kDim + 32 * i + 4 * c);
+  }
+};
+template <>
+struct WsTile<uint16_t> {
+  __device__ static void load(const uint16_t *page, int R0, int c, float4 (&s)[4][4]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(page + (R0 + r) * kDim + 32 * i + 4 * c);
+        s[r][i] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                              __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+      }
+  }
+};
+
+// Pass A for NT pending tokens, in registers:
+// S_n = S_0 diag(D_n) + sum_{t<NT} u_t kp_t^T, stored to HBM; with a boundary
+// slot, S_m (= the partial sum after m terms times 1 / prod_{m<=s<n} d_s) is
+// stored too.  Fully unrolled: no per-token tests but the boundary's.
 template <int NT, bool BOUNDARY, typename Ops>
-__device__ __forceinline__ void ws_replay_rows(const Ops &op, float *fpage, float *gpage,
-                                               float *gbnd, int m, int rg, int ka, int kb) {
-#pragma unroll 1
-  for (int grp = 0; grp < 2; ++grp) {
-    const int key = grp == 0 ? ka : kb;
-    float4 kpr[NT];
+__device__ __forceinline__ void ws_replay(float4 (&s)[4][4], const Ops &op, float *gpage,
+                                          float *gbnd, int m, int R0, int c) {
 #pragma unroll
-    for (int t = 0; t < NT; ++t) kpr[t] = lds4(&op.kp[t][key]);
-    const float4 d4 = lds4(&op.dn[key]);
-    float4 ir4 = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (BOUNDARY && gbnd != nullptr) ir4 = lds4(&op.ir[key]);
-#pragma unroll 2
-    for (int i = 0; i < 8; ++i) {
-      const int row = rg + 16 * i;
-      float u[NT];
+  for (int i = 0; i < 4; ++i) {
+    const float4 d4 = lds4(&op.dn[32 * i + 4 * c]);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) u[t] = op.u[t][row];
-      float4 sn = fmul4(lds4(fpage + row * kDim + key), d4);
+    for (int r = 0; r < 4; ++r) s[r][i] = fmul4(s[r][i], d4);
+  }
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        sn = ffma4s(u[t], kpr[t], sn);
-        if constexpr (BOUNDARY) {
-          if (gbnd != nullptr && t == m - 1) stg4(gbnd + row * kDim + key, fmul4(sn, ir4));
+  for (int t = 0; t < NT; ++t) {
+    const float4 u4 = lds4(&op.u[t][R0]);
+    const float ur[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 k4 = lds4(&op.kp[t][32 * i + 4 * c]);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) s[r][i] = ffma4s(ur[r], k4, s[r][i]);
+    }
+    if constexpr (BOUNDARY) {
+      if (gbnd != nullptr && t == m - 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 ir4 = lds4(&op.ir[32 * i + 4 * c]);
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            stg4(gbnd + (R0 + r) * kDim + 32 * i + 4 * c, fmul4(s[r][i], ir4));
         }
       }
-      stg4(gpage + row * kDim + key, sn);
-      sts4(fpage + row * kDim + key, sn);
     }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) stg4(gpage + (R0 + r) * kDim + 32 * i + 4 * c, s[r][i]);
+}
+
+// Pass B: the dots of the thread's 4 rows with the dot vectors, 8 vectors
+// (one group) at a time, reduced over the 8 lanes c of the row group.  Lane
+// c takes vector 8 g + (j ^ c) in register slot j, so value (slot j, row r)
+// at position 4 j + r is the logical value (4 j + r) ^ 4 c, and every step of
+// the reduce-scatter is one shuffle and one add; lane c ends with the dots
+// of vector 8 g + c with its 4 rows: d[g][r].
+template <int NG>
+__device__ __forceinline__ void ws_dots(const float4 (&s)[4][4], const float *__restrict__ xv,
+                                        int c, float (&d)[NG][4]) {
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    float p[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float *x = xv + (8 * g + (j ^ c)) * kDim + 4 * c;
+      float4 x4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x4[i] = lds4(x + 32 * i);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float2 acc = fmul2(make_float2(s[r][0].x, s[r][0].y), make_float2(x4[0].x, x4[0].y));
+        acc = ffma2(make_float2(s[r][0].z, s[r][0].w), make_float2(x4[0].z, x4[0].w), acc);
+#pragma unroll
+        for (int i = 1; i < 4; ++i) acc = dot4_acc(s[r][i], x4[i], acc);
+        p[4 * j + r] = acc.x + acc.y;
+      }
+    }
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 4 * o; ++i) p[i] += __shfl_xor_sync(0xffffffffu, p[4 * o + i], o);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) d[g][r] = p[r];
+  }
+}
+
+// Row solve of the thread's 4 rows, in registers.  After pass B lane c
+// holds w_c (c < Q) in group 0 and y_t for t = 8 g + c - Q (when that is in
+// 0 .. Q-1) in group g.  For s = 0 .. Q-1 the lane holding w_s has finished
+// its residual v_s - w_s rsk_s - sum_{s'<s} A_ss' u_s'; u_s = beta_s times it
+// is broadcast to the row group and folded into every lane's residual (the
+// A coefficient is 0 for s >= t) and outputs (the B coefficient is 0 for
+// s > t).  Writes o_t (BF16) and, with a record row, u_t (FP32).
+template <int Q, int NG, typename Ops>
+__device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
+                                         const StepParams &p, long long tok0, int h, int rec,
+                                         int R0, int c, int lane) {
+  const int cw = c < Q ? c : Q - 1;  // lanes without a w role compute unused values
+  const float4 v4 = lds4(&op.vv[cw][R0]);
+  const float rk = op.rsk[cw], bt = op.beta[cw];
+  float res[4] = {fmaf(-d[0][0], rk, v4.x), fmaf(-d[0][1], rk, v4.y), fmaf(-d[0][2], rk, v4.z),
+                  fmaf(-d[0][3], rk, v4.w)};
+  float acoef[Q];
+#pragma unroll
+  for (int s2 = 0; s2 < Q; ++s2) acoef[s2] = op.fin_a[cw][s2];
+  bool hy[NG];
+  int ty[NG];
+  float oacc[NG][4], bcoef[NG][Q];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const int V = 8 * g + c;
+    hy[g] = V >= Q && V < 2 * Q;
+    ty[g] = hy[g] ? V - Q : 0;
+    const float rq = op.rsq[ty[g]];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) oacc[g][r] = d[g][r] * rq;
+#pragma unroll
+    for (int s2 = 0; s2 < Q; ++s2) bcoef[g][s2] = op.fin_b[ty[g]][s2];
+  }
+  const int base = lane & ~7;
+#pragma unroll
+  for (int s2 = 0; s2 < Q; ++s2) {
+    float us[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) us[r] = __shfl_sync(0xffffffffu, bt * res[r], base + s2);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) res[r] = fmaf(-acoef[s2], us[r], res[r]);
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) oacc[g][r] = fmaf(bcoef[g][s2], us[r], oacc[g][r]);
+  }
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    if (hy[g]) {
+      const uint2 o2 = make_uint2(pack_bf16x2(oacc[g][0], oacc[g][1]),
+                                  pack_bf16x2(oacc[g][2], oacc[g][3]));
+      *reinterpret_cast<uint2 *>(p.out + ((tok0 + ty[g]) * p.H + h) * kDim + R0) = o2;
+    }
+  }
+  if (c < Q && rec >= 0) {
+    const long long cbase = (long long)rec * p.corr_row_stride + ((long long)h * p.rq + c) * kDim;
+    stg4(p.corr + cbase + R0, make_float4(bt * res[0], bt * res[1], bt * res[2], bt * res[3]));
   }
 }
 
 template <int Q, typename ST, bool REPLAY, bool BOUNDARY>
 __global__ void __launch_bounds__(kWsThreads, 1)
-    kda_step_ws(const StepParams p, int n_items) {
+    kda_step_ws(const StepParams p, const __grid_constant__ WsMaps maps, int n_items) {
   using Smem = WsSmem<Q, ST, BOUNDARY>;
   using Ops = WsOps<Q, BOUNDARY>;
   static_assert(WsLayoutCheck<Q, ST, BOUNDARY>::ok, "layout");
@@ -296,18 +443,28 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
   if (tid == 0) {
 #pragma unroll
-    for (int s = 0; s < NS; ++s) mbar_init(&sm.full[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sm.full[s], 1);
+      sm.sreads[s] = 0;
+    }
     mbar_init(&sm.opfull[0], 1);
     mbar_init(&sm.opfull[1], 1);
-    mbar_init(&sm.opempty[0], 1);
-    mbar_init(&sm.opempty[1], 1);
-    mbar_init(&sm.infull[0], 128);  // one asynchronous arrival per prologue thread
-    mbar_init(&sm.infull[1], 128);
+    mbar_init(&sm.opempty[0], 8);  // one arrival per main warp
+    mbar_init(&sm.opempty[1], 8);
+    mbar_init(&sm.infull[0], 1);  // thread 0's arrival with the copies' byte count
+    mbar_init(&sm.infull[1], 1);
     mbar_init_fence();
+  }
+  // the padding dot vectors (rows 2Q .. of x) stay zero in both ops buffers
+  constexpr int kPadFloats = (ws_vectors<Q>() - 2 * Q) * kDim;
+  if constexpr (kPadFloats > 0) {
+    for (int e = tid; e < 2 * kPadFloats; e += kWsThreads)
+      sm.ops[e / kPadFloats].x[2 * Q + (e % kPadFloats) / kDim][e % kDim] = 0.f;
   }
   __syncthreads();
 
   if (warp < 4) {
+    warpgroup_reg_dealloc<kWsRegsProlog>();
     // =====================================================================
     // prologue warpgroup: thread c owns key channel c
     // =====================================================================
@@ -371,11 +528,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       return it;
     };
-    // All prologue threads: item i's inputs into in[i & 1] with 16-byte
-    // cp.async copies (the load/store path: they do not queue behind the state
-    // pages in the bulk-copy engine); each thread then arrives on infull once
-    // its own copies have landed.
+    // Thread 0: item i's inputs into in[i & 1]: the window's q, k, raw_g and
+    // v rows by four tensor copies, the first n recorded key / gate rows and
+    // corrections by one bulk copy each, all completing on infull[i & 1].
     auto request_inputs = [&](int i) {
+      if (c != 0) return;
       ItemMeta m;
       m.b = sm.next_meta[0];
       m.h = sm.next_meta[1];
@@ -385,39 +542,32 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       m.bslot = sm.next_meta[5];
       m.m = sm.next_meta[6];
       WsIn<Q> &in = sm.in[i & 1];
-      if (c == 0) {
-        in.meta[0] = m.b;
-        in.meta[1] = m.h;
-        in.meta[2] = m.slot;
-        in.meta[3] = m.rec;
-        in.meta[4] = m.n;
-        in.meta[5] = m.bslot;
-        in.meta[6] = m.m;
+      in.meta[0] = m.b;
+      in.meta[1] = m.h;
+      in.meta[2] = m.slot;
+      in.meta[3] = m.rec;
+      in.meta[4] = m.n;
+      in.meta[5] = m.bslot;
+      in.meta[6] = m.m;
+      uint64_t *bar = &sm.infull[i & 1];
+      if (m.slot < 0) {
+        mbar_arrive(bar);
+        return;
       }
-      if (m.slot >= 0) {
-        const long long tok0 = (long long)m.b * Q;
-        const int nrec = (m.rec >= 0) ? m.n : 0;
-        constexpr int kTok = 4 * Q * 16;  // 16-byte chunks of the token rows
-        const int total = kTok + nrec * 64;
-        for (int e = c; e < total; e += 128) {
-          if (e < kTok) {
-            const int x = e / (Q * 16), t = (e / 16) % Q, part = e & 15;
-            const uint16_t *src = x == 0 ? p.q : (x == 1 ? p.k : (x == 2 ? p.g : p.v));
-            cp_async16(&in.tok[x][t][part * 8], src + ((tok0 + t) * p.H + m.h) * kDim + part * 8);
-          } else if (e < kTok + nrec * 32) {
-            const int f = e - kTok;  // key / gate rows: 32 chunks each
-            cp_async16(&in.kg[f >> 5][(f & 31) * 8],
-                       p.kg + (long long)m.rec * p.kg_row_stride +
-                           (long long)m.h * p.rq * (2 * kDim) + (long long)f * 8);
-          } else {
-            const int f = e - kTok - nrec * 32;  // corrections: 32 chunks each
-            cp_async16(&in.corr[f >> 5][(f & 31) * 4],
-                       p.corr + (long long)m.rec * p.corr_row_stride +
-                           (long long)m.h * p.rq * kDim + (long long)f * 4);
-          }
-        }
+      const int nrec = (m.rec >= 0) ? m.n : 0;
+      constexpr uint32_t kTokBytes = 4u * Q * kDim * 2u;
+      const uint32_t rec_bytes = (uint32_t)nrec * kDim * 4u;  // per record tensor
+      mbar_arrive_expect_tx(bar, kTokBytes + 2u * rec_bytes);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) tma_load_3d(&in.tok[x][0][0], &maps.tok[x], 0, m.h, m.b * Q, bar);
+      if (nrec > 0) {
+        bulk_g2s(&in.kg[0][0],
+                 p.kg + (long long)m.rec * p.kg_row_stride + (long long)m.h * p.rq * (2 * kDim),
+                 rec_bytes, bar);
+        bulk_g2s(&in.corr[0][0],
+                 p.corr + (long long)m.rec * p.corr_row_stride + (long long)m.h * p.rq * kDim,
+                 rec_bytes, bar);
       }
-      cp_async_arrive(&sm.infull[i & 1]);
     };
     // per-head / per-token scalars of an item, prefetched one item ahead
     // (kept raw: converting here would wait for the loads at once)
@@ -545,8 +695,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (live) {
 #pragma unroll
         for (int t = 0; t < Q; ++t) {
-          op.xk[t][c] = gam[t] * kk[t];
-          op.xq[t][c] = gam[t] * qq[t];
+          op.x[t][c] = gam[t] * kk[t];
+          op.x[Q + t][c] = gam[t] * qq[t];
           op.ex[t][c] = kk[t] * inv[t];
           op.vv[t][c] = bf16_bits_to_f32(in.tok[3][t][c]);
         }
@@ -586,7 +736,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           constexpr int RB = WsGroup<QV>::kRows;
           constexpr int NCHUNK = 2 * (Q / QV);  // (half, chunk) combinations
           const int prg = (c >> 4) & 1, pl = c & 15;
-          const int pka = WsKeys<float>::a(pl), pkb = WsKeys<float>::b(pl);
+          const int pka = WsKeys::a(pl), pkb = WsKeys::b(pl);
           const int xp = ws_xperm<QV>(pl);
 #pragma unroll 1
           for (int chunk = warp; chunk < NCHUNK; chunk += 4) {
@@ -595,7 +745,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             float4 xa[QV], xb[QV];
 #pragma unroll
             for (int jj = 0; jj < QV; ++jj) {
-              const float *x = half == 0 ? op.xk[v0 + (jj ^ xp)] : op.xq[v0 + (jj ^ xp)];
+              const float *x = op.x[half * Q + v0 + (jj ^ xp)];
               xa[jj] = lds4(x + pka);
               xb[jj] = lds4(x + pkb);
             }
@@ -630,9 +780,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (c < Q * Q) {
           const int t = c / Q, s2 = c - (c / Q) * Q;
           const float rks = rsqrtf(sm.dots_ex[s2][s2] + kNormEps);
-          if (s2 < t)
-            op.fin_a[t][s2] = sm.dots_ex[s2][t] * rks * rsqrtf(sm.dots_ex[t][t] + kNormEps);
-          if (s2 <= t) op.fin_b[t][s2] = sm.dots_ex[s2][Q + t] * rks * op.rsq[t];
+          op.fin_a[t][s2] =
+              s2 < t ? sm.dots_ex[s2][t] * rks * rsqrtf(sm.dots_ex[t][t] + kNormEps) : 0.f;
+          op.fin_b[t][s2] = s2 <= t ? sm.dots_ex[s2][Q + t] * rks * op.rsq[t] : 0.f;
           if (s2 == t) op.rsk[t] = rks;
         }
         // New key / gate records: the old ones were read above.
@@ -661,24 +811,41 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   // =======================================================================
   // main warpgroups
   // =======================================================================
+  warpgroup_reg_alloc<kWsRegsMain>();
+  constexpr int NG = ws_vectors<Q>() / 8;
   const int mt = tid - 128;
-  const int rg = mt >> 4, l = mt & 15;
+  const int c = lane & 7, R0 = 16 * (mt >> 5) + 4 * (lane >> 3);
   const bool leader = mt == 0;
-  const int ka = WsKeys<ST>::a(l), kb = WsKeys<ST>::b(l);
-  int issued = 0;   // pages requested (leader)
-  int consumed = 0;  // items whose page wait was reached
+  int issued_hi = 0;  // lane 0: one past the last item whose page this warp requested
+  int consumed = 0;   // items whose page this warp has read (or skipped, inert)
   if (leader) {
-    for (; issued < NS && issued < count; ++issued) issue(issued, item_slot(issued));
+    for (; issued_hi < NS && issued_hi < count; ++issued_hi) issue(issued_hi, item_slot(issued_hi));
   }
+  // Every main warp counts its read of item j's stage; the eighth (last)
+  // reader requests item j + NS's page into it, so no warp waits for another.
+  auto stage_read = [&](int j, int next_slot) {
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t prior = atom_add_acq_rel_smem(&sm.sreads[j % NS], 1u);
+      if ((prior & 7u) == 7u && j + NS < count) {
+        issue(j + NS, next_slot);
+        issued_hi = j + NS + 1;
+      }
+    }
+  };
+  auto warp_arrive = [&](uint64_t *bar) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  };
+  bool failed = false;
   for (int j = 0; j < count; ++j) {
-    // prefetch the slot of the item whose page will reuse this stage
+    // the slot of the item whose page may follow this one into its stage
     int next_slot = -1;
-    if (leader && j + NS < count) next_slot = item_slot(j + NS);
+    if (lane == 0 && j + NS < count) next_slot = item_slot(j + NS);
 
-    consumed = j;
     bool ok = mbar_wait_bounded(&sm.opfull[j & 1], (uint32_t)((j >> 1) & 1));
-    if (named_bar_or(kBarMain, 256, !ok)) {
-      if (leader) report(p.status, KDA_ERR_TIMEOUT);
+    if (__any_sync(0xffffffffu, !ok)) {
+      failed = true;
       break;
     }
     const Ops &op = sm.ops[j & 1];
@@ -687,29 +854,25 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const long long tok0 = (long long)b * Q;
 
     if (slot < 0) {
-      for (int e = mt; e < Q * kDim; e += 256) {
-        const int t = e / kDim, ch = e - t * kDim;
-        p.out[((tok0 + t) * p.H + h) * kDim + ch] = 0;
-      }
-      named_bar(kBarMain, 256);
-      if (leader) {
-        mbar_arrive(&sm.opempty[j & 1]);
-        if (j + NS < count) {
-          issue(j + NS, next_slot);
-          ++issued;
-        }
-      }
-      consumed = j + 1;  // an inert item's stage phase completed on issue
+      // inert item: zero outputs (lane c: token c of its 4 rows); the
+      // stage's phase was completed when the item was issued
+      if (c < Q)
+        *reinterpret_cast<uint2 *>(p.out + ((tok0 + c) * p.H + h) * kDim + R0) = make_uint2(0, 0);
+      stage_read(j, next_slot);
+      warp_arrive(&sm.opempty[j & 1]);
+      consumed = j + 1;
       continue;
     }
 
     ok = mbar_wait_bounded(&sm.full[j % NS], (uint32_t)((j / NS) & 1));
-    if (named_bar_or(kBarMain, 256, !ok)) {
-      if (leader) report(p.status, KDA_ERR_TIMEOUT);
+    if (__any_sync(0xffffffffu, !ok)) {
+      failed = true;
       break;
     }
     consumed = j + 1;
-    ST *page = sm.stage[j % NS];
+    float4 st[4][4];
+    WsTile<ST>::load(sm.stage[j % NS], R0, c, st);
+    stage_read(j, next_slot);
 
     // ---------------- pass A: replay, write-back (n > 0) ----------------
     if constexpr (REPLAY) {
@@ -720,95 +883,33 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (BOUNDARY && bslot >= 0)
           gbnd = reinterpret_cast<float *>(p.state) + (long long)bslot * p.slot_stride +
                  (long long)h * (kDim * kDim);
-        // disjoint shared arrays: the stage (read S_0, write S_n in place) and
-        // the corrections; saying so lets the loads run ahead of the stores
-        float *fpage = reinterpret_cast<float *>(page);
         // n is uniform per item: one predicate-free instance per count
         switch (n) {
-          case 1: ws_replay_rows<1, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
-          case 2: ws_replay_rows<2, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
-          case 3: ws_replay_rows<3, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
-          case 4: ws_replay_rows<4, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
-          case 5: ws_replay_rows<5, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
-          case 6: ws_replay_rows<6, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
-          case 7: ws_replay_rows<7, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
-          default: ws_replay_rows<8, BOUNDARY>(op, fpage, gpage, gbnd, m, rg, ka, kb); break;
+          case 1: ws_replay<1, BOUNDARY>(st, op, gpage, gbnd, m, R0, c); break;
+          case 2: ws_replay<2, BOUNDARY>(st, op, gpage, gbnd, m, R0, c); break;
+          case 3: ws_replay<3, BOUNDARY>(st, op, gpage, gbnd, m, R0, c); break;
+          case 4: ws_replay<4, BOUNDARY>(st, op, gpage, gbnd, m, R0, c); break;
+          case 5: ws_replay<5, BOUNDARY>(st, op, gpage, gbnd, m, R0, c); break;
+          case 6: ws_replay<6, BOUNDARY>(st, op, gpage, gbnd, m, R0, c); break;
+          case 7: ws_replay<7, BOUNDARY>(st, op, gpage, gbnd, m, R0, c); break;
+          default: ws_replay<8, BOUNDARY>(st, op, gpage, gbnd, m, R0, c); break;
         }
       }
     }
 
-    // keep pass B's vector loads from being hoisted into pass A (registers)
-    asm volatile("" ::: "memory");
-    // ---------------- pass B: 2Q dots per row, Q vectors at a time -------
-    {
-      constexpr int RB = WsGroup<Q>::kRows;
-      const int xp = ws_xperm<Q>(l);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float4 xa[Q], xb[Q];
-#pragma unroll
-        for (int jj = 0; jj < Q; ++jj) {
-          const float *x = half == 0 ? op.xk[jj ^ xp] : op.xq[jj ^ xp];
-          xa[jj] = lds4(x + ka);
-          xb[jj] = lds4(x + kb);
-        }
-        const ST *__restrict__ pg = page;                // disjoint from dots
-        float *__restrict__ dp = &sm.dots[0][0];
-        // unrolled: one group's loads and FMAs overlap the previous group's
-        // shuffle chain
-#pragma unroll
-        for (int i0 = 0; i0 < 8; i0 += RB) {
-          ws_dot_group<Q>(
-              xa, xb, l,
-              [&](int rr, float4 &sa, float4 &sb) {
-                WsKeys<ST>::load(pg, rg + 16 * (i0 + rr), l, sa, sb);
-              },
-              [&](int r, int jj, float v) {
-                dp[(rg + 16 * (i0 + r)) * (2 * Q + 1) + half * Q + jj] = v;
-              });
-        }
-      }
-    }
-    if (REPLAY && n > 0) fence_proxy_async_smem();  // pass A wrote the stage
-    named_bar(kBarMain, 256);  // dots complete, the stage is free
-    if (leader && j + NS < count) {
-      issue(j + NS, next_slot);
-      ++issued;
-    }
+    // ---------------- pass B: 2Q dots per row ----------------------------
+    float d[NG][4];
+    ws_dots<NG>(st, &op.x[0][0], c, d);
 
-    // ---------------- row solve: warpgroup 1, one state row each --------
-    if (mt < kDim) {
-      const int row = mt;
-      float u[Q];
-#pragma unroll
-      for (int t = 0; t < Q; ++t) {
-        float a_t = op.vv[t][row] - sm.dots[row][t] * op.rsk[t];
-#pragma unroll
-        for (int s2 = 0; s2 < t; ++s2) a_t = fmaf(-op.fin_a[t][s2], u[s2], a_t);
-        u[t] = op.beta[t] * a_t;
-      }
-#pragma unroll
-      for (int t = 0; t < Q; ++t) {
-        float o = sm.dots[row][Q + t] * op.rsq[t];
-#pragma unroll
-        for (int s2 = 0; s2 <= t; ++s2) o = fmaf(op.fin_b[t][s2], u[s2], o);
-        p.out[((tok0 + t) * p.H + h) * kDim + row] = f32_to_bf16_bits(o);
-      }
-      if (rec >= 0) {
-        const long long cbase = (long long)rec * p.corr_row_stride +
-                                (long long)h * p.rq * kDim + row;
-#pragma unroll
-        for (int t = 0; t < Q; ++t) p.corr[cbase + t * kDim] = u[t];
-      }
-    }
-    named_bar(kBarMain, 256);  // ops and dots consumed
-    if (leader) mbar_arrive(&sm.opempty[j & 1]);
-    consumed = j + 1;
+    // ---------------- row solve, outputs, corrections --------------------
+    ws_solve<Q, NG>(d, op, p, tok0, h, rec, R0, c, lane);
+    warp_arrive(&sm.opempty[j & 1]);
   }
-  // After a timeout, copies requested but never waited for may still be in
+  if (failed && lane == 0) report(p.status, KDA_ERR_TIMEOUT);
+  // After a timeout, pages this warp requested but never read may still be in
   // flight: let them land (bounded) before this CTA's shared memory goes.
-  if (leader) {
-    for (int jj = consumed; jj < issued; ++jj)
+  if (lane == 0) {
+    for (int jj = consumed; jj < issued_hi; ++jj)
       mbar_wait_bounded(&sm.full[jj % NS], (uint32_t)((jj / NS) & 1));
   }
 }
