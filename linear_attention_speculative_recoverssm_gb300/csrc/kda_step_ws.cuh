@@ -319,21 +319,29 @@ __device__ __forceinline__ void ws_replay(float4 (&s)[4][4], const Ops &op, floa
 template <int NG>
 __device__ __forceinline__ void ws_dots(const float4 (&s)[4][4], const float *__restrict__ xv,
                                         int c, float (&d)[NG][4]) {
+  // vectors of the next slot are loaded while the current slot's FMAs run
+  auto load_slot = [&](int v, float4 (&x4)[4]) {
+    const float *x = xv + (8 * (v >> 3) + ((v & 7) ^ c)) * kDim + 4 * c;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x4[i] = lds4(x + 32 * i);
+  };
+  float4 xa[4], xb[4];
+  load_slot(0, xa);
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     float p[32];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float *x = xv + (8 * g + (j ^ c)) * kDim + 4 * c;
-      float4 x4[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x4[i] = lds4(x + 32 * i);
+      const int v = 8 * g + j;
+      float4(&cur)[4] = (v & 1) ? xb : xa;
+      float4(&nxt)[4] = (v & 1) ? xa : xb;
+      if (v + 1 < 8 * NG) load_slot(v + 1, nxt);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        float2 acc = fmul2(make_float2(s[r][0].x, s[r][0].y), make_float2(x4[0].x, x4[0].y));
-        acc = ffma2(make_float2(s[r][0].z, s[r][0].w), make_float2(x4[0].z, x4[0].w), acc);
+        float2 acc = fmul2(make_float2(s[r][0].x, s[r][0].y), make_float2(cur[0].x, cur[0].y));
+        acc = ffma2(make_float2(s[r][0].z, s[r][0].w), make_float2(cur[0].z, cur[0].w), acc);
 #pragma unroll
-        for (int i = 1; i < 4; ++i) acc = dot4_acc(s[r][i], x4[i], acc);
+        for (int i = 1; i < 4; ++i) acc = dot4_acc(s[r][i], cur[i], acc);
         p[4 * j + r] = acc.x + acc.y;
       }
     }
