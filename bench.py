@@ -283,6 +283,178 @@ def workload_config(case, name):
 
 
 # ---------------------------------------------------------------------------
+# the other rows of the step: standalone commit, mid-size batch, the cluster
+# split's small-batch latencies, the bookkeeping kernels
+# ---------------------------------------------------------------------------
+
+def commit_algorithmic_bytes(c):
+    """Bytes one standalone commit must move: per live (layer, request, head)
+    item the source page read, the destination page written, the boundary
+    page written when the boundary is live, and the n recorded corrections
+    (FP32) and key / gate rows (BF16) read."""
+    L, B, H, Q = c["L"], c["B"], c["H"], c["Q"]
+    esz = c["layers"][0]["state"].dtype.itemsize
+    page = DIM * DIM * esz
+    total = 0
+    for b in range(B):
+        n = min(max(int(c["commit_lens"][b]), 0), Q)
+        live = n > 0 and c["sources"][b] > c["null_slot"] and c["destinations"][b] > c["null_slot"]
+        if not live:
+            continue
+        per = 2 * page + n * (DIM * 4 + 2 * DIM * 2)
+        if c["boundaries"][b] > c["null_slot"] and c["boundary_lens"][b] > 0:
+            per += page
+        total += L * H * per
+    return total
+
+
+def _event_ms(stream, fn, iters):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def measure_rows(dev, stream, peak, cpu_seconds):
+    """Timings of the step's other rows (CUDA events on the launching stream;
+    every pool below is larger than L2 except the latency sweep's, which is a
+    latency measurement by design)."""
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import (KDA_STATE_BF16, kda_commit,
+                                                               kda_defer_commit, kda_flush_plan,
+                                                               kda_replay_verify, layer_tables,
+                                                               synth)
+    rows = {}
+
+    def dt(a):
+        return (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
+                else torch.from_numpy(a)).to(dev)
+
+    # standalone commit, BF16 pools, 4 layers
+    name = "commit-bf16-l4-h32-b64-q4-align"
+    c = synth.make(name)
+    states = [dt(lay["state"]) for lay in c["layers"]]
+    corrs = [dt(lay["corr"]) for lay in c["layers"]]
+    kgs = [dt(lay["key_gate"]) for lay in c["layers"]]
+    tabs = layer_tables(states, corrs, kgs, dev)
+    ct = {k: dt(c[k]) for k in ("A_log", "dt_bias", "sources", "commit_lens", "destinations",
+                                "boundaries", "boundary_lens")}
+
+    def commit():
+        kda_commit(*tabs, ct["A_log"], ct["dt_bias"], ct["sources"], ct["commit_lens"],
+                   ct["destinations"], state_dtype=KDA_STATE_BF16, lower_bound=c["lower_bound"],
+                   L=c["L"], H=c["H"], B=c["B"], Q=c["Q"], n_slots=states[0].shape[0],
+                   n_rows=corrs[0].shape[0], boundaries=ct["boundaries"],
+                   boundary_lens=ct["boundary_lens"], stream=stream)
+    for _ in range(5):
+        commit()
+    ms = _event_ms(stream, commit, 50)
+    nbytes = commit_algorithmic_bytes(c)
+    row = dict(workload=name, ms=ms, bytes_per_launch=nbytes,
+               roofline=dict(bound="hbm", achieved=nbytes / ms / 1e6, peak=peak, unit="GB/s",
+                             frac=nbytes / ms / 1e6 / peak))
+    if cpu_seconds > 0:
+        from oracle import kda_oracle as ko
+        L, B, H = c["L"], c["B"], c["H"]
+        items = np.random.default_rng(0).permutation(L * B * H)
+        ref = [{k: v.copy() for k, v in lay.items()} for lay in c["layers"]]
+        t0, done = time.perf_counter(), 0
+        while done < len(items) and time.perf_counter() - t0 < cpu_seconds:
+            ko.commit(layers=ref, A_log=c["A_log"], dt_bias=c["dt_bias"], sources=c["sources"],
+                      commit_lens=c["commit_lens"], destinations=c["destinations"],
+                      lower_bound=c["lower_bound"], Q=c["Q"], B=B, H=H,
+                      boundaries=c["boundaries"], boundary_lens=c["boundary_lens"],
+                      items=items[done:done + 64])
+            done += len(items[done:done + 64])
+        secs = time.perf_counter() - t0
+        row["cpu_baseline"] = dict(ms=1e3 * secs * len(items) / done, cores=1, kind="oracle",
+                                   sample=f"{done} of {len(items)} (layer, request, head) items, "
+                                          f"{secs:.1f} s on one core, scaled to the launch")
+    rows["commit"] = row
+    del states, corrs, kgs, tabs
+
+    # fused step on the mid-size batch
+    name = "replay-verify-f32-h32-b128-q4"
+    c = synth.make(name)
+    names = ("q", "k", "v", "raw_g", "raw_beta", "A_log", "dt_bias", "state", "state_slots",
+             "record_rows", "pending", "corr", "key_gate")
+    d = {n: dt(c[n]) for n in names}
+    out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"],
+                          d["dt_bias"], d["state"], d["state_slots"], d["record_rows"],
+                          d["pending"], d["corr"], d["key_gate"], out, Q=c["Q"],
+                          lower_bound=c["lower_bound"], q_scale=c["q_scale"], split=0,
+                          stream=stream)
+    for _ in range(5):
+        step()
+    ms = _event_ms(stream, step, 50)
+    ab = algorithmic_bytes(c)
+    row = dict(workload=name, ms=ms, tok_s=ab["live_tokens"] / (ms / 1e3),
+               bytes_per_launch=ab["total"],
+               roofline=dict(bound="hbm", achieved=ab["total"] / ms / 1e6, peak=peak, unit="GB/s",
+                             frac=ab["total"] / ms / 1e6 / peak))
+    if cpu_seconds > 0:
+        rate, items, secs = oracle_rate(c, cpu_seconds)
+        row["cpu_baseline"] = dict(value=rate, unit="tok/s", cores=1, kind="oracle",
+                                   sample=f"{items} live items, {secs:.1f} s on one core")
+    rows["replay_verify_mid_batch"] = row
+    del d, out
+
+    # small batches: per-launch device time (a CUDA graph of 20 launches)
+    lat = {}
+    for B in (1, 4, 16):
+        for Q in (1, 2, 4, 8):
+            c = synth.latency_case(B=B, Q=Q)
+            d = {n: dt(c[n]) for n in names}
+            out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
+            res = {}
+            for split in (1, 2, 4):
+                def one(split=split):
+                    kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"],
+                                      d["A_log"], d["dt_bias"], d["state"], d["state_slots"],
+                                      d["record_rows"], d["pending"], d["corr"], d["key_gate"],
+                                      out, Q=Q, lower_bound=c["lower_bound"],
+                                      q_scale=c["q_scale"], split=split,
+                                      stream=torch.cuda.current_stream())
+                for _ in range(3):
+                    one()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for _ in range(20):
+                        one()
+                g.replay()
+                torch.cuda.synchronize()
+                res[f"split{split}"] = 1e3 * _event_ms(torch.cuda.current_stream(), g.replay,
+                                                       10) / 20
+            lat[f"B{B}_q{Q}"] = res
+    rows["latency_us_h32"] = lat
+
+    # bookkeeping (defer, then flush plan) for 512 requests
+    rng = np.random.default_rng(7)
+    B = 512
+    slots = torch.from_numpy(rng.integers(-1, 1024, B).astype(np.int32)).to(dev)
+    rrows = torch.from_numpy(rng.permutation(B).astype(np.int32)).to(dev)
+    pend = torch.zeros(B, dtype=torch.int32, device=dev)
+    lens = torch.from_numpy(rng.integers(0, 9, B).astype(np.int32)).to(dev)
+    plan = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(4)]
+
+    def book():
+        kda_defer_commit(slots, lens, rrows, pend, stream=stream)
+        kda_flush_plan(slots, rrows, pend, *plan, Q=8, stream=stream)
+    for _ in range(5):
+        book()
+    rows["bookkeeping_us_b512"] = 1e3 * _event_ms(stream, book, 50)
+    return rows
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -403,6 +575,10 @@ def run_ours(args):
     achieved = ab["total"] / (avg_kernel_ms / 1e3) / 1e9
     state_gbs = ab["state"] / (avg_kernel_ms / 1e3) / 1e9
 
+    rows = None
+    if rank == 0 and not args.no_rows:
+        rows = measure_rows(dev, stream, peak, 0.0 if args.no_cpu_baseline else 3.0)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, items, secs = oracle_rate(case, args.cpu_seconds)
@@ -426,7 +602,7 @@ def run_ours(args):
                           peak_source="MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks
                           else "fallback 6.8 TB/s",
                           bytes_per_launch=ab["total"], state_bytes_per_launch=ab["state"]),
-            cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps, clocks=clocks,
+            cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps, clocks=clocks, rows=rows,
         )
         print(json.dumps(line))
     if world > 1:
@@ -442,6 +618,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the commit / mid-batch / latency / bookkeeping timings")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--traffic", type=float, default=None,

@@ -4,16 +4,26 @@
 // align boundary state; class KdaCommit: per-layer address tables, source /
 // length / destination / boundary arrays, null slot).
 //
-// Design: persistent CTAs (one per SM) walk the (layer, request, head)
-// items; thread 0 streams each live item's source page (32 KB BF16 or 64 KB
-// FP32) into a ring of shared-memory stages with one bulk copy per page, NS
-// pages ahead.  Threads 0-127 build key channel c's replay coefficients
-// (recorded key times the suffix decay product, D_n, and the same for the
-// boundary length), threads 128-255 fetch the recorded corrections; then
-// every thread folds 2 rows x 32 keys of the page in registers and stores
-// the result (and the boundary state) straight to global memory.  The
-// product form of the decays is used instead of the log form (the same
-// quantity; it saves one exp per coefficient).
+// Design (one CTA per SM, 384 threads, items (layer, request, head) strided
+// over the grid):
+//  * prologue warpgroup (warps 0-3, thread c <-> key channel c): thread 0
+//    resolves the item chain two items ahead and stages each live item's
+//    recorded key / gate rows and corrections with two bulk copies, one item
+//    ahead; every thread then builds channel c's replay coefficients
+//    (recorded key times the suffix decay product, D_n, the boundary's
+//    1 / prod_{m<=s<n} d_s) and the corrections scaled by their key's rsqrt
+//    norm into one of two shared "ops" buffers.  The product form of the
+//    decays is used instead of the log form (the same quantity; it saves one
+//    exp per coefficient).
+//  * main warpgroups (warps 4-11): each live item's source page (32 KB BF16
+//    or 64 KB FP32) arrives by one bulk copy in a ring of NS stages; thread
+//    (main warp w, lane 8 rs + c) reads rows 16 w + 4 rs .. + 3, keys
+//    32 i + 4 c .. + 3 into registers, and the last warp to read a stage
+//    requests the page NS items ahead into it.  S_n = S_0 D_n +
+//    sum_t u_t (k_t P_t)^T is formed in registers and stored to the
+//    destination (rounded once for a BF16 pool); the boundary state is the
+//    partial sum after m terms times 1 / prod_{m<=s<n} d_s.
+//  * every wait is bounded; a timeout is reported in the status word.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -25,7 +35,8 @@
 namespace kda {
 namespace {
 
-constexpr int kCommitThreads = 256;
+constexpr int kCommitThreads = 384;
+constexpr int kCmBarPro = 1;  // named barrier of the prologue warpgroup
 
 struct CommitParams {
   const uint64_t *state_ptrs, *corr_ptrs, *kg_ptrs;
@@ -38,118 +49,212 @@ struct CommitParams {
   int32_t *status;
 };
 
+// One item's operands, built by the prologue.
+struct alignas(16) CmOps {
+  float kp[kMaxQ][kDim];  // recorded k_t * prod_{t<s<n} d_s
+  float dn[kDim];         // prod_{s<n} d_s
+  float ir[kDim];         // 1 / prod_{m<=s<n} d_s (boundary)
+  float u[kMaxQ][kDim];   // recorded u_t[row] * rsqrt(|k_t|^2 + eps)
+  unsigned long long dst, bnd;  // destination / boundary page (0: none)
+  int meta[4];                  // live, n, m
+};
+
+// One item's records and gate bias, staged by bulk copies, and its resolved
+// indices (written by the thread that requests the copies).
+struct alignas(16) CmIn {
+  uint16_t kg[kMaxQ][2 * kDim];
+  float corr[kMaxQ][kDim];
+  float dt[kDim];
+  unsigned long long dst, bnd;
+  float a;       // exp(A_log) of the item's (layer, head)
+  int meta[3];   // live, n, m
+};
+
 template <typename ST>
 struct CommitSmem {
-  static constexpr int NS = sizeof(ST) == 2 ? 6 : 3;
+  static constexpr int NS = sizeof(ST) == 2 ? 4 : 2;
   ST stage[NS][kDim * kDim];
-  float kp[kMaxQ][kDim];
-  float dn[kDim];
-  float kpb[kMaxQ][kDim];
-  float db[kDim];
-  float uold[kMaxQ][kDim];
+  CmOps ops[2];
+  CmIn in[2];
   float red[4][kMaxQ];
   uint64_t full[NS];
+  uint64_t opfull[2];
+  uint64_t opempty[2];
+  uint64_t infull[2];
+  uint32_t sreads[NS];
 };
 
 template <typename ST>
 struct CommitLayoutCheck {
   using S = CommitSmem<ST>;
-  static_assert(offsetof(S, stage) % 128 == 0 && offsetof(S, kp) % 16 == 0 &&
-                offsetof(S, dn) % 16 == 0 && offsetof(S, kpb) % 16 == 0 &&
-                offsetof(S, db) % 16 == 0 && offsetof(S, full) % 8 == 0,
-                "float4-read members / barrier alignment");
+  static_assert(sizeof(CmOps) % 16 == 0 && sizeof(CmIn) % 16 == 0, "buffer strides");
+  static_assert(offsetof(S, stage) % 128 == 0 && offsetof(S, ops) % 16 == 0 &&
+                offsetof(S, in) % 16 == 0 && offsetof(CmOps, kp) % 16 == 0 &&
+                offsetof(CmOps, dn) % 16 == 0 && offsetof(CmOps, ir) % 16 == 0 &&
+                offsetof(CmOps, u) % 16 == 0 && offsetof(CmIn, kg) % 16 == 0 &&
+                offsetof(CmIn, corr) % 16 == 0 && offsetof(CmIn, dt) % 16 == 0,
+                "float4-read members / bulk-copy targets");
+  static_assert(offsetof(S, full) % 8 == 0 && offsetof(S, opfull) % 8 == 0 &&
+                offsetof(S, opempty) % 8 == 0 && offsetof(S, infull) % 8 == 0, "mbarriers");
+  static_assert(sizeof(S) <= 232448, "shared memory per CTA");
   static constexpr bool ok = true;
 };
 static_assert(CommitLayoutCheck<float>::ok && CommitLayoutCheck<uint16_t>::ok, "layout");
 
-struct CommitItem {
-  int l, b, h;
-  bool live;
-  int src, dst, row, n, bslot, m;
+// The per-request / per-layer values an item depends on, loaded without
+// branching on them (so the loads can be issued well before they are used).
+struct CommitRaw {
+  int n, src, dst, row, bs, blen;
+  uint64_t sp, cp, kp;
+  int64_t ss, cs, ks;
 };
 
-template <typename ST, bool ALIGN>
-__device__ __forceinline__ CommitItem commit_item(const CommitParams &p,
-                                                  int item, bool report_errors) {
+__device__ __forceinline__ CommitRaw commit_raw(const CommitParams &p, bool align, int item) {
+  CommitRaw r;
+  const int b = (item / p.H) % p.B, l = item / (p.H * p.B);
+  r.n = p.commit_lens[b];
+  r.src = p.sources[b];
+  r.dst = p.destinations[b];
+  r.row = p.record_rows != nullptr ? p.record_rows[b] : b;
+  r.bs = align ? p.boundaries[b] : -1;
+  r.blen = align ? p.boundary_lens[b] : 0;
+  r.sp = p.state_ptrs[l];
+  r.cp = p.corr_ptrs[l];
+  r.kp = p.kg_ptrs[l];
+  r.ss = p.state_strides[l];
+  r.cs = p.corr_strides[l];
+  r.ks = p.kg_strides[l];
+  return r;
+}
+
+struct CommitItem {
+  bool live;
+  int l, h, n, m;
+  unsigned long long src, dst, bnd;  // page addresses
+  unsigned long long kg, corr;       // record addresses of the item
+};
+
+// Liveness and addresses of an item: live = n > 0, source and destination
+// above the null slot, record row >= 0; indices outside their pools or
+// misaligned tables make the item dead (and are reported when asked).
+template <typename ST>
+__device__ __forceinline__ CommitItem commit_resolve(const CommitParams &p, int item,
+                                                     const CommitRaw &r, bool report_errors) {
   CommitItem it;
   it.h = item % p.H;
-  it.b = (item / p.H) % p.B;
   it.l = item / (p.H * p.B);
-  int n = p.commit_lens[it.b];
-  n = n > p.Q ? p.Q : n;
+  const int n = r.n > p.Q ? p.Q : r.n;
   it.n = n;
-  it.src = p.sources[it.b];
-  it.dst = p.destinations[it.b];
-  it.row = p.record_rows != nullptr ? p.record_rows[it.b] : it.b;
-  it.live = n > 0 && it.src > p.null_slot && it.dst > p.null_slot && it.row >= 0;
-  it.bslot = -1;
   it.m = 0;
+  it.src = it.dst = it.bnd = it.kg = it.corr = 0;
+  it.live = n > 0 && r.src > p.null_slot && r.dst > p.null_slot && r.row >= 0;
   if (!it.live) return it;
-  bool bad = it.src >= p.n_slots || it.dst >= p.n_slots || it.row >= p.n_rows;
-  const uint64_t sp = p.state_ptrs[it.l], cp = p.corr_ptrs[it.l], kp = p.kg_ptrs[it.l];
-  const bool misaligned = ((sp | cp | kp) & 15) != 0 ||
-                          ((p.state_strides[it.l] * (int64_t)sizeof(ST)) & 15) != 0 ||
-                          ((p.corr_strides[it.l] * 4) & 15) != 0 ||
-                          ((p.kg_strides[it.l] * 2) & 15) != 0;
+  const bool bad = r.src >= p.n_slots || r.dst >= p.n_slots || r.row >= p.n_rows;
+  const bool misaligned = ((r.sp | r.cp | r.kp) & 15) != 0 ||
+                          ((r.ss * (int64_t)sizeof(ST)) & 15) != 0 || ((r.cs * 4) & 15) != 0 ||
+                          ((r.ks * 2) & 15) != 0;
   if (bad || misaligned) {
     if (report_errors) report(p.status, misaligned ? KDA_ERR_ALIGN : KDA_ERR_ARG);
     it.live = false;
     return it;
   }
-  if (ALIGN && p.boundaries != nullptr) {
-    const int bs = p.boundaries[it.b];
-    int m = p.boundary_lens[it.b];
-    m = m > p.Q ? p.Q : m;
-    if (bs >= p.n_slots) {
-      if (report_errors) report(p.status, KDA_ERR_ARG);
-    } else if (m > 0 && bs > p.null_slot) {
-      it.bslot = bs;
-      it.m = m < n ? m : n;
-    }
+  const unsigned long long hoff = (unsigned long long)it.h * (kDim * kDim) * sizeof(ST);
+  it.src = r.sp + (unsigned long long)(r.src * r.ss) * sizeof(ST) + hoff;
+  it.dst = r.sp + (unsigned long long)(r.dst * r.ss) * sizeof(ST) + hoff;
+  it.kg = r.kp + ((unsigned long long)r.row * r.ks + (unsigned long long)it.h * p.Q * 2 * kDim) * 2;
+  it.corr = r.cp + ((unsigned long long)r.row * r.cs + (unsigned long long)it.h * p.Q * kDim) * 4;
+  if (r.bs >= p.n_slots) {
+    if (report_errors) report(p.status, KDA_ERR_ARG);
+  } else if (r.blen > 0 && r.bs > p.null_slot) {
+    const int m = r.blen > p.Q ? p.Q : r.blen;
+    it.m = m < n ? m : n;
+    it.bnd = r.sp + (unsigned long long)(r.bs * r.ss) * sizeof(ST) + hoff;
   }
   return it;
 }
 
+// The thread's 4 x 16 tile of a stage, as FP32.
 template <typename ST>
-__device__ __forceinline__ ST *commit_page(const CommitParams &p, int l, int slot, int h) {
-  return reinterpret_cast<ST *>(p.state_ptrs[l]) + (long long)slot * p.state_strides[l] +
-         (long long)h * (kDim * kDim);
+__device__ __forceinline__ void cm_load_tile(const ST *page, int R0, int c, float4 (&s)[4][4]);
+template <>
+__device__ __forceinline__ void cm_load_tile<float>(const float *page, int R0, int c,
+                                                    float4 (&s)[4][4]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[r][i] = lds4(page + (R0 + r) * kDim + 32 * i + 4 * c);
+}
+template <>
+__device__ __forceinline__ void cm_load_tile<uint16_t>(const uint16_t *page, int R0, int c,
+                                                       float4 (&s)[4][4]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 w = *reinterpret_cast<const uint2 *>(page + (R0 + r) * kDim + 32 * i + 4 * c);
+      s[r][i] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                            __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    }
 }
 
+// Four values of a row to a page (BF16: rounded to nearest even).
 template <typename ST>
-__device__ __forceinline__ float4 load_page4(const ST *page, int row, int key);
+__device__ __forceinline__ void cm_store4(unsigned long long page, int row, int key, float4 v);
 template <>
-__device__ __forceinline__ float4 load_page4<float>(const float *page, int row, int key) {
-  return lds4(page + row * kDim + key);
+__device__ __forceinline__ void cm_store4<float>(unsigned long long page, int row, int key,
+                                                 float4 v) {
+  stg4(reinterpret_cast<float *>(page) + row * kDim + key, v);
 }
 template <>
-__device__ __forceinline__ float4 load_page4<uint16_t>(const uint16_t *page, int row, int key) {
-  const uint2 w = *reinterpret_cast<const uint2 *>(page + row * kDim + key);
-  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+__device__ __forceinline__ void cm_store4<uint16_t>(unsigned long long page, int row, int key,
+                                                    float4 v) {
+  *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(page) + row * kDim + key) =
+      make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 
-template <typename ST>
-__device__ __forceinline__ void store_page4(ST *page, int row, int key, float4 v);
-template <>
-__device__ __forceinline__ void store_page4<float>(float *page, int row, int key, float4 v) {
-  stg4(page + row * kDim + key, v);
-}
-template <>
-__device__ __forceinline__ void store_page4<uint16_t>(uint16_t *page, int row, int key, float4 v) {
-  uint2 w;
-  w.x = pack_bf16x2(v.x, v.y);
-  w.y = pack_bf16x2(v.z, v.w);
-  *reinterpret_cast<uint2 *>(page + row * kDim + key) = w;
+// The fold for NT tokens on the thread's tile (boundary after m terms).
+template <typename ST, int NT, bool ALIGN>
+__device__ __forceinline__ void cm_fold(float4 (&s)[4][4], const CmOps &op, unsigned long long dst,
+                                        unsigned long long bnd, int m, int R0, int c) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 d4 = lds4(&op.dn[32 * i + 4 * c]);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) s[r][i] = fmul4(s[r][i], d4);
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const float4 u4 = lds4(&op.u[t][R0]);
+    const float ur[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 k4 = lds4(&op.kp[t][32 * i + 4 * c]);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) s[r][i] = ffma4s(ur[r], k4, s[r][i]);
+    }
+    if constexpr (ALIGN) {
+      if (bnd != 0 && t == m - 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 ir4 = lds4(&op.ir[32 * i + 4 * c]);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) cm_store4<ST>(bnd, R0 + r, 32 * i + 4 * c, fmul4(s[r][i], ir4));
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cm_store4<ST>(dst, R0 + r, 32 * i + 4 * c, s[r][i]);
 }
 
 template <typename ST, bool ALIGN>
 __global__ void __launch_bounds__(kCommitThreads, 1)
-    kda_commit_persistent(const CommitParams p, int n_items) {
+    kda_commit_ws(const CommitParams p, int n_items) {
   using Smem = CommitSmem<ST>;
   constexpr int NS = Smem::NS;
   constexpr uint32_t kPageBytes = kDim * kDim * sizeof(ST);
-  constexpr int kRotate = sizeof(ST) == 4 ? 1 : 3;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
 
@@ -157,160 +262,242 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int first = blockIdx.x, stride = gridDim.x;
   const int count = first < n_items ? (n_items - first + stride - 1) / stride : 0;
+  auto item_of = [&](int j) { return first + j * stride; };
 
-  if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < NS; ++s) mbar_init(&sm.full[s], 1);
-    mbar_init_fence();
-  }
-  __syncthreads();
-
-  auto issue = [&](int j) {
-    const CommitItem it = commit_item<ST, ALIGN>(p, first + j * stride, false);
+  // Page of item j into stage j % NS (any one thread).
+  auto issue = [&](int j, unsigned long long src) {
     uint64_t *bar = &sm.full[j % NS];
-    if (it.live) {
+    if (src != 0) {
       mbar_arrive_expect_tx(bar, kPageBytes);
-      bulk_g2s(sm.stage[j % NS], commit_page<ST>(p, it.l, it.src, it.h), kPageBytes, bar);
+      bulk_g2s(sm.stage[j % NS], reinterpret_cast<const void *>(src), kPageBytes, bar);
     } else {
       mbar_arrive(bar);
     }
   };
+  auto page_of = [&](int j) {
+    const int item = item_of(j);
+    const CommitItem it = commit_resolve<ST>(p, item, commit_raw(p, ALIGN, item), false);
+    return it.live ? it.src : 0ull;
+  };
+
   if (tid == 0) {
-    for (int j = 0; j < NS && j < count; ++j) issue(j);
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sm.full[s], 1);
+      sm.sreads[s] = 0;
+    }
+    mbar_init(&sm.opfull[0], 1);
+    mbar_init(&sm.opfull[1], 1);
+    mbar_init(&sm.opempty[0], 8);  // one arrival per main warp
+    mbar_init(&sm.opempty[1], 8);
+    mbar_init(&sm.infull[0], 1);
+    mbar_init(&sm.infull[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp < 4) {
+    // =====================================================================
+    // prologue warpgroup: thread c owns key channel c
+    // =====================================================================
+    const int c = tid;
+    // thread 0's item chain: raw values of item j + 2, resolved item j + 1
+    CommitRaw raw2{};
+    CommitItem nxt{};
+    auto request = [&](int i, const CommitItem &it) {  // thread 0
+      uint64_t *bar = &sm.infull[i & 1];
+      CmIn &in = sm.in[i & 1];
+      in.meta[0] = it.live ? 1 : 0;
+      in.meta[1] = it.n;
+      in.meta[2] = it.m;
+      in.dst = it.dst;
+      in.bnd = it.bnd;
+      if (!it.live) {
+        mbar_arrive(bar);
+        return;
+      }
+      in.a = __expf(p.A_log[it.l * p.H + it.h]);
+      const uint32_t bytes = (uint32_t)it.n * kDim * 4u;  // per record tensor
+      mbar_arrive_expect_tx(bar, 2u * bytes + kDim * 4u);
+      bulk_g2s(&in.kg[0][0], reinterpret_cast<const void *>(it.kg), bytes, bar);
+      bulk_g2s(&in.corr[0][0], reinterpret_cast<const void *>(it.corr), bytes, bar);
+      bulk_g2s(&in.dt[0], p.dt_bias + ((long long)it.l * p.H + it.h) * kDim, kDim * 4u, bar);
+    };
+    int requested = 0, taken = 0;
+    if (c == 0 && count > 0) {
+      const CommitItem it0 = commit_resolve<ST>(p, item_of(0), commit_raw(p, ALIGN, item_of(0)), true);
+      request(0, it0);
+      requested = 1;
+      if (count > 1) nxt = commit_resolve<ST>(p, item_of(1), commit_raw(p, ALIGN, item_of(1)), true);
+      if (count > 2) raw2 = commit_raw(p, ALIGN, item_of(2));
+    }
+    bool failed = false;
+    for (int j = 0; j < count; ++j) {
+      CmOps &op = sm.ops[j & 1];
+      const CmIn &in = sm.in[j & 1];
+      if (c == 0 && j + 1 < count) {
+        request(j + 1, nxt);
+        requested = j + 2;
+        if (j + 2 < count) nxt = commit_resolve<ST>(p, item_of(j + 2), raw2, true);
+        if (j + 3 < count) raw2 = commit_raw(p, ALIGN, item_of(j + 3));
+      }
+      bool ok = mbar_wait_bounded(&sm.infull[j & 1], (uint32_t)((j >> 1) & 1));
+      if (named_bar_or(kCmBarPro, 128, !ok)) {
+        failed = true;
+        break;
+      }
+      taken = j + 1;
+      struct {
+        bool live;
+        int n, m;
+        unsigned long long dst, bnd;
+      } it;
+      it.live = in.meta[0] != 0;
+      it.n = in.meta[1];
+      it.m = in.meta[2];
+      it.dst = in.dst;
+      it.bnd = in.bnd;
+      const float a = in.a, dt = in.dt[c];
+      float kr[kMaxQ], dr[kMaxQ];
+      if (it.live) {
+#pragma unroll
+        for (int t = 0; t < kMaxQ; ++t) {
+          kr[t] = 0.f;
+          dr[t] = 1.f;
+          if (t < it.n) {
+            kr[t] = bf16_bits_to_f32(in.kg[t][c]);
+            dr[t] = gate_decay(a, bf16_bits_to_f32(in.kg[t][kDim + c]), dt, p.lower_bound);
+          }
+        }
+        float sq[kMaxQ];
+#pragma unroll
+        for (int t = 0; t < kMaxQ; ++t) sq[t] = kr[t] * kr[t];
+        reduce_scatter<kMaxQ, 8>(sq, lane & 7);
+        sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 8);
+        sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 16);
+        if (lane < kMaxQ) sm.red[warp][lane] = sq[0];
+      }
+      // the ops buffer of item j - 2 must have been consumed
+      if (j >= 2) {
+        ok = mbar_wait_bounded(&sm.opempty[j & 1], (uint32_t)(((j >> 1) - 1) & 1));
+        if (named_bar_or(kCmBarPro, 128, !ok)) {
+          failed = true;
+          break;
+        }
+      }
+      if (c == 0) {
+        op.meta[0] = it.live ? 1 : 0;
+        op.meta[1] = it.n;
+        op.meta[2] = it.m;
+        op.dst = it.dst;
+        op.bnd = it.bnd;
+      }
+      if (it.live) {
+        float fd = 1.f;
+#pragma unroll
+        for (int t = kMaxQ - 1; t >= 0; --t) {
+          if (t < it.n) {
+            op.kp[t][c] = kr[t] * fd;
+            fd *= dr[t];
+          }
+        }
+        op.dn[c] = fd;
+        if constexpr (ALIGN) {
+          if (it.bnd != 0) {
+            float rm = 1.f;  // prod_{m <= s < n} d_s
+#pragma unroll
+            for (int t = kMaxQ - 1; t >= 0; --t)
+              if (t >= it.m && t < it.n) rm *= dr[t];
+            op.ir[c] = __fdividef(1.f, rm);
+          }
+        }
+        named_bar(kCmBarPro, 128);  // channel sums written
+#pragma unroll
+        for (int t = 0; t < kMaxQ; ++t) {
+          if (t < it.n) {
+            const float tot = (sm.red[0][t] + sm.red[2][t]) + (sm.red[1][t] + sm.red[3][t]);
+            op.u[t][c] = in.corr[t][c] * rsqrtf(tot + kNormEps);
+          }
+        }
+      }
+      named_bar(kCmBarPro, 128);  // in[j & 1] and the sums read, ops[j & 1] complete
+      if (c == 0) mbar_arrive(&sm.opfull[j & 1]);
+    }
+    if (failed && c == 0) report(p.status, KDA_ERR_TIMEOUT);
+    // after a timeout: record copies requested but never waited for land first
+    if (c == 0) {
+      for (int i = taken; i < requested; ++i)
+        mbar_wait_bounded(&sm.infull[i & 1], (uint32_t)((i >> 1) & 1));
+    }
+    return;
   }
 
-  const int g = tid >> 2, l4 = tid & 3;
-  const int c = tid & (kDim - 1);
+  // =======================================================================
+  // main warpgroups
+  // =======================================================================
+  const int mt = tid - 128;
+  const int c = lane & 7, R0 = 16 * (mt >> 5) + 4 * (lane >> 3);
+  int issued_hi = 0;  // lane 0: one past the last item whose page this warp requested
+  int consumed = 0;   // items whose page this warp has read (or skipped)
+  if (mt == 0) {
+    for (; issued_hi < NS && issued_hi < count; ++issued_hi) issue(issued_hi, page_of(issued_hi));
+  }
+  auto stage_read = [&](int j, unsigned long long next_src) {
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t prior = atom_add_acq_rel_smem(&sm.sreads[j % NS], 1u);
+      if ((prior & 7u) == 7u && j + NS < count) {
+        issue(j + NS, next_src);
+        issued_hi = j + NS + 1;
+      }
+    }
+  };
+  bool failed = false;
   for (int j = 0; j < count; ++j) {
-    const CommitItem it = commit_item<ST, ALIGN>(p, first + j * stride, tid == 0);
-    if (!it.live) {
-      if (tid == 0 && j + NS < count) issue(j + NS);
+    unsigned long long next_src = 0;
+    if (lane == 0 && j + NS < count) next_src = page_of(j + NS);
+    bool ok = mbar_wait_bounded(&sm.opfull[j & 1], (uint32_t)((j >> 1) & 1));
+    if (__any_sync(0xffffffffu, !ok)) {
+      failed = true;
+      break;
+    }
+    const CmOps &op = sm.ops[j & 1];
+    const bool live = op.meta[0] != 0;
+    const int n = op.meta[1], m = op.meta[2];
+    const unsigned long long dst = op.dst, bnd = op.bnd;
+    if (!live) {
+      stage_read(j, next_src);  // the stage's phase completed when the item was issued
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.opempty[j & 1]);
+      consumed = j + 1;
       continue;
     }
-    // ---- coefficients (threads 0-127) and corrections (128-255) ----
-    if (tid < kDim) {
-      const float a = __expf(p.A_log[it.l * p.H + it.h]);
-      const float dt = p.dt_bias[((long long)it.l * p.H + it.h) * kDim + c];
-      const uint16_t *kg = reinterpret_cast<const uint16_t *>(p.kg_ptrs[it.l]) +
-                           (long long)it.row * p.kg_strides[it.l] +
-                           (long long)it.h * p.Q * (2 * kDim) + c;
-      float kr[kMaxQ], dr[kMaxQ];
-#pragma unroll
-      for (int t = 0; t < kMaxQ; ++t) {
-        kr[t] = 0.f;
-        dr[t] = 1.f;
-        if (t < it.n) {
-          kr[t] = bf16_bits_to_f32(kg[t * 2 * kDim]);
-          dr[t] = gate_decay(a, bf16_bits_to_f32(kg[t * 2 * kDim + kDim]), dt, p.lower_bound);
-        }
-      }
-      float fd = 1.f;
-#pragma unroll
-      for (int t = kMaxQ - 1; t >= 0; --t) {
-        if (t < it.n) {
-          sm.kp[t][c] = kr[t] * fd;
-          fd *= dr[t];
-        }
-      }
-      sm.dn[c] = fd;
-      if constexpr (ALIGN) {
-        if (it.bslot >= 0) {
-          float fb = 1.f;
-#pragma unroll
-          for (int t = kMaxQ - 1; t >= 0; --t) {
-            if (t < it.m) {
-              sm.kpb[t][c] = kr[t] * fb;
-              fb *= dr[t];
-            }
-          }
-          sm.db[c] = fb;
-        }
-      }
-      float sq[kMaxQ];
-#pragma unroll
-      for (int t = 0; t < kMaxQ; ++t) sq[t] = kr[t] * kr[t];
-      reduce_scatter<kMaxQ, 8>(sq, lane & 7);
-      sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 8);
-      sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 16);
-      if (lane < kMaxQ) sm.red[warp][lane] = sq[0];
-    } else {
-      const float *corr = reinterpret_cast<const float *>(p.corr_ptrs[it.l]) +
-                          (long long)it.row * p.corr_strides[it.l] +
-                          (long long)it.h * p.Q * kDim + c;
-#pragma unroll
-      for (int t = 0; t < kMaxQ; ++t)
-        if (t < it.n) sm.uold[t][c] = corr[t * kDim];
+    ok = mbar_wait_bounded(&sm.full[j % NS], (uint32_t)((j / NS) & 1));
+    if (__any_sync(0xffffffffu, !ok)) {
+      failed = true;
+      break;
     }
-    const bool ok = mbar_wait_bounded(&sm.full[j % NS], (uint32_t)((j / NS) & 1));
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        report(p.status, KDA_ERR_TIMEOUT);
-        for (int jj = j; jj < j + NS && jj < count; ++jj)
-          mbar_wait_bounded(&sm.full[jj % NS], (uint32_t)((jj / NS) & 1));
-      }
-      __syncthreads();
-      return;
+    consumed = j + 1;
+    float4 st[4][4];
+    cm_load_tile<ST>(sm.stage[j % NS], R0, c, st);
+    stage_read(j, next_src);
+    switch (n) {
+      case 1: cm_fold<ST, 1, ALIGN>(st, op, dst, bnd, m, R0, c); break;
+      case 2: cm_fold<ST, 2, ALIGN>(st, op, dst, bnd, m, R0, c); break;
+      case 3: cm_fold<ST, 3, ALIGN>(st, op, dst, bnd, m, R0, c); break;
+      case 4: cm_fold<ST, 4, ALIGN>(st, op, dst, bnd, m, R0, c); break;
+      case 5: cm_fold<ST, 5, ALIGN>(st, op, dst, bnd, m, R0, c); break;
+      case 6: cm_fold<ST, 6, ALIGN>(st, op, dst, bnd, m, R0, c); break;
+      case 7: cm_fold<ST, 7, ALIGN>(st, op, dst, bnd, m, R0, c); break;
+      default: cm_fold<ST, 8, ALIGN>(st, op, dst, bnd, m, R0, c); break;
     }
-
-    // ---- fold 2 rows x 32 keys per thread ----
-    const int v0 = g, v1 = g + 64;
-    float u0[kMaxQ], u1[kMaxQ];
-#pragma unroll
-    for (int t = 0; t < kMaxQ; ++t) {
-      u0[t] = u1[t] = 0.f;
-      if (t < it.n) {
-        const float tot = (sm.red[0][t] + sm.red[2][t]) + (sm.red[1][t] + sm.red[3][t]);
-        const float rs = rsqrtf(tot + kNormEps);
-        u0[t] = sm.uold[t][v0] * rs;
-        u1[t] = sm.uold[t][v1] * rs;
-      }
-    }
-    const ST *page = sm.stage[j % NS];
-    ST *dst = commit_page<ST>(p, it.l, it.dst, it.h);
-    ST *bnd = (ALIGN && it.bslot >= 0) ? commit_page<ST>(p, it.l, it.bslot, it.h) : nullptr;
-#pragma unroll
-    for (int cc0 = 0; cc0 < 8; ++cc0) {
-      const int cc = cc0 ^ (g & kRotate);
-      const int key = 4 * (l4 + 4 * cc);
-      const float4 s0 = load_page4<ST>(page, v0, key);
-      const float4 s1 = load_page4<ST>(page, v1, key);
-      if constexpr (ALIGN) {
-        if (bnd != nullptr) {
-          const float4 d4 = lds4(&sm.db[key]);
-          float4 b0 = make_float4(s0.x * d4.x, s0.y * d4.y, s0.z * d4.z, s0.w * d4.w);
-          float4 b1 = make_float4(s1.x * d4.x, s1.y * d4.y, s1.z * d4.z, s1.w * d4.w);
-#pragma unroll
-          for (int t = 0; t < kMaxQ; ++t) {
-            if (t < it.m) {
-              const float4 k4 = lds4(&sm.kpb[t][key]);
-              b0.x = fmaf(u0[t], k4.x, b0.x); b0.y = fmaf(u0[t], k4.y, b0.y);
-              b0.z = fmaf(u0[t], k4.z, b0.z); b0.w = fmaf(u0[t], k4.w, b0.w);
-              b1.x = fmaf(u1[t], k4.x, b1.x); b1.y = fmaf(u1[t], k4.y, b1.y);
-              b1.z = fmaf(u1[t], k4.z, b1.z); b1.w = fmaf(u1[t], k4.w, b1.w);
-            }
-          }
-          store_page4<ST>(bnd, v0, key, b0);
-          store_page4<ST>(bnd, v1, key, b1);
-        }
-      }
-      const float4 d4 = lds4(&sm.dn[key]);
-      float4 r0 = make_float4(s0.x * d4.x, s0.y * d4.y, s0.z * d4.z, s0.w * d4.w);
-      float4 r1 = make_float4(s1.x * d4.x, s1.y * d4.y, s1.z * d4.z, s1.w * d4.w);
-#pragma unroll
-      for (int t = 0; t < kMaxQ; ++t) {
-        if (t < it.n) {
-          const float4 k4 = lds4(&sm.kp[t][key]);
-          r0.x = fmaf(u0[t], k4.x, r0.x); r0.y = fmaf(u0[t], k4.y, r0.y);
-          r0.z = fmaf(u0[t], k4.z, r0.z); r0.w = fmaf(u0[t], k4.w, r0.w);
-          r1.x = fmaf(u1[t], k4.x, r1.x); r1.y = fmaf(u1[t], k4.y, r1.y);
-          r1.z = fmaf(u1[t], k4.z, r1.z); r1.w = fmaf(u1[t], k4.w, r1.w);
-        }
-      }
-      store_page4<ST>(dst, v0, key, r0);
-      store_page4<ST>(dst, v1, key, r1);
-    }
-    __syncthreads();  // the stage and the coefficient arrays are free again
-    if (tid == 0 && j + NS < count) issue(j + NS);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.opempty[j & 1]);
+  }
+  if (failed && lane == 0) report(p.status, KDA_ERR_TIMEOUT);
+  if (lane == 0) {
+    for (int jj = consumed; jj < issued_hi; ++jj)
+      mbar_wait_bounded(&sm.full[jj % NS], (uint32_t)((jj / NS) & 1));
   }
 }
 
@@ -318,7 +505,7 @@ std::atomic<uint64_t> g_commit_configured[4];
 
 template <typename ST, bool ALIGN>
 int launch_commit_t(const CommitParams &p, int n_items, cudaStream_t stream, int slot) {
-  auto kern = kda_commit_persistent<ST, ALIGN>;
+  auto kern = kda_commit_ws<ST, ALIGN>;
   const size_t smem = sizeof(CommitSmem<ST>);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
