@@ -216,6 +216,18 @@ int kda_flush_plan(const int32_t *state_slots, const int32_t *record_rows,
                    int32_t *boundary_lens, int B, int Q, int null_slot,
                    int n_rows, int32_t *status, void *stream);
 
+/*
+ * kda_selftest_wait_timeout -- failure-detection self-test.  Launches one
+ * small kernel whose bounded wait on a barrier that nothing completes runs
+ * out after the library's fixed wait limit (about 2 s); the kernel then
+ * writes KDA_ERR_TIMEOUT to *status (device int32, set to 0 by the caller)
+ * and returns, leaving the context usable -- the same path every device
+ * wait of the step and commit kernels takes when a copy or a hand-off never
+ * arrives.  Returns KDA_ERR_ARG for a NULL status, KDA_ERR_CUDA if the
+ * launch fails.
+ */
+int kda_selftest_wait_timeout(int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

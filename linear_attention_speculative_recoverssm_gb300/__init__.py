@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     kda_defer_commit,
     kda_flush_plan,
     kda_replay_verify,
+    kda_selftest_wait_timeout,
     kda_verify,
     layer_tables,
     load,

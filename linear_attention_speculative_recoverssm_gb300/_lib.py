@@ -25,7 +25,7 @@ KDA_STATE_F32 = 0
 KDA_STATE_BF16 = 1
 
 EXPORTS = ("kda_abi_version", "kda_error_string", "kda_verify", "kda_replay_verify",
-           "kda_commit", "kda_defer_commit", "kda_flush_plan")
+           "kda_commit", "kda_defer_commit", "kda_flush_plan", "kda_selftest_wait_timeout")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -42,6 +42,7 @@ _SIGS = {
     "kda_commit": ([_P] * 14 + [_I, _F, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "kda_defer_commit": ([_P] * 5 + [_I, _I, _I, _P, _P], _I),
     "kda_flush_plan": ([_P] * 7 + [_I, _I, _I, _I, _P, _P], _I),
+    "kda_selftest_wait_timeout": ([_P, _P], _I),
 }
 
 _lib = None
@@ -197,3 +198,10 @@ def kda_flush_plan(state_slots, record_rows, pending, commit_lens, final_slots, 
         _ptr(final_slots), _ptr(boundary_slots), _ptr(boundary_lens), state_slots.shape[0], Q,
         null_slot, pending.shape[0], _ptr(status), _stream(stream))
     return _check("kda_flush_plan", rc, raise_on_error)
+
+
+def kda_selftest_wait_timeout(status, *, stream=None, raise_on_error=True):
+    """Failure-detection self-test: a device wait that runs out writes
+    KDA_ERR_TIMEOUT to ``status`` (device int32)."""
+    rc = load().kda_selftest_wait_timeout(_ptr(status), _stream(stream))
+    return _check("kda_selftest_wait_timeout", rc, raise_on_error)

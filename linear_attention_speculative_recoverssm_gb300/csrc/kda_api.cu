@@ -266,3 +266,8 @@ int kda_flush_plan(const int32_t *state_slots, const int32_t *record_rows, const
 }
 
 }  // extern "C"
+
+int kda_selftest_wait_timeout(int32_t *status, void *stream) {
+  if (!status) return KDA_ERR_ARG;
+  return kda::launch_selftest_timeout(status, static_cast<cudaStream_t>(stream));
+}

@@ -56,6 +56,21 @@ __global__ void kda_flush_plan_kernel(const int32_t *state_slots, const int32_t 
   boundary_lens[b] = 0;
 }
 
+// Failure-detection self-test: a bounded wait on a barrier whose phase
+// nothing completes.  The wait gives up after the library's fixed limit and
+// the kernel reports KDA_ERR_TIMEOUT, exactly as the step kernels do when a
+// copy or a hand-off never arrives; nothing faults and nothing hangs.
+__global__ void kda_selftest_timeout_kernel(int32_t *status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(&bar, 0u);
+  if (!ok && threadIdx.x == 0) report(status, KDA_ERR_TIMEOUT);
+}
+
 constexpr int kBookThreads = 128;
 
 }  // namespace
@@ -77,6 +92,11 @@ int launch_flush_plan(const int32_t *state_slots, const int32_t *record_rows,
   kda_flush_plan_kernel<<<grid, kBookThreads, 0, stream>>>(
       state_slots, record_rows, pending, commit_lens, final_slots, boundary_slots,
       boundary_lens, B, Q, null_slot, n_rows, status);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int launch_selftest_timeout(int32_t *status, cudaStream_t stream) {
+  kda_selftest_timeout_kernel<<<1, 32, 0, stream>>>(status);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -37,4 +37,6 @@ int launch_flush_plan(const int32_t *state_slots, const int32_t *record_rows,
                       int32_t *boundary_slots, int32_t *boundary_lens, int B, int Q,
                       int null_slot, int n_rows, int32_t *status, cudaStream_t stream);
 
+int launch_selftest_timeout(int32_t *status, cudaStream_t stream);
+
 }  // namespace kda

@@ -15,26 +15,6 @@
 
 namespace kda {
 
-template <int Q, typename ST, bool REPLAY, bool BOUNDARY>
-int launch_persistent(const StepParams &p, int n_items, cudaStream_t stream) {
-  auto kern = kda_step_persistent<Q, ST, REPLAY, BOUNDARY>;
-  constexpr size_t smem = sizeof(StepSmem<Q, ST, default_stages<ST>(), BOUNDARY>);
-  static std::atomic<uint64_t> configured{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load() & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return KDA_ERR_CUDA;
-    configured.fetch_or(bit);
-  }
-  const int sms = device_sm_count(dev);
-  const int grid = n_items < sms ? n_items : sms;
-  kern<<<grid, kThreads, smem, stream>>>(p, n_items);
-  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
-}
-
 // cuTensorMapEncodeTiled from the driver, looked up once.
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {

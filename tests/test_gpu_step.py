@@ -206,6 +206,25 @@ def test_out_of_range_indices_are_reported_not_faulted():
     assert not out[3].any()  # treated as inert
 
 
+def test_device_wait_that_runs_out_reports_timeout_and_context_survives():
+    """A bounded device wait on a barrier nothing completes gives up and
+    reports KDA_ERR_TIMEOUT; afterwards the same context still computes a
+    step that matches the oracle."""
+    import time
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import (KDA_ERR_TIMEOUT,
+                                                               kda_selftest_wait_timeout)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    kda_selftest_wait_timeout(status)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(status.item()) == KDA_ERR_TIMEOUT
+    assert 0.5 < waited < 30.0  # the wait limit, not an instant return or a hang
+    case = synth.replay_verify_case(B=4, H=2, Q=3, slots=8, seed=31)
+    _run_and_compare(case, split=1)
+
+
 def test_empty_batch_is_a_noop():
     import torch
     from linear_attention_speculative_recoverssm_gb300 import kda_replay_verify
