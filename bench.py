@@ -92,34 +92,45 @@ def algorithmic_bytes(case):
 # kernel sources are the ones it was measured on)
 # ---------------------------------------------------------------------------
 
-STEP_KERNEL_SOURCES = ("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
-                       "kda_step_q8.cu")
-PROFILED_TRAFFIC = dict(
-    sources_sha256="7a59e23a756a742c00ad3c76a16f9345257be157110abbe4815d1c47273c3c92",
-    workload=WORKLOAD,
-    bytes_per_launch=1073.3e6 * 31104 / 7808,
-    how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
-        "replay-verify-f32-h64-b128-q8 (1073.3 MB, 7808 live items), scaled by live items "
-        "to this workload's 31104",
-)
+PROFILED = {
+    # one kda_step_ws launch of the profiling workload, scaled by live items
+    "step": dict(
+        sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
+                 "kda_step_q8.cu"),
+        sha256="da82add0fcc02af20f4c4097cbe073724d4faa0a5615257669869d2ba69f66e4",
+        workload=WORKLOAD,
+        bytes_per_launch=1072.7e6 * 31104 / 7808,
+        how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
+            "replay-verify-f32-h64-b128-q8 (608.2 + 464.4 MB, 7808 live items), scaled by "
+            "live items to this workload's 31104"),
+    # one kda_commit_ws launch of the standalone-commit workload itself
+    "commit": dict(
+        sources=("kda_commit.cu", "kda_device.cuh"),
+        sha256="81457ecd777e6d7bb00e5a07c292afd3fee65d1767f44ef9e53fdae79e5c3f12",
+        workload="commit-bf16-l4-h32-b64-q4-align",
+        bytes_per_launch=(194.7 + 166.2) * 1e6,
+        how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_commit_ws launch of "
+            "this workload"),
+}
 
 
-def step_kernel_digest():
+def sources_digest(names):
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_speculative_recoverssm_gb300", "csrc")
-    for name in STEP_KERNEL_SOURCES:
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic(workload):
-    if workload != PROFILED_TRAFFIC["workload"]:
+def profiled_traffic(row, workload):
+    """ncu DRAM bytes per launch of a row's kernel, or None when the workload
+    differs or the kernel sources changed since they were measured."""
+    e = PROFILED[row]
+    if workload != e["workload"] or sources_digest(e["sources"]) != e["sha256"]:
         return None
-    if step_kernel_digest() != PROFILED_TRAFFIC["sources_sha256"]:
-        return None
-    return PROFILED_TRAFFIC["bytes_per_launch"]
+    return e["bytes_per_launch"]
 
 
 # ---------------------------------------------------------------------------
@@ -356,7 +367,8 @@ def measure_rows(dev, stream, peak, cpu_seconds):
     nbytes = commit_algorithmic_bytes(c)
     row = dict(workload=name, ms=ms, bytes_per_launch=nbytes,
                roofline=dict(bound="hbm", achieved=nbytes / ms / 1e6, peak=peak, unit="GB/s",
-                             frac=nbytes / ms / 1e6 / peak))
+                             frac=nbytes / ms / 1e6 / peak,
+                             traffic=profiled_traffic("commit", name)))
     if cpu_seconds > 0:
         from oracle import kda_oracle as ko
         L, B, H = c["L"], c["B"], c["H"]
@@ -598,7 +610,7 @@ def run_ours(args):
             roofline=dict(bound="hbm", achieved=achieved, peak=peak, unit="GB/s",
                           frac=achieved / peak,
                           traffic=args.traffic if args.traffic is not None
-                          else profiled_traffic(args.workload),
+                          else profiled_traffic("step", args.workload),
                           peak_source="MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks
                           else "fallback 6.8 TB/s",
                           bytes_per_launch=ab["total"], state_bytes_per_launch=ab["state"]),
