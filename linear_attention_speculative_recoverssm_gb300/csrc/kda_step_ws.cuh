@@ -64,6 +64,10 @@ constexpr int kWsRegsMain = 184;
 static_assert(128 * kWsRegsProlog + 256 * kWsRegsMain <= kWsThreads * kWsRegsLaunch,
               "register split exceeds the launch allocation");
 constexpr int kBarPro = 1;   // named barrier of the prologue warpgroup
+// Operand buffers between the prologue and the main warpgroups: the prologue
+// may run up to this many items ahead, which absorbs the per-item jitter of
+// either side.
+constexpr int kWsOpsBufs = 3;
 
 // Reduced over channels by the prologue per item: sum q_t^2 (Q values),
 // then the recorded keys' sums of squares (8 values).
@@ -81,14 +85,13 @@ struct alignas(16) WsOps {
   // x[t] = Gamma_t * k_t and x[Q + t] = Gamma_t * q_t (unnormalised), then
   // zero rows up to a multiple of 8 (written once, at kernel start)
   float x[ws_vectors<Q>()][kDim];
-  float ex[Q][kDim];  // k_s / Gamma_s (unnormalised): the pair-product rows
   float kp[kMaxQ][kDim];
   float dn[kDim];
   // boundary: 1 / prod_{m <= s < n} d_s, turning the first m replay terms
   // of S_n's sum into S_m
   float ir[BOUNDARY ? kDim : 4];
   float u[kMaxQ][kDim];  // recorded u_t[row] * rsqrt norm of its key
-  float vv[Q][kDim];
+  uint16_t vv[Q][kDim];  // v_t[row] (BF16 bits, as staged)
   float beta[kMaxQ];
   float rsq[Q];          // rsqrt(|q_t|^2 + eps) * q_scale
   float rsrec[kMaxQ];    // rsqrt(|recorded k_t|^2 + eps)
@@ -124,14 +127,15 @@ template <int Q, typename ST, bool BOUNDARY>
 struct WsSmem {
   static constexpr int NS = ws_stages<ST>();
   ST stage[NS][kDim * kDim];
-  WsOps<Q, BOUNDARY> ops[2];
+  WsOps<Q, BOUNDARY> ops[kWsOpsBufs];
   WsIn<Q> in[2];
+  float ex[Q][kDim];            // prologue: k_s / Gamma_s, the pair-product rows
   float dots_ex[Q][2 * Q + 1];  // prologue: the pair-product rows' dots
   float red[4][kWsRed];
   uint64_t full[NS];
   uint32_t sreads[NS];  // main-warp reads of each stage (8 per use)
-  uint64_t opfull[2];
-  uint64_t opempty[2];
+  uint64_t opfull[kWsOpsBufs];
+  uint64_t opempty[kWsOpsBufs];
   uint64_t infull[2];
   int next_meta[8];  // resolved index chain of the next item to request
 };
@@ -147,7 +151,8 @@ struct WsLayoutCheck {
   static_assert(offsetof(O, x) % 16 == 0 && offsetof(O, u) % 16 == 0 &&
                 offsetof(O, vv) % 16 == 0 &&
                 offsetof(O, kp) % 16 == 0 && offsetof(O, dn) % 16 == 0 &&
-                offsetof(O, ex) % 16 == 0 && offsetof(O, ir) % 16 == 0,
+                offsetof(O, vv) % 8 == 0 && offsetof(O, ir) % 16 == 0 &&
+                offsetof(S, ex) % 16 == 0,
                 "float4-read ops members");
   static_assert(sizeof(WsIn<Q>) % 128 == 0 && offsetof(S, in) % 128 == 0 &&
                 offsetof(WsIn<Q>, tok) % 16 == 0 && offsetof(WsIn<Q>, kg) % 16 == 0 &&
@@ -367,7 +372,9 @@ __device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
                                          const StepParams &p, long long tok0, int h, int rec,
                                          int R0, int c, int lane) {
   const int cw = c < Q ? c : Q - 1;  // lanes without a w role compute unused values
-  const float4 v4 = lds4(&op.vv[cw][R0]);
+  const uint2 vb = *reinterpret_cast<const uint2 *>(&op.vv[cw][R0]);
+  const float4 v4 = make_float4(__uint_as_float(vb.x << 16), __uint_as_float(vb.x & 0xffff0000u),
+                                __uint_as_float(vb.y << 16), __uint_as_float(vb.y & 0xffff0000u));
   const float rk = op.rsk[cw], bt = op.beta[cw];
   float res[4] = {fmaf(-d[0][0], rk, v4.x), fmaf(-d[0][1], rk, v4.y), fmaf(-d[0][2], rk, v4.z),
                   fmaf(-d[0][3], rk, v4.w)};
@@ -455,10 +462,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       mbar_init(&sm.full[s], 1);
       sm.sreads[s] = 0;
     }
-    mbar_init(&sm.opfull[0], 1);
-    mbar_init(&sm.opfull[1], 1);
-    mbar_init(&sm.opempty[0], 8);  // one arrival per main warp
-    mbar_init(&sm.opempty[1], 8);
+    for (int b = 0; b < kWsOpsBufs; ++b) {
+      mbar_init(&sm.opfull[b], 1);
+      mbar_init(&sm.opempty[b], 8);  // one arrival per main warp
+    }
     mbar_init(&sm.infull[0], 1);  // thread 0's arrival with the copies' byte count
     mbar_init(&sm.infull[1], 1);
     mbar_init_fence();
@@ -466,7 +473,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   // the padding dot vectors (rows 2Q .. of x) stay zero in both ops buffers
   constexpr int kPadFloats = (ws_vectors<Q>() - 2 * Q) * kDim;
   if constexpr (kPadFloats > 0) {
-    for (int e = tid; e < 2 * kPadFloats; e += kWsThreads)
+    for (int e = tid; e < kWsOpsBufs * kPadFloats; e += kWsThreads)
       sm.ops[e / kPadFloats].x[2 * Q + (e % kPadFloats) / kDim][e % kDim] = 0.f;
   }
   __syncthreads();
@@ -612,7 +619,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     }
 
     for (int j = 0; j < count; ++j) {
-      Ops &op = sm.ops[j & 1];
+      Ops &op = sm.ops[j % kWsOpsBufs];
       const WsIn<Q> &in = sm.in[j & 1];
       const float dt = dt_n, a_log_h = alog_n;
       const uint32_t braw_bits = beta_n;
@@ -683,9 +690,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (j + 3 < count) load_raw(j + 3);
       }
 
-      // ---- the ops buffer of item j - 2 must have been consumed ----
-      if (j >= 2) {
-        ok = mbar_wait_bounded(&sm.opempty[j & 1], (uint32_t)(((j >> 1) - 1) & 1));
+      // ---- the ops buffer of item j - kWsOpsBufs must have been consumed ----
+      if (j >= kWsOpsBufs) {
+        ok = mbar_wait_bounded(&sm.opempty[j % kWsOpsBufs],
+                               (uint32_t)((j / kWsOpsBufs - 1) & 1));
         if (named_bar_or(kBarPro, 128, !ok)) {
           if (c == 0) report(p.status, KDA_ERR_TIMEOUT);
           break;
@@ -705,8 +713,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         for (int t = 0; t < Q; ++t) {
           op.x[t][c] = gam[t] * kk[t];
           op.x[Q + t][c] = gam[t] * qq[t];
-          op.ex[t][c] = kk[t] * inv[t];
-          op.vv[t][c] = bf16_bits_to_f32(in.tok[3][t][c]);
+          sm.ex[t][c] = kk[t] * inv[t];
+          op.vv[t][c] = in.tok[3][t][c];
         }
         if (c < Q) op.beta[c] = sigmoidf_fast(bf16_bits_to_f32(braw_bits));
         if (REPLAY && it.n > 0) {
@@ -767,8 +775,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                   [&](int rr, float4 &sa, float4 &sb) {
                     const int srow = base + rr;
                     if (srow < Q) {
-                      sa = lds4(&op.ex[srow][pka]);
-                      sb = lds4(&op.ex[srow][pkb]);
+                      sa = lds4(&sm.ex[srow][pka]);
+                      sb = lds4(&sm.ex[srow][pkb]);
                     } else {
                       sa = sb = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
@@ -805,7 +813,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
       }
       named_bar(kBarPro, 128);  // in[j & 1] read, ops[j & 1] complete
-      if (c == 0) mbar_arrive(&sm.opfull[j & 1]);
+      if (c == 0) mbar_arrive(&sm.opfull[j % kWsOpsBufs]);
     }
     // After a timeout: input copies requested but never waited for must
     // land (bounded) before this CTA's shared memory goes.
@@ -851,12 +859,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     int next_slot = -1;
     if (lane == 0 && j + NS < count) next_slot = item_slot(j + NS);
 
-    bool ok = mbar_wait_bounded(&sm.opfull[j & 1], (uint32_t)((j >> 1) & 1));
+    bool ok = mbar_wait_bounded(&sm.opfull[j % kWsOpsBufs], (uint32_t)((j / kWsOpsBufs) & 1));
     if (__any_sync(0xffffffffu, !ok)) {
       failed = true;
       break;
     }
-    const Ops &op = sm.ops[j & 1];
+    const Ops &op = sm.ops[j % kWsOpsBufs];
     const int b = op.meta[0], h = op.meta[1], slot = op.meta[2], rec = op.meta[3];
     const int n = op.meta[4], bslot = op.meta[5], m = op.meta[6];
     const long long tok0 = (long long)b * Q;
@@ -867,7 +875,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (c < Q)
         *reinterpret_cast<uint2 *>(p.out + ((tok0 + c) * p.H + h) * kDim + R0) = make_uint2(0, 0);
       stage_read(j, next_slot);
-      warp_arrive(&sm.opempty[j & 1]);
+      warp_arrive(&sm.opempty[j % kWsOpsBufs]);
       consumed = j + 1;
       continue;
     }
@@ -911,7 +919,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     // ---------------- row solve, outputs, corrections --------------------
     ws_solve<Q, NG>(d, op, p, tok0, h, rec, R0, c, lane);
-    warp_arrive(&sm.opempty[j & 1]);
+    warp_arrive(&sm.opempty[j % kWsOpsBufs]);
   }
   if (failed && lane == 0) report(p.status, KDA_ERR_TIMEOUT);
   // After a timeout, pages this warp requested but never read may still be in
