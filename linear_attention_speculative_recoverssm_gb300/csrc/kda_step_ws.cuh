@@ -487,8 +487,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // The index chain slot / record row -> pending count -> records runs two
     // items ahead in thread 0; warp 0 requests item j + 1's inputs while
     // item j is built, so the warpgroup itself never waits on HBM latency.
-    int rs_slot = -1, rs_rec = -1, rs_bslot = -1, rs_blen = 0, rs_pend = 0;  // item j + 2
-    auto publish_next = [&](const ItemMeta &m) {  // item j + 1, read by warp 0
+    // Raw per-request values of an item (no branch on them, so the loads stay
+    // in flight) and its pending count, loaded a step later from its row.
+    struct Raw {
+      int slot = -1, rec = -1, bslot = -1, blen = 0, pend = 0;
+    };
+    Raw r2, r3;  // items j + 2 (row and pending loaded) and j + 3 (row loaded)
+    auto publish_next = [&](const ItemMeta &m) {  // item j + 1, read by thread 0
       sm.next_meta[0] = m.b;
       sm.next_meta[1] = m.h;
       sm.next_meta[2] = m.slot;
@@ -497,24 +502,26 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       sm.next_meta[5] = m.bslot;
       sm.next_meta[6] = m.m;
     };
-    auto load_raw = [&](int i) {
+    auto load_raw = [&](int i, Raw &r) {
       const int b = (first + i * stride) / p.H;
-      rs_slot = p.state_slots[b];
-      rs_rec = p.record_rows != nullptr ? p.record_rows[b] : b;
-      rs_bslot = -1;
-      rs_blen = 0;
+      r.slot = p.state_slots[b];
+      r.rec = p.record_rows != nullptr ? p.record_rows[b] : b;
+      r.bslot = -1;
+      r.blen = 0;
       if (BOUNDARY && p.bnd_slots != nullptr) {
-        rs_bslot = p.bnd_slots[b];
-        rs_blen = p.bnd_lens[b];
+        r.bslot = p.bnd_slots[b];
+        r.blen = p.bnd_lens[b];
       }
+      r.pend = 0;
     };
-    auto load_pending = [&]() {
-      rs_pend = 0;
-      if (REPLAY && rs_rec >= 0 && rs_rec < p.n_rows && rs_slot > p.null_slot &&
-          rs_slot < p.n_slots)
-        rs_pend = p.pending[rs_rec];
+    auto load_pending = [&](Raw &r) {
+      r.pend = 0;
+      if (REPLAY && r.rec >= 0 && r.rec < p.n_rows && r.slot > p.null_slot && r.slot < p.n_slots)
+        r.pend = p.pending[r.rec];
     };
-    auto resolve = [&](int i) {  // item_meta from the loaded raw values
+    auto resolve = [&](int i, const Raw &r) {  // item_meta from the loaded raw values
+      const int rs_slot = r.slot, rs_rec = r.rec, rs_bslot = r.bslot, rs_blen = r.blen,
+                rs_pend = r.pend;
       ItemMeta it;
       it.b = (first + i * stride) / p.H;
       it.h = (first + i * stride) - it.b * p.H;
@@ -601,18 +608,24 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     if (count > 0) {
       requested = 1;
       if (c == 0) {
-        load_raw(0);
-        load_pending();
-        publish_next(resolve(0));
+        Raw r0;
+        load_raw(0, r0);
+        load_pending(r0);
+        publish_next(resolve(0, r0));
       }
       named_bar(kBarPro, 128);  // next_meta published
       request_inputs(0);
       named_bar(kBarPro, 128);  // next_meta read by every thread
       if (c == 0 && count > 1) {
-        load_raw(1);
-        load_pending();
-        publish_next(resolve(1));
-        if (count > 2) load_raw(2);
+        Raw r1;
+        load_raw(1, r1);
+        load_pending(r1);
+        publish_next(resolve(1, r1));
+        if (count > 2) {
+          load_raw(2, r2);
+          load_pending(r2);
+        }
+        if (count > 3) load_raw(3, r3);
       }
       named_bar(kBarPro, 128);  // next_meta published
       load_small(0);
@@ -628,7 +641,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         requested = j + 2;
         load_small(j + 1);
       }
-      if (c == 0 && j + 2 < count) load_pending();  // item j + 2 (its row is loaded)
 
       bool ok = mbar_wait_bounded(&sm.infull[j & 1], (uint32_t)((j >> 1) & 1));
       if (named_bar_or(kBarPro, 128, !ok)) {
@@ -685,9 +697,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
       }
       // thread 0: the index chain of item j + 2, then the row of item j + 3
+      // (each value was loaded at least one item earlier)
       if (c == 0 && j + 2 < count) {
-        publish_next(resolve(j + 2));
-        if (j + 3 < count) load_raw(j + 3);
+        publish_next(resolve(j + 2, r2));
+        r2 = r3;
+        if (j + 3 < count) load_pending(r2);
+        if (j + 4 < count) load_raw(j + 4, r3);
       }
 
       // ---- the ops buffer of item j - kWsOpsBufs must have been consumed ----
