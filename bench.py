@@ -97,11 +97,11 @@ PROFILED = {
     "step": dict(
         sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
                  "kda_step_q8.cu"),
-        sha256="da82add0fcc02af20f4c4097cbe073724d4faa0a5615257669869d2ba69f66e4",
+        sha256="5c7f75d60d75ae5029525cc65b03173ab79be72d8f8ad07cbc54ba2bfdc937a0",
         workload=WORKLOAD,
-        bytes_per_launch=1072.7e6 * 31104 / 7808,
+        bytes_per_launch=(608.2 + 464.5) * 1e6 * 31104 / 7808,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
-            "replay-verify-f32-h64-b128-q8 (608.2 + 464.4 MB, 7808 live items), scaled by "
+            "replay-verify-f32-h64-b128-q8 (608.2 + 464.5 MB, 7808 live items), scaled by "
             "live items to this workload's 31104"),
     # one kda_commit_ws launch of the standalone-commit workload itself
     "commit": dict(
