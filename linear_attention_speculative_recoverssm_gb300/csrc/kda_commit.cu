@@ -6,8 +6,9 @@
 //
 // Design (one CTA per SM, 384 threads, items (layer, request, head) strided
 // over the grid):
-//  * prologue warpgroup (warps 0-3, thread c <-> key channel c): thread 0
-//    resolves the item chain two items ahead and stages each live item's
+//  * two prologue warpgroups (warps 0-3 and 4-7, alternate items; thread c
+//    <-> key channel c): thread 0 of each resolves its item chain two items
+//    ahead and stages each live item's
 //    recorded key / gate rows and corrections with two bulk copies, one item
 //    ahead; every thread then builds channel c's replay coefficients
 //    (recorded key times the suffix decay product, D_n, the boundary's
@@ -15,7 +16,7 @@
 //    norm into one of two shared "ops" buffers.  The product form of the
 //    decays is used instead of the log form (the same quantity; it saves one
 //    exp per coefficient).
-//  * main warpgroups (warps 4-11): each live item's source page (32 KB BF16
+//  * main warpgroups (warps 8-15): each live item's source page (32 KB BF16
 //    or 64 KB FP32) arrives by one bulk copy in a ring of NS stages; thread
 //    (main warp w, lane 8 rs + c) reads rows 16 w + 4 rs .. + 3, keys
 //    32 i + 4 c .. + 3 into registers, and the last warp to read a stage
@@ -35,8 +36,13 @@
 namespace kda {
 namespace {
 
-constexpr int kCommitThreads = 384;
-constexpr int kCmBarPro = 1;  // named barrier of the prologue warpgroup
+// Two prologue warpgroups take alternate items (the per-item prologue is a
+// latency chain; two of them keep up with the main warpgroups), then two main
+// warpgroups.
+constexpr int kCmProWGs = 2;
+constexpr int kCommitThreads = 128 * (kCmProWGs + 2);
+constexpr int kCmOps = 2 * kCmProWGs;  // operand buffers: two per prologue warpgroup
+constexpr int kCmBarPro = 1;           // + warpgroup: named barrier of a prologue warpgroup
 
 struct CommitParams {
   const uint64_t *state_ptrs, *corr_ptrs, *kg_ptrs;
@@ -56,6 +62,9 @@ struct alignas(16) CmOps {
   float ir[kDim];         // 1 / prod_{m<=s<n} d_s (boundary)
   float u[kMaxQ][kDim];   // recorded u_t[row] * rsqrt(|k_t|^2 + eps)
   unsigned long long dst, bnd;  // destination / boundary page (0: none)
+  // the source page of the item NS later (0: none or dead), which the last
+  // reader of this item's stage requests into it
+  unsigned long long next_src;
   int meta[4];                  // live, n, m
 };
 
@@ -74,13 +83,13 @@ template <typename ST>
 struct CommitSmem {
   static constexpr int NS = sizeof(ST) == 2 ? 4 : 2;
   ST stage[NS][kDim * kDim];
-  CmOps ops[2];
-  CmIn in[2];
-  float red[4][kMaxQ];
+  CmOps ops[kCmOps];
+  CmIn in[kCmProWGs][2];
+  float red[kCmProWGs][4][kMaxQ];
   uint64_t full[NS];
-  uint64_t opfull[2];
-  uint64_t opempty[2];
-  uint64_t infull[2];
+  uint64_t opfull[kCmOps];
+  uint64_t opempty[kCmOps];
+  uint64_t infull[kCmProWGs][2];
   uint32_t sreads[NS];
 };
 
@@ -286,27 +295,34 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
       mbar_init(&sm.full[s], 1);
       sm.sreads[s] = 0;
     }
-    mbar_init(&sm.opfull[0], 1);
-    mbar_init(&sm.opfull[1], 1);
-    mbar_init(&sm.opempty[0], 8);  // one arrival per main warp
-    mbar_init(&sm.opempty[1], 8);
-    mbar_init(&sm.infull[0], 1);
-    mbar_init(&sm.infull[1], 1);
+    for (int b = 0; b < kCmOps; ++b) {
+      mbar_init(&sm.opfull[b], 1);
+      mbar_init(&sm.opempty[b], 8);  // one arrival per main warp
+    }
+    for (int w = 0; w < kCmProWGs; ++w) {
+      mbar_init(&sm.infull[w][0], 1);
+      mbar_init(&sm.infull[w][1], 1);
+    }
     mbar_init_fence();
   }
   __syncthreads();
 
-  if (warp < 4) {
+  if (warp < 4 * kCmProWGs) {
     // =====================================================================
-    // prologue warpgroup: thread c owns key channel c
+    // prologue warpgroup pw: items j = pw, pw + 2, ...; thread c owns key
+    // channel c.  Its k-th item is j = pw + 2 k.
     // =====================================================================
-    const int c = tid;
-    // thread 0's item chain: raw values of item j + 2, resolved item j + 1
+    const int pw = warp >> 2, wl = warp & 3;
+    const int c = tid - 128 * pw;
+    const int bar_id = kCmBarPro + pw;
+    const int nk = count > pw ? (count - pw + kCmProWGs - 1) / kCmProWGs : 0;
+    auto jof = [&](int k) { return pw + kCmProWGs * k; };
+    // thread 0's item chain: raw values of item k + 2, resolved item k + 1
     CommitRaw raw2{};
     CommitItem nxt{};
-    auto request = [&](int i, const CommitItem &it) {  // thread 0
-      uint64_t *bar = &sm.infull[i & 1];
-      CmIn &in = sm.in[i & 1];
+    auto request = [&](int k, const CommitItem &it) {  // thread 0
+      uint64_t *bar = &sm.infull[pw][k & 1];
+      CmIn &in = sm.in[pw][k & 1];
       in.meta[0] = it.live ? 1 : 0;
       in.meta[1] = it.n;
       in.meta[2] = it.m;
@@ -323,30 +339,43 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
       bulk_g2s(&in.corr[0][0], reinterpret_cast<const void *>(it.corr), bytes, bar);
       bulk_g2s(&in.dt[0], p.dt_bias + ((long long)it.l * p.H + it.h) * kDim, kDim * 4u, bar);
     };
+    auto resolve = [&](int k, const CommitRaw &r) {
+      return commit_resolve<ST>(p, item_of(jof(k)), r, true);
+    };
     int requested = 0, taken = 0;
-    if (c == 0 && count > 0) {
-      const CommitItem it0 = commit_resolve<ST>(p, item_of(0), commit_raw(p, ALIGN, item_of(0)), true);
-      request(0, it0);
+    if (c == 0 && nk > 0) {
+      request(0, resolve(0, commit_raw(p, ALIGN, item_of(jof(0)))));
       requested = 1;
-      if (count > 1) nxt = commit_resolve<ST>(p, item_of(1), commit_raw(p, ALIGN, item_of(1)), true);
-      if (count > 2) raw2 = commit_raw(p, ALIGN, item_of(2));
+      if (nk > 1) nxt = resolve(1, commit_raw(p, ALIGN, item_of(jof(1))));
+      if (nk > 2) raw2 = commit_raw(p, ALIGN, item_of(jof(2)));
     }
     bool failed = false;
-    for (int j = 0; j < count; ++j) {
-      CmOps &op = sm.ops[j & 1];
-      const CmIn &in = sm.in[j & 1];
-      if (c == 0 && j + 1 < count) {
-        request(j + 1, nxt);
-        requested = j + 2;
-        if (j + 2 < count) nxt = commit_resolve<ST>(p, item_of(j + 2), raw2, true);
-        if (j + 3 < count) raw2 = commit_raw(p, ALIGN, item_of(j + 3));
+    for (int k = 0; k < nk; ++k) {
+      const int j = jof(k);
+      CmOps &op = sm.ops[j % kCmOps];
+      const CmIn &in = sm.in[pw][k & 1];
+      // thread 0: the source page of item j + NS (items j + 2 and j + 4 are
+      // this warpgroup's next two), handed to the main warps with this item
+      unsigned long long next_src = 0;
+      if (c == 0 && k + 1 < nk) {
+        const CommitItem it1 = nxt;  // item j + 2
+        request(k + 1, it1);
+        requested = k + 2;
+        if (k + 2 < nk) nxt = resolve(k + 2, raw2);  // item j + 4
+        if (k + 3 < nk) raw2 = commit_raw(p, ALIGN, item_of(jof(k + 3)));
+        static_assert(NS == 2 || NS == 4, "page ring of 2 or 4 stages");
+        if constexpr (NS == 2) {
+          next_src = it1.live ? it1.src : 0ull;
+        } else {
+          next_src = (k + 2 < nk && nxt.live) ? nxt.src : 0ull;
+        }
       }
-      bool ok = mbar_wait_bounded(&sm.infull[j & 1], (uint32_t)((j >> 1) & 1));
-      if (named_bar_or(kCmBarPro, 128, !ok)) {
+      bool ok = mbar_wait_bounded(&sm.infull[pw][k & 1], (uint32_t)((k >> 1) & 1));
+      if (named_bar_or(bar_id, 128, !ok)) {
         failed = true;
         break;
       }
-      taken = j + 1;
+      taken = k + 1;
       struct {
         bool live;
         int n, m;
@@ -375,12 +404,12 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
         reduce_scatter<kMaxQ, 8>(sq, lane & 7);
         sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 8);
         sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 16);
-        if (lane < kMaxQ) sm.red[warp][lane] = sq[0];
+        if (lane < kMaxQ) sm.red[pw][wl][lane] = sq[0];
       }
-      // the ops buffer of item j - 2 must have been consumed
-      if (j >= 2) {
-        ok = mbar_wait_bounded(&sm.opempty[j & 1], (uint32_t)(((j >> 1) - 1) & 1));
-        if (named_bar_or(kCmBarPro, 128, !ok)) {
+      // the ops buffer of item j - kCmOps must have been consumed
+      if (j >= kCmOps) {
+        ok = mbar_wait_bounded(&sm.opempty[j % kCmOps], (uint32_t)((j / kCmOps - 1) & 1));
+        if (named_bar_or(bar_id, 128, !ok)) {
           failed = true;
           break;
         }
@@ -391,6 +420,7 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
         op.meta[2] = it.m;
         op.dst = it.dst;
         op.bnd = it.bnd;
+        op.next_src = next_src;
       }
       if (it.live) {
         float fd = 1.f;
@@ -411,23 +441,24 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
             op.ir[c] = __fdividef(1.f, rm);
           }
         }
-        named_bar(kCmBarPro, 128);  // channel sums written
+        named_bar(bar_id, 128);  // channel sums written
 #pragma unroll
         for (int t = 0; t < kMaxQ; ++t) {
           if (t < it.n) {
-            const float tot = (sm.red[0][t] + sm.red[2][t]) + (sm.red[1][t] + sm.red[3][t]);
+            const float tot = (sm.red[pw][0][t] + sm.red[pw][2][t]) +
+                              (sm.red[pw][1][t] + sm.red[pw][3][t]);
             op.u[t][c] = in.corr[t][c] * rsqrtf(tot + kNormEps);
           }
         }
       }
-      named_bar(kCmBarPro, 128);  // in[j & 1] and the sums read, ops[j & 1] complete
-      if (c == 0) mbar_arrive(&sm.opfull[j & 1]);
+      named_bar(bar_id, 128);  // in and the sums read, the ops buffer complete
+      if (c == 0) mbar_arrive(&sm.opfull[j % kCmOps]);
     }
     if (failed && c == 0) report(p.status, KDA_ERR_TIMEOUT);
     // after a timeout: record copies requested but never waited for land first
     if (c == 0) {
       for (int i = taken; i < requested; ++i)
-        mbar_wait_bounded(&sm.infull[i & 1], (uint32_t)((i >> 1) & 1));
+        mbar_wait_bounded(&sm.infull[pw][i & 1], (uint32_t)((i >> 1) & 1));
     }
     return;
   }
@@ -435,7 +466,7 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
   // =======================================================================
   // main warpgroups
   // =======================================================================
-  const int mt = tid - 128;
+  const int mt = tid - 128 * kCmProWGs;
   const int c = lane & 7, R0 = 16 * (mt >> 5) + 4 * (lane >> 3);
   int issued_hi = 0;  // lane 0: one past the last item whose page this warp requested
   int consumed = 0;   // items whose page this warp has read (or skipped)
@@ -454,21 +485,20 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
   };
   bool failed = false;
   for (int j = 0; j < count; ++j) {
-    unsigned long long next_src = 0;
-    if (lane == 0 && j + NS < count) next_src = page_of(j + NS);
-    bool ok = mbar_wait_bounded(&sm.opfull[j & 1], (uint32_t)((j >> 1) & 1));
+    bool ok = mbar_wait_bounded(&sm.opfull[j % kCmOps], (uint32_t)((j / kCmOps) & 1));
     if (__any_sync(0xffffffffu, !ok)) {
       failed = true;
       break;
     }
-    const CmOps &op = sm.ops[j & 1];
+    const CmOps &op = sm.ops[j % kCmOps];
+    const unsigned long long next_src = op.next_src;
     const bool live = op.meta[0] != 0;
     const int n = op.meta[1], m = op.meta[2];
     const unsigned long long dst = op.dst, bnd = op.bnd;
     if (!live) {
       stage_read(j, next_src);  // the stage's phase completed when the item was issued
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.opempty[j & 1]);
+      if (lane == 0) mbar_arrive(&sm.opempty[j % kCmOps]);
       consumed = j + 1;
       continue;
     }
@@ -492,7 +522,7 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
       default: cm_fold<ST, 8, ALIGN>(st, op, dst, bnd, m, R0, c); break;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.opempty[j & 1]);
+    if (lane == 0) mbar_arrive(&sm.opempty[j % kCmOps]);
   }
   if (failed && lane == 0) report(p.status, KDA_ERR_TIMEOUT);
   if (lane == 0) {

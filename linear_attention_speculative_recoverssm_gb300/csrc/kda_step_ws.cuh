@@ -868,11 +868,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
   };
+  // lane 0: the raw slot of item j + NS + 1, loaded an item before its use
+  // (the page that may follow item j into its stage is item j + NS's)
+  auto raw_slot = [&](int i) { return p.state_slots[(first + i * stride) / p.H]; };
+  auto valid_slot = [&](int s) { return (s > p.null_slot && s < p.n_slots) ? s : -1; };
+  int raw_ahead = -1;
+  if (lane == 0 && NS < count) raw_ahead = raw_slot(NS);
   bool failed = false;
   for (int j = 0; j < count; ++j) {
-    // the slot of the item whose page may follow this one into its stage
     int next_slot = -1;
-    if (lane == 0 && j + NS < count) next_slot = item_slot(j + NS);
+    if (lane == 0 && j + NS < count) {
+      next_slot = valid_slot(raw_ahead);
+      if (j + NS + 1 < count) raw_ahead = raw_slot(j + NS + 1);
+    }
 
     bool ok = mbar_wait_bounded(&sm.opfull[j % kWsOpsBufs], (uint32_t)((j / kWsOpsBufs) & 1));
     if (__any_sync(0xffffffffu, !ok)) {
