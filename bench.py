@@ -97,18 +97,18 @@ PROFILED = {
     "step": dict(
         sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
                  "kda_step_q8.cu"),
-        sha256="5c7f75d60d75ae5029525cc65b03173ab79be72d8f8ad07cbc54ba2bfdc937a0",
+        sha256="cd3fdf1792a091ed3caa9b60ed40e06f33cc42d20a185ba7db096d56313f548c",
         workload=WORKLOAD,
-        bytes_per_launch=(608.2 + 464.5) * 1e6 * 31104 / 7808,
+        bytes_per_launch=(608.2 + 464.3) * 1e6 * 31104 / 7808,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
-            "replay-verify-f32-h64-b128-q8 (608.2 + 464.5 MB, 7808 live items), scaled by "
+            "replay-verify-f32-h64-b128-q8 (608.2 + 464.3 MB, 7808 live items), scaled by "
             "live items to this workload's 31104"),
     # one kda_commit_ws launch of the standalone-commit workload itself
     "commit": dict(
         sources=("kda_commit.cu", "kda_device.cuh"),
-        sha256="81457ecd777e6d7bb00e5a07c292afd3fee65d1767f44ef9e53fdae79e5c3f12",
+        sha256="8040a2430119aa7890c25ff2f24dcb67a01bb6657a4bb6d1d1c84f98cd4fa7d9",
         workload="commit-bf16-l4-h32-b64-q4-align",
-        bytes_per_launch=(194.7 + 166.2) * 1e6,
+        bytes_per_launch=(194.7 + 167.2) * 1e6,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_commit_ws launch of "
             "this workload"),
 }
