@@ -319,6 +319,25 @@ def commit_algorithmic_bytes(c):
     return total
 
 
+def verify_algorithmic_bytes(case):
+    """Bytes one verify-only launch (the checkpoint is read, never written)
+    must move: per live item the state page, this window's inputs and
+    outputs, and with a record row the new records; per inert item its
+    zero outputs."""
+    B, H, Q = case["B"], case["H"], case["Q"]
+    page = DIM * DIM * case["state"].dtype.itemsize
+    total = 0
+    for b in range(B):
+        if case["state_slots"][b] <= case["null_slot"]:
+            total += H * Q * DIM * 2
+            continue
+        per = page + 4 * Q * DIM * 2 + Q * 2 + Q * DIM * 2
+        if case["record_rows"][b] >= 0:
+            per += Q * (DIM * 4 + 2 * DIM * 2)
+        total += H * per
+    return total
+
+
 def _event_ms(stream, fn, iters):
     import torch
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -416,6 +435,23 @@ def measure_rows(dev, stream, peak, cpu_seconds):
         row["cpu_baseline"] = dict(value=rate, unit="tok/s", cores=1, kind="oracle",
                                    sample=f"{items} live items, {secs:.1f} s on one core")
     rows["replay_verify_mid_batch"] = row
+
+    # the stock verify (checkpoint read-only) on the same batch
+    from linear_attention_speculative_recoverssm_gb300 import kda_verify
+
+    def verify():
+        kda_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"], d["dt_bias"],
+                   d["state"], d["state_slots"], d["corr"], d["key_gate"], out, Q=c["Q"],
+                   lower_bound=c["lower_bound"], q_scale=c["q_scale"],
+                   record_rows=d["record_rows"], stream=stream)
+    for _ in range(5):
+        verify()
+    ms = _event_ms(stream, verify, 50)
+    nbytes = verify_algorithmic_bytes(c)
+    rows["verify_mid_batch"] = dict(
+        workload=name, ms=ms, tok_s=ab["live_tokens"] / (ms / 1e3), bytes_per_launch=nbytes,
+        roofline=dict(bound="hbm", achieved=nbytes / ms / 1e6, peak=peak, unit="GB/s",
+                      frac=nbytes / ms / 1e6 / peak))
     del d, out
 
     # small batches: per-launch device time (a CUDA graph of 20 launches)

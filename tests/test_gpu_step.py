@@ -285,3 +285,43 @@ def test_full_size_sampled(name):
                                               case["key_gate"][r, h, :Q])
         else:
             assert not got_out[b, :, h].any()
+
+
+# --------------------------------------------------------------------------
+# degenerate and extreme cases
+# --------------------------------------------------------------------------
+
+def test_every_request_inert():
+    """A batch whose every slot is the null slot: zero outputs, nothing else
+    written (pool, records and pending bit-identical)."""
+    case = synth.replay_verify_case(B=12, H=3, Q=4, slots=16, seed=41)
+    case["state_slots"][:] = case["null_slot"]
+    d, _ = _run_and_compare(case, split=1)
+    assert not tu.to_numpy(d["out"]).any()
+
+
+@pytest.mark.parametrize("fill", ["zero", "max"])
+def test_pending_all_zero_or_all_full(fill):
+    """Every request with nothing to replay (the checkpoint must stay
+    bit-identical) or with the full record capacity pending."""
+    case = synth.replay_verify_case(B=24, H=4, Q=8, slots=32, seed=43 if fill == "zero" else 44)
+    case["pending"][:] = 0 if fill == "zero" else case["RQ"]
+    _run_and_compare(case, split=1)
+
+
+@pytest.mark.parametrize("B,H,Q", [(3, 4, 2), (1, 1, 8), (7, 3, 5)])
+def test_fewer_items_than_sms_whole_items(B, H, Q):
+    """Persistent CTAs with fewer items than SMs (one item per CTA, the rest
+    idle), odd head counts, a single head."""
+    case = synth.replay_verify_case(B=B, H=H, Q=Q, slots=B + 4, seed=50 + B * 10 + H)
+    _run_and_compare(case, split=1)
+
+
+@pytest.mark.parametrize("lower_bound", [-10.0, 0.0])
+def test_gate_bound_extremes(lower_bound):
+    """At the largest supported |lower_bound| the decay products over the
+    window span e^-80 (1/Gamma stays finite in FP32); at 0 there is no decay
+    (the plain delta rule)."""
+    case = synth.replay_verify_case(B=16, H=4, Q=8, slots=24, seed=61)
+    case["lower_bound"] = lower_bound
+    _run_and_compare(case, split=1)
