@@ -499,7 +499,105 @@ def measure_rows(dev, stream, peak, cpu_seconds):
     for _ in range(5):
         book()
     rows["bookkeeping_us_b512"] = 1e3 * _event_ms(stream, book, 50)
+    del slots, rrows, pend, lens, plan
+
+    rows["decode_loop"] = measure_decode_loop(dev, dt, peak)
     return rows
+
+
+def decode_loop_bytes(c, eager):
+    """Algorithmic bytes of one graph of the decode workload.  Deferred:
+    the stock verify, then fused steps whose pending counts are the previous
+    step's accepted counts, then the flush's in-place commit of the last
+    step's.  Eager: every step the stock verify and a commit of its accepted
+    tokens.  The bookkeeping's few bytes per request are left out."""
+    steps, live = c["steps"], c["state_slots"] > c["null_slot"]
+
+    def commit_bytes(lens):
+        return commit_algorithmic_bytes(dict(
+            L=1, B=c["B"], H=c["H"], Q=c["RQ"], layers=[dict(state=c["state"])],
+            commit_lens=np.where(live & (c["record_rows"] >= 0), lens, 0),
+            sources=c["state_slots"], destinations=c["state_slots"],
+            boundaries=np.zeros(c["B"], np.int32), boundary_lens=np.zeros(c["B"], np.int32),
+            null_slot=c["null_slot"]))
+    total = 0
+    for s in range(steps):
+        if eager or s == 0:
+            total += verify_algorithmic_bytes(c)
+        else:
+            step = dict(c)
+            step["pending"] = np.zeros_like(c["pending"])
+            has = live & (c["record_rows"] >= 0)
+            step["pending"][c["record_rows"][has]] = c["accepted"][s - 1][has]
+            total += algorithmic_bytes(step)["total"]
+        if eager:
+            total += commit_bytes(c["accepted"][s])
+    if not eager:
+        total += commit_bytes(c["accepted"][steps - 1])
+    return total
+
+
+def measure_decode_loop(dev, dt, peak):
+    """Eight decode steps of the large batch as one CUDA graph, in two
+    schedules: deferred (the fused replay + verify; the stock verify after
+    each flush; defer after sampling; a flush after the eighth step) and
+    eager (the stock verify, then a commit of the accepted tokens every
+    step, which reads and writes every live checkpoint once more)."""
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import DeferredRecoverSSM, synth
+    name = "decode-loop-f32-h64-b512-q8"
+    c = synth.make(name)
+    steps, B, H, Q = c["steps"], c["B"], c["H"], c["Q"]
+    keys = ("q", "k", "v", "raw_g", "raw_beta")
+    d = {n: dt(c[n]) for n in ("A_log", "dt_bias", "state", "state_slots", "record_rows",
+                               "pending", "corr", "key_gate")}
+    win = {key: dt(c["windows"][key]) for key in keys}
+    acc0 = dt(c["accepted"])
+    acc = acc0.clone()
+    eager_all = torch.ones(B, dtype=torch.uint8, device=dev)
+    out = torch.zeros(c["windows"]["v"].shape[1:], dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream()  # graphs are captured on a side stream
+    loop = DeferredRecoverSSM(d["state"], d["state_slots"], d["record_rows"], d["pending"],
+                              d["corr"], d["key_gate"], d["A_log"], d["dt_bias"], Q=Q,
+                              lower_bound=c["lower_bound"], q_scale=c["q_scale"],
+                              stream=stream)
+
+    def cycle(eager):
+        acc.copy_(acc0)
+        loop.flushed = True
+        for s in range(steps):
+            w = int(c["window_of_step"][s])
+            if eager:
+                loop.flushed = True
+            loop.verify(*(win[key][w] for key in keys), out)
+            loop.accept(acc[s], eager_all if eager else None)
+        if not eager:
+            loop.flush()
+
+    live = c["state_slots"] > 0
+    tokens = int(live.sum()) * Q
+    accepted = int(c["accepted"][:, live].sum()) / steps
+    row = dict(workload=name, steps_per_graph=steps,
+               launches_per_graph=dict(deferred=2 * steps + 2, eager=3 * steps))
+    torch.cuda.synchronize()
+    for eager in (False, True):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            cycle(eager)  # warm-up outside the graph
+            with torch.cuda.graph(g, stream=stream):
+                cycle(eager)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ms = _event_ms(torch.cuda.current_stream(), g.replay, 5) / steps
+        nbytes = decode_loop_bytes(c, eager)
+        gbs = nbytes / (ms * steps) / 1e6
+        row["eager" if eager else "deferred"] = dict(
+            ms_per_step=ms, verify_tok_s=tokens / (ms / 1e3),
+            accepted_tok_s=accepted / (ms / 1e3), bytes_per_graph=nbytes,
+            roofline=dict(bound="hbm", achieved=gbs, peak=peak, unit="GB/s", frac=gbs / peak))
+    row["eager_over_deferred"] = row["eager"]["ms_per_step"] / row["deferred"]["ms_per_step"]
+    return row
 
 
 # ---------------------------------------------------------------------------

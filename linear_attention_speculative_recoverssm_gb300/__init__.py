@@ -2,7 +2,8 @@
 
 The compute lives in libkda_recoverssm.so (hand-written CUDA kernels behind a
 C ABI, declared in include/kda_recoverssm.h).  This package holds the build
-script (``_build``), the thin ctypes binding (``_lib``) and the seeded
+script (``_build``), the thin ctypes binding (``_lib``), the deferred
+RecoverSSM's step sequencing across decode steps (``decode``) and the seeded
 synthetic-input generator (``synth``).  Calling any entry point without the
 built library raises ImportError; there is no CPU fallback.
 """
@@ -26,3 +27,4 @@ from ._lib import (  # noqa: F401
     layer_tables,
     load,
 )
+from .decode import DeferredRecoverSSM  # noqa: F401

@@ -134,6 +134,47 @@ def replay_verify_case(*, B, H, Q, slots, seed, RQ=None, rows=None, K=128,
     return case
 
 
+def decode_loop_case(*, B, H, Q, slots, steps, seed, windows=None, K=128, V=128,
+                     padding_frac=0.0, accept_min=0, eager_frac=0.0):
+    """Operands of a multi-step speculative decode of one layer.
+
+    The first step's operands are those of ``replay_verify_case`` with every
+    live request owning a record row and nothing pending yet.  Added:
+
+    * ``windows``: each step's q, k, v, raw_g [steps, B*Q, H, K|V] and
+      raw_beta [steps, B*Q, H] (BF16 bits), drawn like the first window (step
+      0 is the first window itself); with ``windows=W`` only W distinct
+      windows are drawn and step s uses window s mod W;
+    * ``accepted`` [steps, B] int32: how many of the step's Q tokens sampling
+      accepts, uniform on accept_min..Q;
+    * ``eager`` [steps, B] uint8: the rows committed at once instead of
+      deferred, an ``eager_frac`` share of the requests per step.
+    """
+    case = replay_verify_case(B=B, H=H, Q=Q, slots=slots, seed=seed, K=K, V=V,
+                              padding_frac=padding_frac)
+    case["pending"][:] = 0
+    rng = np.random.default_rng(seed + 7919)
+    n_win = steps if windows is None else min(windows, steps)
+    T = B * Q
+    keys = ("q", "k", "v", "raw_g", "raw_beta")
+    stacks = {key: np.empty((n_win,) + case[key].shape, dtype=np.uint16) for key in keys}
+    for key in keys:
+        stacks[key][0] = case[key]
+    for w in range(1, n_win):
+        q = _unit_directions(rng, (T, H, K)) * np.float32(K ** -0.5)
+        stacks["q"][w] = to_bf16_bits(q)
+        stacks["k"][w] = to_bf16_bits(_unit_directions(rng, (T, H, K)))
+        stacks["v"][w] = to_bf16_bits(_normal(rng, (T, H, V)))
+        stacks["raw_g"][w] = to_bf16_bits(_normal(rng, (T, H, K)))
+        stacks["raw_beta"][w] = to_bf16_bits(_normal(rng, (T, H)))
+    case["windows"] = stacks
+    case["window_of_step"] = np.arange(steps, dtype=np.int64) % n_win
+    case["accepted"] = rng.integers(accept_min, Q + 1, size=(steps, B), dtype=np.int32)
+    case["eager"] = (rng.random((steps, B)) < eager_frac).astype(np.uint8)
+    case["steps"] = steps
+    return case
+
+
 def commit_case(*, L, B, H, Q, slots, seed, K=128, V=128, state_dtype="bf16",
                 null_frac=0.10, in_place_frac=0.5, boundary_frac=0.25):
     """Operands of the standalone commit over L layers.
@@ -199,7 +240,8 @@ def commit_case(*, L, B, H, Q, slots, seed, K=128, V=128, state_dtype="bf16",
     )
 
 
-# The workloads of the five measured configurations, by what they are.
+# The workloads of the five measured configurations and the measured next
+# rows, by what they are.
 WORKLOADS = {
     "tiny-b2-h2-q2": dict(kind="replay_verify", B=2, H=2, Q=2, slots=4,
                           seed=0),
@@ -211,6 +253,12 @@ WORKLOADS = {
     "replay-verify-f32-h64-b512-q8": dict(kind="replay_verify", B=512, H=64,
                                           Q=8, slots=1024, seed=3,
                                           padding_frac=0.05),
+    # eight decode steps of the large-batch shape (a flush after every
+    # eighth, so the first step of each cycle is the stock verify); sampling
+    # accepts 1..8 tokens per request and step; two distinct windows
+    "decode-loop-f32-h64-b512-q8": dict(kind="decode_loop", B=512, H=64, Q=8,
+                                        slots=1024, steps=8, seed=6, windows=2,
+                                        padding_frac=0.05, accept_min=1),
     # the large-batch shape at a quarter of the requests (the same kernel
     # instance, ~0.6 GB of state): small enough for a full profiler capture
     "replay-verify-f32-h64-b128-q8": dict(kind="replay_verify", B=128, H=64,
@@ -226,6 +274,8 @@ def make(name, **overrides):
     kind = spec.pop("kind")
     if kind == "commit":
         return commit_case(**spec)
+    if kind == "decode_loop":
+        return decode_loop_case(**spec)
     return replay_verify_case(**spec)
 
 

@@ -33,6 +33,11 @@ What it computes, and where the pages define it (page titles as printed):
 * ``defer_commit`` / ``flush_plan`` -- the two bookkeeping steps, as integer
   code (page "...recoverssm.kernels", ``_defer_commit_kernel`` and
   ``_prepare_flush_plan_kernel``).
+* ``decode_stock`` -- several decode steps of one layer by the stock
+  recurrence alone (verify every window from the state, then advance the
+  state by the accepted tokens, ``advance_item``): the result the deferred
+  protocol (records, pending replays, eager commits, flushes) must equal
+  (page "...cutedsl.kda.fused", module docstring).
 
 Self-check formulations, used only by the oracle's own pin tests:
 
@@ -183,6 +188,22 @@ def verify_item(S, q, k, v, raw_g, raw_beta, a_log, dt_bias, lower_bound,
         S = S + np.outer(u[t], kn)
         o[t] = S @ qn
     return u, o
+
+
+def advance_item(S, k, v, raw_g, raw_beta, a, a_log, dt_bias, lower_bound):
+    """The state after the first ``a`` tokens of a window by the stock
+    recurrence, S <- S diag(d_t); u_t = beta_t (v_t - S kn_t);
+    S <- S + u_t kn_t^T: the checkpoint that committing ``a`` accepted tokens
+    yields.  Returns a new FP64 array; S is not modified."""
+    S = np.array(S, dtype=np.float64, copy=True)
+    for t in range(a):
+        d = decay(raw_g[t], a_log, dt_bias, lower_bound)
+        kn = l2norm(k[t])
+        beta = sigmoid(raw_beta[t])
+        S = S * d[None, :]
+        u = beta * (v[t] - S @ kn)
+        S = S + np.outer(u, kn)
+    return S
 
 
 # --------------------------------------------------------------------------
@@ -339,6 +360,47 @@ def flush_plan(*, state_slots, record_rows, pending, commit_lens, final_slots,
         final_slots[b] = slot
         boundary_slots[b] = null_slot
         boundary_lens[b] = 0
+
+
+def decode_stock(*, windows, window_of_step, accepted, A_log, dt_bias,
+                 lower_bound, q_scale, state, state_slots, B, H, Q,
+                 null_slot=0, items=None):
+    """Speculative decoding of one layer over several steps by the stock
+    recurrence alone, with no records, deferral or flush: per live item an
+    FP64 state starts from its pool page; at every step the window is
+    verified from the state (outputs), then the state advances by the
+    window's first accepted tokens (page "...cutedsl.kda.fused", module
+    docstring: what the deferred RecoverSSM must reproduce; the accepted count
+    is what sampling records as the pending replay).
+
+    windows: q, k, v, raw_g [W, B*Q, H, K|V] and raw_beta [W, B*Q, H] (BF16
+    bits), step s using window ``window_of_step[s]``; accepted [steps, B],
+    clamped to [0, Q].  Returns (outs, finals): outs [steps, B*Q, H, V] FP64
+    (zero on inert rows) and finals, a dict (b, h) -> the FP64 state after
+    the last step.
+    """
+    steps = accepted.shape[0]
+    V = state.shape[2]
+    outs = np.zeros((steps, B * Q, H, V))
+    finals = {}
+    for b, h in _items(B, H, items):
+        slot = int(state_slots[b])
+        if slot <= null_slot:
+            continue
+        a_log = float(A_log[h])
+        bias = dt_bias[h].astype(np.float64)
+        tok = slice(b * Q, (b + 1) * Q)
+        S = state_to_f64(state[slot, h])
+        for s in range(steps):
+            w = int(window_of_step[s])
+            q, k, v, g, beta = (bf16_to_f64(windows[key][w, tok, h])
+                                for key in ("q", "k", "v", "raw_g", "raw_beta"))
+            _, outs[s, tok, h] = verify_item(S, q, k, v, g, beta, a_log, bias,
+                                             lower_bound, q_scale)
+            a = min(max(int(accepted[s, b]), 0), Q)
+            S = advance_item(S, k, v, g, beta, a, a_log, bias, lower_bound)
+        finals[(b, h)] = S
+    return outs, finals
 
 
 # --------------------------------------------------------------------------

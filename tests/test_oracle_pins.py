@@ -447,3 +447,150 @@ def test_bookkeeping_hand_worked():
                   pending=np.array(f["pending"], np.int32), B=B, Q=f["Q"], **plan)
     for k, v in f["expect"].items():
         np.testing.assert_array_equal(plan[k], v)
+
+
+# ---------------------------------------------------------------------------
+# several decode steps: the stock recurrence and the deferred protocol
+# ---------------------------------------------------------------------------
+
+_WINDOW_KEYS = ("q", "k", "v", "raw_g", "raw_beta")
+
+
+def _decode_case(**kw):
+    base = dict(B=6, H=2, Q=3, slots=16, steps=7, seed=31, K=8, V=6)
+    base.update(kw)
+    return synth.decode_loop_case(**base)
+
+
+def _stock(case, **kw):
+    return ko.decode_stock(windows=case["windows"], window_of_step=case["window_of_step"],
+                           accepted=case["accepted"], A_log=case["A_log"],
+                           dt_bias=case["dt_bias"], lower_bound=case["lower_bound"],
+                           q_scale=case["q_scale"], state=case["state"],
+                           state_slots=case["state_slots"], B=case["B"], H=case["H"],
+                           Q=case["Q"], **kw)
+
+
+def _oracle_protocol(case, flush_every):
+    """The deferred protocol run by the oracle's own step functions: a fused
+    step (or the stock verify right after a flush), then defer with the eager
+    rows committed at once, and a flush every ``flush_every`` steps and at the
+    end.  Returns (FP64 outputs per step, the final pool)."""
+    c = {key: (val.copy() if isinstance(val, np.ndarray) else val) for key, val in case.items()}
+    B, H, Q = c["B"], c["H"], c["Q"]
+    slots, rows = c["state_slots"], c["record_rows"]
+    layer = dict(state=c["state"], corr=c["corr"], key_gate=c["key_gate"])
+    common = dict(A_log=c["A_log"][None], dt_bias=c["dt_bias"][None],
+                  lower_bound=c["lower_bound"], Q=c["RQ"], B=B, H=H, record_rows=rows)
+    outs, flushed = [], False
+    steps = c["accepted"].shape[0]
+    for s in range(steps):
+        win = {key: c["windows"][key][c["window_of_step"][s]] for key in _WINDOW_KEYS}
+        out = np.zeros(win["v"].shape, dtype=np.uint16)
+        out64 = np.zeros(win["v"].shape)
+        ko.replay_verify(**win, A_log=c["A_log"], dt_bias=c["dt_bias"],
+                         lower_bound=c["lower_bound"], q_scale=c["q_scale"], state=c["state"],
+                         state_slots=slots, record_rows=rows, corr=c["corr"],
+                         key_gate=c["key_gate"], out=out, B=B, H=H, Q=Q,
+                         pending=None if flushed else c["pending"], out_f64=out64)
+        outs.append(out64)
+        lens = c["accepted"][s].copy()
+        eager = c["eager"][s]
+        ko.defer_commit(state_slots=slots, commit_lens=lens, record_rows=rows,
+                        pending=c["pending"], B=B, eager=eager)
+        if eager.any():
+            ko.commit(layers=[layer], sources=slots, commit_lens=lens, destinations=slots,
+                      **common)
+        flushed = False
+        if (s + 1) % flush_every == 0 or s == steps - 1:
+            plan = dict(commit_lens=np.zeros(B, np.int32), final_slots=np.zeros(B, np.int32),
+                        boundary_slots=np.zeros(B, np.int32),
+                        boundary_lens=np.zeros(B, np.int32))
+            ko.flush_plan(state_slots=slots, record_rows=rows, pending=c["pending"], B=B, Q=Q,
+                          **plan)
+            ko.commit(layers=[layer], sources=slots, commit_lens=plan["commit_lens"],
+                      destinations=plan["final_slots"], boundaries=plan["boundary_slots"],
+                      boundary_lens=plan["boundary_lens"], **common)
+            flushed = True
+    return outs, c["state"]
+
+
+@pytest.mark.parametrize("flush_every,eager_frac", [(3, 0.3), (100, 0.0), (1, 0.5)])
+def test_deferred_protocol_equals_stock_recurrence(flush_every, eager_frac):
+    # Records, pending replays, eager commits and flushes are a schedule of
+    # the stock recurrence: outputs and final checkpoints agree with it up to
+    # the FP32 roundings of records and checkpoints.
+    case = _decode_case(padding_frac=0.2, eager_frac=eager_frac)
+    assert case["accepted"].any() and (case["accepted"] < case["Q"]).any()
+    outs, pool = _oracle_protocol(case, flush_every)
+    ref_outs, finals = _stock(case)
+    for s, o in enumerate(outs):
+        scale = np.abs(ref_outs[s]).max()
+        assert np.abs(o - ref_outs[s]).max() <= 1e-5 * scale, f"step {s}"
+    live = [(b, h) for b in range(case["B"]) for h in range(case["H"])
+            if case["state_slots"][b] > 0]
+    assert set(finals) == set(live)
+    for (b, h), S in finals.items():
+        got = pool[case["state_slots"][b], h].astype(np.float64)
+        assert np.abs(got - S).max() <= 1e-5 * np.abs(S).max(), (b, h)
+    for b in range(case["B"]):
+        if case["state_slots"][b] <= 0:
+            assert not any(o[b * case["Q"]:(b + 1) * case["Q"]].any() for o in ref_outs)
+
+
+def test_decode_stock_nothing_accepted_keeps_the_checkpoint():
+    # No token accepted: the state never moves, so every step's outputs are
+    # the one-window verify from the initial page.
+    case = _decode_case()
+    case["accepted"][:] = 0
+    ref_outs, finals = _stock(case)
+    for (b, h), S in finals.items():
+        np.testing.assert_array_equal(S, case["state"][case["state_slots"][b], h])
+    for s in range(case["steps"]):
+        step = dict(case)
+        for key in _WINDOW_KEYS:
+            step[key] = case["windows"][key][case["window_of_step"][s]]
+        step["state"] = case["state"].copy()
+        out64 = np.zeros(ref_outs[s].shape)
+        _run(step, pending=False, out_f64=out64)
+        np.testing.assert_allclose(ref_outs[s], out64, rtol=0, atol=1e-12)
+
+
+def test_decode_stock_without_decay_or_writes_is_a_fixed_gemv():
+    # lower_bound = 0 gives d = 1 and beta = sigmoid(-inf) = 0 gives u = 0:
+    # the state is S_0 forever and o_t = S_0 qn_t at every step.
+    case = _decode_case(B=3, H=2, Q=2, K=6, V=5)
+    case["lower_bound"] = 0.0
+    case["windows"]["raw_beta"][:] = 0xFF80  # BF16 -inf
+    ref_outs, finals = _stock(case)
+    K = case["windows"]["q"].shape[-1]
+    for (b, h), S in finals.items():
+        S0 = case["state"][case["state_slots"][b], h].astype(np.float64)
+        np.testing.assert_array_equal(S, S0)
+        for s in range(case["steps"]):
+            w = case["window_of_step"][s]
+            for t in range(case["Q"]):
+                q = ko.bf16_to_f64(case["windows"]["q"][w, b * case["Q"] + t, h])
+                qn = q / math.sqrt(float(q @ q) + 1e-6) * case["q_scale"]
+                np.testing.assert_allclose(ref_outs[s][b * case["Q"] + t, h], S0 @ qn,
+                                           rtol=1e-13, atol=1e-15)
+    assert K == 6
+
+
+def test_decode_stock_full_acceptance_is_one_long_recurrence():
+    # Accepting every token of every window makes the steps one sequential
+    # recurrence over the concatenated windows: step s's outputs are the
+    # long verify's outputs at positions s*Q .. s*Q + Q - 1.
+    case = _decode_case(B=1, H=1, Q=3, steps=5)
+    case["accepted"][:] = case["Q"]
+    ref_outs, finals = _stock(case)
+    Q, steps = case["Q"], case["steps"]
+    seq = {key: np.concatenate([case["windows"][key][case["window_of_step"][s]]
+                                for s in range(steps)])[:, 0] for key in _WINDOW_KEYS}
+    S0 = case["state"][case["state_slots"][0], 0]
+    _, o = ko.verify_item(S0, *(ko.bf16_to_f64(seq[key]) for key in _WINDOW_KEYS),
+                          float(case["A_log"][0]), case["dt_bias"][0].astype(np.float64),
+                          case["lower_bound"], case["q_scale"])
+    for s in range(steps):
+        np.testing.assert_allclose(ref_outs[s][:, 0], o[s * Q:(s + 1) * Q], rtol=1e-12,
+                                   atol=1e-14)
