@@ -60,15 +60,18 @@ def algorithmic_bytes(case):
     written; with a record row, Q corrections and Q key/gate records
     (512 + 512 B per token) written.  Per inert item: its outputs (zeros)
     written.  Plus the per-request indices and the per-head gate
-    parameters, read once.
+    parameters, read once.  With windows of different lengths (``q_lens``)
+    each request's q_b replaces Q.
     """
     B, H, Q, RQ = case["B"], case["H"], case["Q"], case["RQ"]
     slots, rows, pending = case["state_slots"], case["record_rows"], case["pending"]
+    q_lens = case.get("q_lens")
     page = DIM * DIM * 4
     total = 0
     state = 0
     live_items = 0
     for b in range(B):
+        Q = int(q_lens[b]) if q_lens is not None else case["Q"]
         if slots[b] <= case["null_slot"]:
             total += H * Q * DIM * 2
             continue
@@ -83,7 +86,11 @@ def algorithmic_bytes(case):
         total += H * per
         live_items += H
     total += B * 4 * 2 + len(pending) * 0 + H * (4 + DIM * 4)
-    live_tokens = int((slots > case["null_slot"]).sum()) * Q
+    if q_lens is not None:
+        total += (B + 1) * 4
+        live_tokens = int(q_lens[slots > case["null_slot"]].sum())
+    else:
+        live_tokens = int((slots > case["null_slot"]).sum()) * case["Q"]
     return dict(total=total, state=state, live_items=live_items, live_tokens=live_tokens)
 
 
@@ -453,6 +460,30 @@ def measure_rows(dev, stream, peak, cpu_seconds):
         roofline=dict(bound="hbm", achieved=nbytes / ms / 1e6, peak=peak, unit="GB/s",
                       frac=nbytes / ms / 1e6 / peak))
     del d, out
+
+    # the large batch with windows of 1..8 tokens (query_start_loc)
+    name = "replay-verify-varlen-f32-h64-b512-q8"
+    c = synth.make(name)
+    d = {n: dt(c[n]) for n in names + ("query_start_loc",)}
+    out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
+
+    def step_varlen():
+        kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"],
+                          d["dt_bias"], d["state"], d["state_slots"], d["record_rows"],
+                          d["pending"], d["corr"], d["key_gate"], out, Q=c["Q"],
+                          lower_bound=c["lower_bound"], q_scale=c["q_scale"], split=0,
+                          query_start_loc=d["query_start_loc"], stream=stream)
+    for _ in range(5):
+        step_varlen()
+    ms = _event_ms(stream, step_varlen, 50)
+    ab_v = algorithmic_bytes(c)
+    rows["replay_verify_varlen"] = dict(
+        workload=name, ms=ms, tok_s=ab_v["live_tokens"] / (ms / 1e3),
+        mean_window=float(c["q_lens"][c["state_slots"] > c["null_slot"]].mean()),
+        bytes_per_launch=ab_v["total"],
+        roofline=dict(bound="hbm", achieved=ab_v["total"] / ms / 1e6, peak=peak, unit="GB/s",
+                      frac=ab_v["total"] / ms / 1e6 / peak))
+    del d, out, c
 
     # small batches: per-launch device time (a CUDA graph of 20 launches)
     lat = {}

@@ -24,7 +24,16 @@
  *    `stream` (a cudaStream_t passed as void*, NULL = the legacy default
  *    stream) and returns at once.
  *  - BF16 tensors are passed as raw bit patterns (kda_bf16, uint16_t).
- *  - Activations are token-major: token b*Q + t belongs to request b.
+ *  - Activations are token-major, [n_tokens, H, 128].  Without
+ *    query_start_loc, token b*Q + t is token t of request b's window and
+ *    n_tokens = B*Q.  With query_start_loc ([B + 1] int32, the stock
+ *    wrapper's argument), request b's window is tokens query_start_loc[b]
+ *    .. query_start_loc[b + 1] - 1, of length q_b <= Q, and n_tokens <= B*Q
+ *    (its activation-capacity check).  A request whose window does not lie
+ *    in 0 .. n_tokens or is longer than Q is reported as KDA_ERR_ARG in the
+ *    status word and nothing of it is read or written.  Only a window's q_b
+ *    tokens are verified and only their outputs and records are written;
+ *    the replay of pending tokens does not depend on the window.
  *  - A state slot is inert when slot <= null_slot (the pages use 0).  A
  *    record row < 0 means the request has none.
  *  - Live slots, destinations, boundary slots and record rows must be
@@ -42,8 +51,9 @@
  *                           row stride is not a multiple of 16 bytes;
  *      KDA_ERR_UNSUPPORTED  unknown state dtype, or K / V != 128;
  *      KDA_ERR_CUDA         the launch itself failed.
- *  - B == 0 is a no-op that returns KDA_OK (the stock wrapper returns early
- *    on zero tokens).
+ *  - B == 0 is a no-op that returns KDA_OK whatever the other arguments;
+ *    so is n_tokens == 0 once the arguments pass the checks (the stock
+ *    wrapper returns early on zero tokens).
  */
 #ifndef KDA_RECOVERSSM_H
 #define KDA_RECOVERSSM_H
@@ -88,21 +98,24 @@ const char *kda_error_string(int status);
  *   S <- S diag(d_t); u_t = sigmoid(raw_beta_t) (v_t - S kn_t);
  *   S <- S + u_t kn_t^T; o_t = S qn_t
  * computed in the equivalent chunked form of the "kda.fused" page (step 2):
- * the state is only read.  Writes out[b*Q + t, h, :] = BF16(o_t) and, when
+ * the state is only read.  (With query_start_loc, t < q_b and token
+ * query_start_loc[b] + t replace t < Q and token b*Q + t.)  Writes
+ * out[b*Q + t, h, :] = BF16(o_t) and, when
  * the record row r (record_rows[b], or b when record_rows is NULL) is >= 0,
  * corr[r, h, t, :] = u_t (FP32), key_gate[r, h, t, 0:128] = k_t and
  * key_gate[r, h, t, 128:256] = raw_g_t (BF16 copies).  Inert requests
  * write zeros to `out` only.
  *
- *   q, k, raw_g   [B*Q, H, 128] BF16;  v [B*Q, H, 128] BF16
- *   raw_beta      [B*Q, H] BF16
+ *   q, k, raw_g   [n_tokens, H, 128] BF16;  v [n_tokens, H, 128] BF16
+ *   raw_beta      [n_tokens, H] BF16
+ *   query_start_loc [B + 1] int32 or NULL (see the conventions above)
  *   A_log [H] FP32; dt_bias [H, 128] FP32
  *   state_pool    [n_slots, H, 128, 128] of state_dtype, slot stride
  *                 `slot_stride` elements (>= H*128*128)
  *   state_slots   [B] int32; record_rows [B] int32 or NULL
  *   corr          [n_rows, H, rq, 128] FP32, row stride corr_row_stride
  *   key_gate      [n_rows, H, rq, 256] BF16, row stride kg_row_stride
- *   out           [B*Q, H, 128] BF16
+ *   out           [n_tokens, H, 128] BF16
  *   1 <= Q <= rq <= 8; H >= 1; -10 <= lower_bound <= 10 (a bounded gate:
  *   the chunked form divides by prod_{r<=t} d_r, which must stay inside
  *   FP32; KDA_ERR_UNSUPPORTED otherwise).
@@ -112,6 +125,7 @@ int kda_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                const float *A_log, const float *dt_bias, float lower_bound,
                float q_scale, const void *state_pool, int state_dtype,
                int64_t slot_stride, int n_slots, const int32_t *state_slots,
+               const int32_t *query_start_loc, int n_tokens,
                const int32_t *record_rows, float *corr, kda_bf16 *key_gate,
                int64_t corr_row_stride, int64_t kg_row_stride, int n_rows,
                int rq, kda_bf16 *out, int B, int H, int Q, int null_slot,
@@ -143,7 +157,9 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                       const float *A_log, const float *dt_bias,
                       float lower_bound, float q_scale, float *state_pool,
                       int64_t slot_stride, int n_slots,
-                      const int32_t *state_slots, const int32_t *record_rows,
+                      const int32_t *state_slots,
+                      const int32_t *query_start_loc, int n_tokens,
+                      const int32_t *record_rows,
                       const int32_t *pending, float *corr, kda_bf16 *key_gate,
                       int64_t corr_row_stride, int64_t kg_row_stride,
                       int n_rows, int rq, const int32_t *boundary_slots,

@@ -35,10 +35,11 @@ _F = ctypes.c_float
 _SIGS = {
     "kda_abi_version": ([], _I),
     "kda_error_string": ([_I], ctypes.c_char_p),
-    "kda_verify": ([_P] * 7 + [_F, _F, _P, _I, _I64, _I, _P, _P, _P, _P, _I64, _I64, _I, _I,
-                    _P, _I, _I, _I, _I, _P, _P], _I),
-    "kda_replay_verify": ([_P] * 7 + [_F, _F, _P, _I64, _I, _P, _P, _P, _P, _P, _I64, _I64,
-                           _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "kda_verify": ([_P] * 7 + [_F, _F, _P, _I, _I64, _I, _P, _P, _I, _P, _P, _P, _I64, _I64,
+                               _I, _I, _P, _I, _I, _I, _I, _P, _P], _I),
+    "kda_replay_verify": ([_P] * 7 + [_F, _F, _P, _I64, _I, _P, _P, _I, _P, _P, _P, _P, _I64,
+                                      _I64, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
+                          _I),
     "kda_commit": ([_P] * 14 + [_I, _F, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "kda_defer_commit": ([_P] * 5 + [_I, _I, _I, _P, _P], _I),
     "kda_flush_plan": ([_P] * 7 + [_I, _I, _I, _I, _P, _P], _I),
@@ -113,13 +114,17 @@ def _check_step_dtypes(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_slots, re
 
 
 def kda_verify(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, state_slots, corr,
-               key_gate, out, *, Q, lower_bound, q_scale, record_rows=None, null_slot=0,
-               status=None, stream=None, raise_on_error=True):
+               key_gate, out, *, Q, lower_bound, q_scale, record_rows=None,
+               query_start_loc=None, null_slot=0, status=None, stream=None,
+               raise_on_error=True):
     """Stock verify of one window (state read only).  Shapes as in
-    include/kda_recoverssm.h; state_pool is float32 or bfloat16."""
+    include/kda_recoverssm.h; state_pool is float32 or bfloat16; the
+    activations' first dimension is the token count (B*Q without
+    query_start_loc)."""
     import torch
     _check_step_dtypes(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_slots, record_rows,
                        corr, key_gate, out)
+    _expect(query_start_loc, torch.int32, "query_start_loc")
     dtype = KDA_STATE_F32 if state_pool.dtype == torch.float32 else KDA_STATE_BF16
     if state_pool.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("state_pool must be float32 or bfloat16")
@@ -128,20 +133,22 @@ def kda_verify(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, state_slots
     rc = load().kda_verify(
         _ptr(q), _ptr(k), _ptr(v), _ptr(raw_g), _ptr(raw_beta), _ptr(A_log), _ptr(dt_bias),
         lower_bound, q_scale, _ptr(state_pool), dtype, state_pool.stride(0),
-        state_pool.shape[0], _ptr(state_slots), _ptr(record_rows), _ptr(corr), _ptr(key_gate),
-        corr.stride(0), key_gate.stride(0), corr.shape[0], corr.shape[2], _ptr(out), B, H, Q,
-        null_slot, _ptr(status), _stream(stream))
+        state_pool.shape[0], _ptr(state_slots), _ptr(query_start_loc), q.shape[0],
+        _ptr(record_rows), _ptr(corr), _ptr(key_gate), corr.stride(0), key_gate.stride(0),
+        corr.shape[0], corr.shape[2], _ptr(out), B, H, Q, null_slot, _ptr(status),
+        _stream(stream))
     return _check("kda_verify", rc, raise_on_error)
 
 
 def kda_replay_verify(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, state_slots,
                       record_rows, pending, corr, key_gate, out, *, Q, lower_bound, q_scale,
-                      boundary_slots=None, boundary_lens=None, null_slot=0, split=0,
-                      status=None, stream=None, raise_on_error=True):
+                      boundary_slots=None, boundary_lens=None, query_start_loc=None,
+                      null_slot=0, split=0, status=None, stream=None, raise_on_error=True):
     """Fused replay + verify (FP32 state pool, written in place)."""
     import torch
     _check_step_dtypes(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_slots, record_rows,
                        corr, key_gate, out)
+    _expect(query_start_loc, torch.int32, "query_start_loc")
     _expect(state_pool, torch.float32, "state_pool")
     _expect(pending, torch.int32, "pending")
     B = state_slots.shape[0]
@@ -149,10 +156,10 @@ def kda_replay_verify(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, stat
     rc = load().kda_replay_verify(
         _ptr(q), _ptr(k), _ptr(v), _ptr(raw_g), _ptr(raw_beta), _ptr(A_log), _ptr(dt_bias),
         lower_bound, q_scale, _ptr(state_pool), state_pool.stride(0), state_pool.shape[0],
-        _ptr(state_slots), _ptr(record_rows), _ptr(pending), _ptr(corr), _ptr(key_gate),
-        corr.stride(0), key_gate.stride(0), corr.shape[0], corr.shape[2],
-        _ptr(boundary_slots), _ptr(boundary_lens), _ptr(out), B, H, Q, null_slot, split,
-        _ptr(status), _stream(stream))
+        _ptr(state_slots), _ptr(query_start_loc), q.shape[0], _ptr(record_rows), _ptr(pending),
+        _ptr(corr), _ptr(key_gate), corr.stride(0), key_gate.stride(0), corr.shape[0],
+        corr.shape[2], _ptr(boundary_slots), _ptr(boundary_lens), _ptr(out), B, H, Q,
+        null_slot, split, _ptr(status), _stream(stream))
     return _check("kda_replay_verify", rc, raise_on_error)
 
 

@@ -20,6 +20,14 @@ int launch_step_q5(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q6(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q7(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q8(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_varlen_q1(const StepParams &, int, int, cudaStream_t);
+int launch_step_varlen_q2(const StepParams &, int, int, cudaStream_t);
+int launch_step_varlen_q3(const StepParams &, int, int, cudaStream_t);
+int launch_step_varlen_q4(const StepParams &, int, int, cudaStream_t);
+int launch_step_varlen_q5(const StepParams &, int, int, cudaStream_t);
+int launch_step_varlen_q6(const StepParams &, int, int, cudaStream_t);
+int launch_step_varlen_q7(const StepParams &, int, int, cudaStream_t);
+int launch_step_varlen_q8(const StepParams &, int, int, cudaStream_t);
 
 namespace {
 std::atomic<int> g_sm_count[64];
@@ -38,6 +46,21 @@ int device_sm_count(int dev) {
 
 int launch_step(const StepParams &p, int n_items, int Q, int variant, int split,
                 cudaStream_t stream) {
+  // windows from query_start_loc on the persistent kernel: its own instances
+  // (the cluster split reads the windows at run time)
+  if (p.qsl != nullptr && split == 1) {
+    switch (Q) {
+      case 1: return launch_step_varlen_q1(p, n_items, variant, stream);
+      case 2: return launch_step_varlen_q2(p, n_items, variant, stream);
+      case 3: return launch_step_varlen_q3(p, n_items, variant, stream);
+      case 4: return launch_step_varlen_q4(p, n_items, variant, stream);
+      case 5: return launch_step_varlen_q5(p, n_items, variant, stream);
+      case 6: return launch_step_varlen_q6(p, n_items, variant, stream);
+      case 7: return launch_step_varlen_q7(p, n_items, variant, stream);
+      case 8: return launch_step_varlen_q8(p, n_items, variant, stream);
+      default: return KDA_ERR_ARG;
+    }
+  }
   switch (Q) {
     case 1: return launch_step_q1(p, n_items, variant, split, stream);
     case 2: return launch_step_q2(p, n_items, variant, split, stream);
@@ -73,10 +96,16 @@ int check_step_args(const void *q, const void *k, const void *v, const void *g,
                     const void *state_pool, int state_bytes, int64_t slot_stride, int n_slots,
                     const void *state_slots, const void *corr, const void *key_gate,
                     int64_t corr_row_stride, int64_t kg_row_stride, int n_rows, int rq,
-                    const void *out, int B, int H, int Q) {
+                    const void *out, int B, int H, int Q, const void *query_start_loc,
+                    int n_tokens) {
   if (B < 0 || H < 1 || Q < 1 || Q > KDA_MAX_WINDOW || rq < Q || rq > KDA_MAX_WINDOW)
     return KDA_ERR_ARG;
-  if (B == 0) return kNothingToDo;  // zero tokens: empty buffers may be NULL
+  if (B == 0) return kNothingToDo;  // no requests: empty buffers may be NULL
+  // the activations hold n_tokens rows: B*Q without query_start_loc, at most
+  // B*Q with it (the stock wrapper's activation-capacity check)
+  if (n_tokens < 0 || (long long)n_tokens > (long long)B * Q) return KDA_ERR_ARG;
+  if (query_start_loc == nullptr && (long long)n_tokens != (long long)B * Q) return KDA_ERR_ARG;
+  if (n_tokens == 0) return kNothingToDo;  // zero tokens
   if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !state_pool || !state_slots ||
       !corr || !key_gate || !out)
     return KDA_ERR_ARG;
@@ -100,6 +129,7 @@ kda::StepParams make_params(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16
                             const kda_bf16 *raw_g, const kda_bf16 *raw_beta, const float *A_log,
                             const float *dt_bias, float lower_bound, float q_scale, void *state,
                             int64_t slot_stride, int n_slots, const int32_t *state_slots,
+                            const int32_t *query_start_loc, int n_tokens,
                             const int32_t *record_rows, const int32_t *pending, float *corr,
                             kda_bf16 *key_gate, int64_t corr_row_stride, int64_t kg_row_stride,
                             int n_rows, int rq, const int32_t *boundary_slots,
@@ -119,6 +149,8 @@ kda::StepParams make_params(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16
   p.slot_stride = slot_stride;
   p.n_slots = n_slots;
   p.state_slots = state_slots;
+  p.qsl = query_start_loc;
+  p.n_tokens = n_tokens;
   p.record_rows = record_rows;
   p.pending = pending;
   p.bnd_slots = boundary_slots;
@@ -141,7 +173,7 @@ kda::StepParams make_params(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16
 
 extern "C" {
 
-int kda_abi_version(void) { return 1; }
+int kda_abi_version(void) { return 2; }
 
 const char *kda_error_string(int status) {
   switch (status) {
@@ -159,21 +191,22 @@ int kda_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kd
                const kda_bf16 *raw_beta, const float *A_log, const float *dt_bias,
                float lower_bound, float q_scale, const void *state_pool, int state_dtype,
                int64_t slot_stride, int n_slots, const int32_t *state_slots,
-               const int32_t *record_rows, float *corr, kda_bf16 *key_gate,
-               int64_t corr_row_stride, int64_t kg_row_stride, int n_rows, int rq,
-               kda_bf16 *out, int B, int H, int Q, int null_slot, int32_t *status,
-               void *stream) {
+               const int32_t *query_start_loc, int n_tokens, const int32_t *record_rows,
+               float *corr, kda_bf16 *key_gate, int64_t corr_row_stride,
+               int64_t kg_row_stride, int n_rows, int rq, kda_bf16 *out, int B, int H, int Q,
+               int null_slot, int32_t *status, void *stream) {
   if (state_dtype != KDA_STATE_F32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_UNSUPPORTED;
   if (!gate_bound_ok(lower_bound)) return KDA_ERR_UNSUPPORTED;
   const int sb = state_dtype == KDA_STATE_F32 ? 4 : 2;
   int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, sb,
                            slot_stride, n_slots, state_slots, corr, key_gate, corr_row_stride,
-                           kg_row_stride, n_rows, rq, out, B, H, Q);
+                           kg_row_stride, n_rows, rq, out, B, H, Q, query_start_loc, n_tokens);
   if (rc == kNothingToDo) return KDA_OK;
   if (rc != KDA_OK) return rc;
   const kda::StepParams p = make_params(
       q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound, q_scale,
-      const_cast<void *>(state_pool), slot_stride, n_slots, state_slots, record_rows, nullptr,
+      const_cast<void *>(state_pool), slot_stride, n_slots, state_slots, query_start_loc,
+      n_tokens, record_rows, nullptr,
       corr, key_gate, corr_row_stride, kg_row_stride, n_rows, rq, nullptr, nullptr, out, B, H,
       null_slot, status);
   return kda::launch_step(p, B * H, Q, state_dtype == KDA_STATE_F32 ? 0 : 1, 1,
@@ -184,6 +217,7 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                       const kda_bf16 *raw_g, const kda_bf16 *raw_beta, const float *A_log,
                       const float *dt_bias, float lower_bound, float q_scale, float *state_pool,
                       int64_t slot_stride, int n_slots, const int32_t *state_slots,
+                      const int32_t *query_start_loc, int n_tokens,
                       const int32_t *record_rows, const int32_t *pending, float *corr,
                       kda_bf16 *key_gate, int64_t corr_row_stride, int64_t kg_row_stride,
                       int n_rows, int rq, const int32_t *boundary_slots,
@@ -192,7 +226,7 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   if (!gate_bound_ok(lower_bound)) return KDA_ERR_UNSUPPORTED;
   int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, 4, slot_stride,
                            n_slots, state_slots, corr, key_gate, corr_row_stride, kg_row_stride,
-                           n_rows, rq, out, B, H, Q);
+                           n_rows, rq, out, B, H, Q, query_start_loc, n_tokens);
   if (split != 0 && split != 1 && split != 2 && split != 4) return KDA_ERR_ARG;
   if (rc == kNothingToDo) return KDA_OK;
   if (rc != KDA_OK) return rc;
@@ -212,8 +246,9 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   if (split > 1 && items > 65535) split = 1;
   const kda::StepParams p = make_params(
       q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound, q_scale, state_pool, slot_stride,
-      n_slots, state_slots, record_rows, pending, corr, key_gate, corr_row_stride, kg_row_stride,
-      n_rows, rq, boundary_slots, boundary_lens, out, B, H, null_slot, status);
+      n_slots, state_slots, query_start_loc, n_tokens, record_rows, pending, corr, key_gate,
+      corr_row_stride, kg_row_stride, n_rows, rq, boundary_slots, boundary_lens, out, B, H,
+      null_slot, status);
   return kda::launch_step(p, items, Q, boundary_slots ? 3 : 2, split,
                           static_cast<cudaStream_t>(stream));
 }

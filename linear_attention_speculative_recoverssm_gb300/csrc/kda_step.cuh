@@ -23,6 +23,10 @@ struct StepParams {
   long long slot_stride;  // elements per slot
   int n_slots;
   const int32_t *state_slots, *record_rows, *pending;
+  // request b's window: tokens qsl[b] .. qsl[b + 1] - 1 of the n_tokens
+  // activation rows (qsl == nullptr: tokens b*Q .. b*Q + Q - 1)
+  const int32_t *qsl;
+  int n_tokens;
   const int32_t *bnd_slots, *bnd_lens;
   float *corr;
   uint16_t *kg;
@@ -48,6 +52,8 @@ struct Red {
 
 struct ItemMeta {
   int b, h;
+  int tok0;   // first token of the window
+  int qb;     // window length, 0 .. Q
   int slot;   // < 0: inert
   int rec;    // < 0: no records
   int n;      // pending tokens to replay
@@ -55,8 +61,14 @@ struct ItemMeta {
   int m;      // boundary length (min(m, n))
 };
 
+// A request's window from query_start_loc: valid when it lies inside the
+// activations and holds at most Q tokens.
+__device__ __forceinline__ bool window_ok(const StepParams &p, int q0, int q1, int Q) {
+  return q0 >= 0 && q1 >= q0 && q1 <= p.n_tokens && q1 - q0 <= Q;
+}
+
 template <bool REPLAY, bool BOUNDARY>
-__device__ __forceinline__ ItemMeta item_meta(const StepParams &p, int item,
+__device__ __forceinline__ ItemMeta item_meta(const StepParams &p, int item, int Q,
                                               bool report_errors) {
   ItemMeta it;
   it.b = item / p.H;
@@ -67,6 +79,20 @@ __device__ __forceinline__ ItemMeta item_meta(const StepParams &p, int item,
     slot = -1;
   }
   it.slot = slot > p.null_slot ? slot : -1;
+  it.tok0 = it.b * Q;
+  it.qb = Q;
+  if (p.qsl != nullptr) {
+    const int q0 = p.qsl[it.b], q1 = p.qsl[it.b + 1];
+    if (window_ok(p, q0, q1, Q)) {
+      it.tok0 = q0;
+      it.qb = q1 - q0;
+    } else {  // nothing of the request is read or written
+      if (report_errors) report(p.status, KDA_ERR_ARG);
+      it.slot = -1;
+      it.tok0 = 0;
+      it.qb = 0;
+    }
+  }
   int rec = p.record_rows != nullptr ? p.record_rows[it.b] : it.b;
   if (rec >= p.n_rows) {
     if (report_errors && it.slot >= 0) report(p.status, KDA_ERR_ARG);

@@ -112,10 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   cluster_arrive_relaxed();  // waited before the first store into a peer
 
-  const ItemMeta it = item_meta<true, BOUNDARY>(p, item, tid == 0 && rank == 0);
-  const long long tok0 = (long long)it.b * Q;
+  const ItemMeta it = item_meta<true, BOUNDARY>(p, item, Q, tid == 0 && rank == 0);
+  const long long tok0 = it.tok0;
   if (it.slot < 0) {
-    for (int e = tid; e < Q * ROWS; e += kThreads) {
+    for (int e = tid; e < it.qb * ROWS; e += kThreads) {
       const int t = e / ROWS, r = e - t * ROWS;
       p.out[((tok0 + t) * p.H + it.h) * kDim + row0 + r] = 0;
     }
@@ -145,11 +145,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     float gam = 1.f;
 #pragma unroll
     for (int t = 0; t < Q; ++t) {
+      // tokens past the window count as zero inputs (their results are
+      // never written)
       const long long off = ((tok0 + t) * p.H + it.h) * kDim + c;
-      kbits[t] = p.k[off];
-      gbits[t] = p.g[off];
+      uint16_t qbits = 0;
+      kbits[t] = gbits[t] = 0;
+      if (t < it.qb) {
+        kbits[t] = p.k[off];
+        gbits[t] = p.g[off];
+        qbits = p.q[off];
+      }
       kk[t] = bf16_bits_to_f32(kbits[t]);
-      qq[t] = bf16_bits_to_f32(p.q[off]);
+      qq[t] = bf16_bits_to_f32(qbits);
       dd[t] = gate_decay(a, bf16_bits_to_f32(gbits[t]), dt, p.lower_bound);
       gam *= dd[t];
       sm.xk[t][c] = gam * kk[t];
@@ -231,10 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (c < ROWS) {
 #pragma unroll
       for (int t = 0; t < Q; ++t)
-        sm.vv[t][c] = bf16_bits_to_f32(p.v[voff + (long long)t * p.H * kDim]);
+        sm.vv[t][c] = t < it.qb ? bf16_bits_to_f32(p.v[voff + (long long)t * p.H * kDim]) : 0.f;
     }
     if (c < Q)
-      sm.beta[c] = sigmoidf_fast(bf16_bits_to_f32(p.beta[(tok0 + c) * p.H + it.h]));
+      sm.beta[c] =
+          c < it.qb ? sigmoidf_fast(bf16_bits_to_f32(p.beta[(tok0 + c) * p.H + it.h])) : 0.f;
   }
   __syncthreads();
 
@@ -288,8 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (long long)it.h * p.rq * (2 * kDim) + c;
 #pragma unroll
     for (int t = 0; t < Q; ++t) {
-      p.kg[kbase + t * 2 * kDim] = kbits[t];
-      p.kg[kbase + t * 2 * kDim + kDim] = gbits[t];
+      if (t < it.qb) {
+        p.kg[kbase + t * 2 * kDim] = kbits[t];
+        p.kg[kbase + t * 2 * kDim + kDim] = gbits[t];
+      }
     }
   }
   const bool ok = mbar_wait_bounded(&sm.full, 0);
@@ -387,13 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       float o = sm.dots[Q + t][r] * sm.scal[Q + t];
 #pragma unroll
       for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sm.scal[2 * Q + t * Q + s2], uu[s2], o);
-      p.out[((tok0 + t) * p.H + it.h) * kDim + row] = f32_to_bf16_bits(o);
+      if (t < it.qb) p.out[((tok0 + t) * p.H + it.h) * kDim + row] = f32_to_bf16_bits(o);
     }
     if (it.rec >= 0) {
       const long long cbase = (long long)it.rec * p.corr_row_stride +
                               (long long)it.h * p.rq * kDim + row;
 #pragma unroll
-      for (int t = 0; t < Q; ++t) p.corr[cbase + t * kDim] = uu[t];
+      for (int t = 0; t < Q; ++t)
+        if (t < it.qb) p.corr[cbase + t * kDim] = uu[t];
     }
   }
 }

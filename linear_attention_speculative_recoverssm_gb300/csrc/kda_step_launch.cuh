@@ -29,14 +29,15 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// The four token-major inputs [B*Q, H, 128] (BF16) as 3-D tensors (128, H,
-// B*Q) with a (128, 1, Q) box: one item's window rows per copy.
+// The four token-major inputs [n_tokens, H, 128] (BF16) as 3-D tensors (128,
+// H, n_tokens) with a (128, 1, Q) box: one item's window rows per copy (rows
+// past the activations arrive as zeros).
 template <int Q>
 int encode_token_maps(const StepParams &p, WsMaps &maps) {
   const auto encode = tensor_map_encoder();
   if (encode == nullptr) return KDA_ERR_CUDA;
   const uint16_t *src[4] = {p.q, p.k, p.g, p.v};
-  const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)p.H, (cuuint64_t)p.B * Q};
+  const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)p.H, (cuuint64_t)p.n_tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)p.H * kDim * 2};
   const cuuint32_t box[3] = {(cuuint32_t)kDim, 1, (cuuint32_t)Q};
   const cuuint32_t estride[3] = {1, 1, 1};
@@ -51,9 +52,9 @@ int encode_token_maps(const StepParams &p, WsMaps &maps) {
   return KDA_OK;
 }
 
-template <int Q, typename ST, bool REPLAY, bool BOUNDARY>
+template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN>
 int launch_ws(const StepParams &p, int n_items, cudaStream_t stream) {
-  auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY>;
+  auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY, VARLEN>;
   constexpr size_t smem = sizeof(WsSmem<Q, ST, BOUNDARY>);
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -104,18 +105,25 @@ int launch_cluster(const StepParams &p, int n_items, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// The persistent kernel for one variant: 0 verify (FP32 state), 1 verify
+// (BF16 state), 2 replay + verify, 3 replay + verify with boundary states.
+template <int Q, bool VARLEN>
+int launch_ws_variant(const StepParams &p, int n_items, int variant, cudaStream_t stream) {
+  switch (variant) {
+    case 0: return launch_ws<Q, float, false, false, VARLEN>(p, n_items, stream);
+    case 1: return launch_ws<Q, uint16_t, false, false, VARLEN>(p, n_items, stream);
+    case 2: return launch_ws<Q, float, true, false, VARLEN>(p, n_items, stream);
+    case 3: return launch_ws<Q, float, true, true, VARLEN>(p, n_items, stream);
+    default: return KDA_ERR_ARG;
+  }
+}
+
+// Uniform windows (split 1: the persistent kernel; 2 or 4: the cluster
+// split, which also serves windows from query_start_loc).
 template <int Q>
 int launch_step_q(const StepParams &p, int n_items, int variant, int split,
                   cudaStream_t stream) {
-  if (split == 1) {
-    switch (variant) {
-      case 0: return launch_ws<Q, float, false, false>(p, n_items, stream);
-      case 1: return launch_ws<Q, uint16_t, false, false>(p, n_items, stream);
-      case 2: return launch_ws<Q, float, true, false>(p, n_items, stream);
-      case 3: return launch_ws<Q, float, true, true>(p, n_items, stream);
-      default: return KDA_ERR_ARG;
-    }
-  }
+  if (split == 1) return launch_ws_variant<Q, false>(p, n_items, variant, stream);
   // the cluster split serves the fused FP32 replay + verify
   if (variant != 2 && variant != 3) return KDA_ERR_UNSUPPORTED;
   const bool bnd = variant == 3;

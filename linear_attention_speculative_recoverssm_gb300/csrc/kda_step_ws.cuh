@@ -98,7 +98,7 @@ struct alignas(16) WsOps {
   float rsk[Q];          // rsqrt(|k_t|^2 + eps)
   float fin_a[Q][Q];     // normalised A_ts (s < t), 0 for s >= t
   float fin_b[Q][Q];     // normalised B_ts (s <= t), 0 for s > t
-  int meta[8];  // b, h, slot, rec, n, bslot, m
+  int meta[8];  // b (tok0 with VARLEN), h, slot, rec, n, bslot, m, qb (VARLEN)
 };
 
 // Tensor maps of the four token-major BF16 inputs [B*Q, H, 128], in the
@@ -115,7 +115,7 @@ struct alignas(128) WsIn {
   uint16_t tok[4][Q][kDim];      // q, k, raw_g, v rows of this window (BF16)
   uint16_t kg[kMaxQ][2 * kDim];  // recorded key / raw gate rows (first n)
   float corr[kMaxQ][kDim];       // recorded corrections (first n)
-  int meta[8];                   // b, h, slot, rec, n, bslot, m
+  int meta[8];                   // as in WsOps
 };
 
 template <typename ST>
@@ -367,10 +367,10 @@ __device__ __forceinline__ void ws_dots(const float4 (&s)[4][4], const float *__
 // is broadcast to the row group and folded into every lane's residual (the
 // A coefficient is 0 for s >= t) and outputs (the B coefficient is 0 for
 // s > t).  Writes o_t (BF16) and, with a record row, u_t (FP32).
-template <int Q, int NG, typename Ops>
+template <int Q, int NG, bool VARLEN, typename Ops>
 __device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
-                                         const StepParams &p, long long tok0, int h, int rec,
-                                         int R0, int c, int lane) {
+                                         const StepParams &p, long long tok0, int qb, int h,
+                                         int rec, int R0, int c, int lane) {
   const int cw = c < Q ? c : Q - 1;  // lanes without a w role compute unused values
   const uint2 vb = *reinterpret_cast<const uint2 *>(&op.vv[cw][R0]);
   const float4 v4 = make_float4(__uint_as_float(vb.x << 16), __uint_as_float(vb.x & 0xffff0000u),
@@ -410,19 +410,22 @@ __device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
   }
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
-    if (hy[g]) {
+    if (hy[g] && (!VARLEN || ty[g] < qb)) {
       const uint2 o2 = make_uint2(pack_bf16x2(oacc[g][0], oacc[g][1]),
                                   pack_bf16x2(oacc[g][2], oacc[g][3]));
       *reinterpret_cast<uint2 *>(p.out + ((tok0 + ty[g]) * p.H + h) * kDim + R0) = o2;
     }
   }
-  if (c < Q && rec >= 0) {
+  if ((VARLEN ? c < qb : c < Q) && rec >= 0) {
     const long long cbase = (long long)rec * p.corr_row_stride + ((long long)h * p.rq + c) * kDim;
     stg4(p.corr + cbase + R0, make_float4(bt * res[0], bt * res[1], bt * res[2], bt * res[3]));
   }
 }
 
-template <int Q, typename ST, bool REPLAY, bool BOUNDARY>
+// VARLEN: windows from query_start_loc (p.qsl, non-null), each of q_b <= Q
+// tokens; otherwise request b's window is tokens b*Q .. b*Q + Q - 1.  The
+// meta words carry b (uniform) or the window's first token and length.
+template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN>
 __global__ void __launch_bounds__(kWsThreads, 1)
     kda_step_ws(const StepParams p, const __grid_constant__ WsMaps maps, int n_items) {
   using Smem = WsSmem<Q, ST, BOUNDARY>;
@@ -490,17 +493,18 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // Raw per-request values of an item (no branch on them, so the loads stay
     // in flight) and its pending count, loaded a step later from its row.
     struct Raw {
-      int slot = -1, rec = -1, bslot = -1, blen = 0, pend = 0;
+      int slot = -1, rec = -1, bslot = -1, blen = 0, pend = 0, q0 = 0, q1 = 0;
     };
     Raw r2, r3;  // items j + 2 (row and pending loaded) and j + 3 (row loaded)
     auto publish_next = [&](const ItemMeta &m) {  // item j + 1, read by thread 0
-      sm.next_meta[0] = m.b;
+      sm.next_meta[0] = VARLEN ? m.tok0 : m.b;
       sm.next_meta[1] = m.h;
       sm.next_meta[2] = m.slot;
       sm.next_meta[3] = m.rec;
       sm.next_meta[4] = m.n;
       sm.next_meta[5] = m.bslot;
       sm.next_meta[6] = m.m;
+      if constexpr (VARLEN) sm.next_meta[7] = m.qb;
     };
     auto load_raw = [&](int i, Raw &r) {
       const int b = (first + i * stride) / p.H;
@@ -513,6 +517,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         r.blen = p.bnd_lens[b];
       }
       r.pend = 0;
+      if constexpr (VARLEN) {
+        r.q0 = p.qsl[b];
+        r.q1 = p.qsl[b + 1];
+      }
     };
     auto load_pending = [&](Raw &r) {
       r.pend = 0;
@@ -531,6 +539,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         slot = -1;
       }
       it.slot = slot > p.null_slot ? slot : -1;
+      it.tok0 = it.b * Q;
+      it.qb = Q;
+      if constexpr (VARLEN) {
+        if (window_ok(p, r.q0, r.q1, Q)) {
+          it.tok0 = r.q0;
+          it.qb = r.q1 - r.q0;
+        } else {  // nothing of the request is read or written
+          report(p.status, KDA_ERR_ARG);
+          it.slot = -1;
+          it.tok0 = 0;
+          it.qb = 0;
+        }
+      }
       int rec = rs_rec;
       if (rec >= p.n_rows) {
         if (it.slot >= 0) report(p.status, KDA_ERR_ARG);
@@ -556,13 +577,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     auto request_inputs = [&](int i) {
       if (c != 0) return;
       ItemMeta m;
-      m.b = sm.next_meta[0];
+      m.b = m.tok0 = sm.next_meta[0];
       m.h = sm.next_meta[1];
       m.slot = sm.next_meta[2];
       m.rec = sm.next_meta[3];
       m.n = sm.next_meta[4];
       m.bslot = sm.next_meta[5];
       m.m = sm.next_meta[6];
+      m.qb = VARLEN ? sm.next_meta[7] : Q;
       WsIn<Q> &in = sm.in[i & 1];
       in.meta[0] = m.b;
       in.meta[1] = m.h;
@@ -571,6 +593,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       in.meta[4] = m.n;
       in.meta[5] = m.bslot;
       in.meta[6] = m.m;
+      if constexpr (VARLEN) in.meta[7] = m.qb;
       uint64_t *bar = &sm.infull[i & 1];
       if (m.slot < 0) {
         mbar_arrive(bar);
@@ -581,7 +604,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const uint32_t rec_bytes = (uint32_t)nrec * kDim * 4u;  // per record tensor
       mbar_arrive_expect_tx(bar, kTokBytes + 2u * rec_bytes);
 #pragma unroll
-      for (int x = 0; x < 4; ++x) tma_load_3d(&in.tok[x][0][0], &maps.tok[x], 0, m.h, m.b * Q, bar);
+      // (rows past the window or the activations arrive as zeros or as other
+      // requests' tokens; nothing computed from them is written)
+      for (int x = 0; x < 4; ++x)
+        tma_load_3d(&in.tok[x][0][0], &maps.tok[x], 0, m.h, VARLEN ? m.tok0 : m.b * Q, bar);
       if (nrec > 0) {
         bulk_g2s(&in.kg[0][0],
                  p.kg + (long long)m.rec * p.kg_row_stride + (long long)m.h * p.rq * (2 * kDim),
@@ -595,12 +621,20 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // (kept raw: converting here would wait for the loads at once)
     float dt_n = 0.f, alog_n = 0.f;
     uint32_t beta_n = 0;
+    // The window of item i is read from next_meta, which holds item i's
+    // resolved chain whenever this runs.
     auto load_small = [&](int i) {
       const int b = (first + i * stride) / p.H;
       const int h = (first + i * stride) - b * p.H;
       dt_n = p.dt_bias[h * kDim + c];
       alog_n = p.A_log[h];
-      if (c < Q) beta_n = p.beta[((long long)b * Q + c) * p.H + h];
+      if constexpr (VARLEN) {
+        const long long tok = sm.next_meta[0];
+        beta_n = 0;
+        if (c < sm.next_meta[7]) beta_n = p.beta[(tok + c) * p.H + h];
+      } else {
+        if (c < Q) beta_n = p.beta[((long long)b * Q + c) * p.H + h];
+      }
     };
 
     int requested = 0;  // items whose inputs were requested (warp 0)
@@ -615,6 +649,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       named_bar(kBarPro, 128);  // next_meta published
       request_inputs(0);
+      if constexpr (VARLEN) load_small(0);  // item 0's window is in next_meta
       named_bar(kBarPro, 128);  // next_meta read by every thread
       if (c == 0 && count > 1) {
         Raw r1;
@@ -628,7 +663,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (count > 3) load_raw(3, r3);
       }
       named_bar(kBarPro, 128);  // next_meta published
-      load_small(0);
+      if constexpr (!VARLEN) load_small(0);
     }
 
     for (int j = 0; j < count; ++j) {
@@ -656,6 +691,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       it.n = in.meta[4];
       it.bslot = in.meta[5];
       it.m = in.meta[6];
+      it.qb = VARLEN ? in.meta[7] : Q;
       const bool live = it.slot >= 0;
 
       // (inputs are re-read from the stage where needed: fewer live registers)
@@ -722,6 +758,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         op.meta[4] = it.n;
         op.meta[5] = it.bslot;
         op.meta[6] = it.m;
+        if constexpr (VARLEN) op.meta[7] = it.qb;
       }
       if (live) {
 #pragma unroll
@@ -822,8 +859,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                                   (long long)it.h * p.rq * (2 * kDim) + c;
 #pragma unroll
           for (int t = 0; t < Q; ++t) {
-            p.kg[kbase + t * 2 * kDim] = in.tok[1][t][c];
-            p.kg[kbase + t * 2 * kDim + kDim] = in.tok[2][t][c];
+            if (!VARLEN || t < it.qb) {
+              p.kg[kbase + t * 2 * kDim] = in.tok[1][t][c];
+              p.kg[kbase + t * 2 * kDim + kDim] = in.tok[2][t][c];
+            }
           }
         }
       }
@@ -888,14 +927,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       break;
     }
     const Ops &op = sm.ops[j % kWsOpsBufs];
-    const int b = op.meta[0], h = op.meta[1], slot = op.meta[2], rec = op.meta[3];
+    const int h = op.meta[1], slot = op.meta[2], rec = op.meta[3];
     const int n = op.meta[4], bslot = op.meta[5], m = op.meta[6];
-    const long long tok0 = (long long)b * Q;
+    const int qb = VARLEN ? op.meta[7] : Q;
+    const long long tok0 = VARLEN ? (long long)op.meta[0] : (long long)op.meta[0] * Q;
 
     if (slot < 0) {
       // inert item: zero outputs (lane c: token c of its 4 rows); the
       // stage's phase was completed when the item was issued
-      if (c < Q)
+      if (c < qb)
         *reinterpret_cast<uint2 *>(p.out + ((tok0 + c) * p.H + h) * kDim + R0) = make_uint2(0, 0);
       stage_read(j, next_slot);
       warp_arrive(&sm.opempty[j % kWsOpsBufs]);
@@ -941,7 +981,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     ws_dots<NG>(st, &op.x[0][0], c, d);
 
     // ---------------- row solve, outputs, corrections --------------------
-    ws_solve<Q, NG>(d, op, p, tok0, h, rec, R0, c, lane);
+    ws_solve<Q, NG, VARLEN>(d, op, p, tok0, qb, h, rec, R0, c, lane);
     warp_arrive(&sm.opempty[j % kWsOpsBufs]);
   }
   if (failed && lane == 0) report(p.status, KDA_ERR_TIMEOUT);

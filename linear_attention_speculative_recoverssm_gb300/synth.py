@@ -134,6 +134,36 @@ def replay_verify_case(*, B, H, Q, slots, seed, RQ=None, rows=None, K=128,
     return case
 
 
+WINDOW_KEYS = ("q", "k", "v", "raw_g", "raw_beta")
+
+
+def pack_windows(case, q_lens):
+    """The first q_lens[b] tokens of each request's window, packed one
+    request after another, and the query_start_loc [B + 1] (int32) that
+    indexes them: request b's tokens are rows query_start_loc[b] ..
+    query_start_loc[b + 1] - 1."""
+    B, Q = case["B"], case["Q"]
+    qsl = np.zeros(B + 1, dtype=np.int32)
+    qsl[1:] = np.cumsum(q_lens)
+    idx = np.concatenate([np.arange(b * Q, b * Q + int(q_lens[b]), dtype=np.int64)
+                          for b in range(B)])
+    packed = {key: np.ascontiguousarray(case[key][idx]) for key in WINDOW_KEYS}
+    packed["query_start_loc"] = qsl
+    return packed
+
+
+def varlen_case(*, B, H, Q, slots, seed, q_min=0, **kw):
+    """A replay + verify step whose requests verify windows of different
+    lengths q_b ~ U{q_min..Q} (``q_lens`` [B]), packed as query_start_loc
+    describes; everything else as ``replay_verify_case``."""
+    case = replay_verify_case(B=B, H=H, Q=Q, slots=slots, seed=seed, **kw)
+    rng = np.random.default_rng(seed + 104729)
+    q_lens = rng.integers(q_min, Q + 1, size=B).astype(np.int32)
+    case.update(pack_windows(case, q_lens))
+    case["q_lens"] = q_lens
+    return case
+
+
 def decode_loop_case(*, B, H, Q, slots, steps, seed, windows=None, K=128, V=128,
                      padding_frac=0.0, accept_min=0, eager_frac=0.0):
     """Operands of a multi-step speculative decode of one layer.
@@ -253,6 +283,10 @@ WORKLOADS = {
     "replay-verify-f32-h64-b512-q8": dict(kind="replay_verify", B=512, H=64,
                                           Q=8, slots=1024, seed=3,
                                           padding_frac=0.05),
+    # the large-batch step with windows of 1..8 tokens per request
+    "replay-verify-varlen-f32-h64-b512-q8": dict(kind="varlen", B=512, H=64, Q=8,
+                                                 slots=1024, seed=8, q_min=1,
+                                                 padding_frac=0.05),
     # eight decode steps of the large-batch shape (a flush after every
     # eighth, so the first step of each cycle is the stock verify); sampling
     # accepts 1..8 tokens per request and step; two distinct windows
@@ -276,6 +310,8 @@ def make(name, **overrides):
         return commit_case(**spec)
     if kind == "decode_loop":
         return decode_loop_case(**spec)
+    if kind == "varlen":
+        return varlen_case(**spec)
     return replay_verify_case(**spec)
 
 

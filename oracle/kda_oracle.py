@@ -26,7 +26,9 @@ What it computes, and where the pages define it (page titles as printed):
   the checkpoint (page "...recoverssm.kernels", ``kda_recoverssm_verify``).
   Records of the new window are written to the request's record row (module
   docstring step 3).  Inert rows (slot <= null) output zeros only (fused
-  kernel, first branch).
+  kernel, first branch).  Windows of different lengths are given by
+  ``query_start_loc`` as the stock verify takes them (page
+  "...recoverssm.kernels", ``kda_recoverssm_verify``).
 * ``commit`` -- the standalone commit: the replay alone, source -> destination,
   plus the align-mode boundary state S_min(m, n) (page
   "...recoverssm.cutedsl.commit", module docstring and ``KdaCommit.kernel``).
@@ -220,7 +222,7 @@ def replay_verify(*, q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound,
                   q_scale, state, state_slots, record_rows, corr, key_gate,
                   out, B, H, Q, null_slot=0, pending=None,
                   boundary_slots=None, boundary_lens=None, items=None,
-                  out_f64=None):
+                  out_f64=None, query_start_loc=None):
     """The RecoverSSM step for every (request, head) item, in place.
 
     Shapes: q, k, raw_g [B*Q, H, K] and v [B*Q, H, V] (BF16 bits);
@@ -232,11 +234,27 @@ def replay_verify(*, q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound,
     gate); out [B*Q, H, V] BF16 bits.  ``items`` restricts the work to the
     listed flat item ids b*H + h.  Returns nothing; writes state (iff n > 0
     and pending given), the boundary slot (align), records and outputs.
+
+    With ``query_start_loc`` ([B + 1], the stock wrapper's argument on page
+    "...recoverssm.kernels"), the activations hold the packed windows:
+    request b's window is tokens query_start_loc[b] .. query_start_loc[b+1]
+    - 1, its length q_b <= Q; only those q_b tokens are verified, and only
+    their outputs and records are written.  A window outside the activations
+    or longer than Q leaves the request untouched.  The replay does not
+    depend on the window.
     """
     K = q.shape[-1]
     RQ = corr.shape[2]
+    n_tok = q.shape[0]
     for b, h in _items(B, H, items):
-        tok = slice(b * Q, (b + 1) * Q)
+        if query_start_loc is None:
+            t0, qb = b * Q, Q
+        else:
+            t0 = int(query_start_loc[b])
+            qb = int(query_start_loc[b + 1]) - t0
+            if t0 < 0 or qb < 0 or qb > Q or t0 + qb > n_tok:
+                continue
+        tok = slice(t0, t0 + qb)
         slot = int(state_slots[b])
         if slot <= null_slot:
             out[tok, h, :] = 0
@@ -276,9 +294,9 @@ def replay_verify(*, q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound,
         if out_f64 is not None:
             out_f64[tok, h, :] = o
         if rec >= 0:
-            corr[rec, h, :Q] = u.astype(np.float32)
-            key_gate[rec, h, :Q, :K] = k[tok, h]
-            key_gate[rec, h, :Q, K:] = raw_g[tok, h]
+            corr[rec, h, :qb] = u.astype(np.float32)
+            key_gate[rec, h, :qb, :K] = k[tok, h]
+            key_gate[rec, h, :qb, K:] = raw_g[tok, h]
 
 
 def commit(*, layers, A_log, dt_bias, sources, commit_lens, destinations,

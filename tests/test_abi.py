@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_error_strings(lib):
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == 2
     assert lib.kda_error_string(0) == b"ok"
     assert lib.kda_error_string(-2).startswith(b"pointer")
     assert lib.kda_error_string(123) == b"unknown status"
@@ -47,7 +47,8 @@ A = 0x10000  # a 16-byte aligned stand-in address: never dereferenced below
 
 def _verify_args(**over):
     args = dict(q=A, k=A, v=A, g=A, beta=A, A_log=A, dt_bias=A, lb=-5.0, qs=0.088,
-                state=A, dtype=0, slot_stride=2 * 128 * 128, n_slots=4, slots=A, rows=A,
+                state=A, dtype=0, slot_stride=2 * 128 * 128, n_slots=4, slots=A, qsl=None,
+                n_tokens=4, rows=A,
                 corr=A, kg=A, crs=2 * 2 * 128, krs=2 * 2 * 256, n_rows=2, rq=2, out=A,
                 B=2, H=2, Q=2, null=0, status=None, stream=None)
     args.update(over)
@@ -63,7 +64,10 @@ def _verify_args(**over):
     (dict(slot_stride=2 * 128 * 128 + 1), _lib.KDA_ERR_ALIGN),
     (dict(dtype=7), _lib.KDA_ERR_UNSUPPORTED),
     (dict(lb=-20.0), _lib.KDA_ERR_UNSUPPORTED), (dict(lb=float("nan")), _lib.KDA_ERR_UNSUPPORTED),
-    (dict(B=0), _lib.KDA_OK),
+    (dict(B=0, n_tokens=0), _lib.KDA_OK),
+    # the token count: B*Q without query_start_loc, at most B*Q with it
+    (dict(n_tokens=3), _lib.KDA_ERR_ARG), (dict(qsl=A, n_tokens=5), _lib.KDA_ERR_ARG),
+    (dict(qsl=A, n_tokens=-1), _lib.KDA_ERR_ARG), (dict(qsl=A, n_tokens=0), _lib.KDA_OK),
 ])
 def test_verify_host_checks(lib, over, code):
     assert lib.kda_verify(*_verify_args(**over)) == code
@@ -71,7 +75,8 @@ def test_verify_host_checks(lib, over, code):
 
 def test_replay_verify_host_checks(lib):
     base = dict(q=A, k=A, v=A, g=A, beta=A, A_log=A, dt_bias=A, lb=-5.0, qs=0.088, state=A,
-                slot_stride=2 * 128 * 128, n_slots=4, slots=A, rows=A, pending=A, corr=A,
+                slot_stride=2 * 128 * 128, n_slots=4, slots=A, qsl=None, n_tokens=4, rows=A,
+                pending=A, corr=A,
                 kg=A, crs=2 * 2 * 128, krs=2 * 2 * 256, n_rows=2, rq=2, bslots=None,
                 blens=None, out=A, B=2, H=2, Q=2, null=0, split=1, status=None, stream=None)
 
@@ -85,7 +90,10 @@ def test_replay_verify_host_checks(lib):
     assert call(rows=None) == _lib.KDA_ERR_ARG
     assert call(bslots=A) == _lib.KDA_ERR_ARG  # boundary lengths missing
     assert call(corr=A + 8) == _lib.KDA_ERR_ALIGN
-    assert call(B=0) == _lib.KDA_OK
+    assert call(B=0, n_tokens=0) == _lib.KDA_OK
+    assert call(n_tokens=5) == _lib.KDA_ERR_ARG
+    assert call(qsl=A, n_tokens=9) == _lib.KDA_ERR_ARG
+    assert call(qsl=A, n_tokens=0) == _lib.KDA_OK  # zero tokens: nothing to do
 
 
 def test_commit_and_bookkeeping_host_checks(lib):

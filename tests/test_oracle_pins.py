@@ -594,3 +594,73 @@ def test_decode_stock_full_acceptance_is_one_long_recurrence():
     for s in range(steps):
         np.testing.assert_allclose(ref_outs[s][:, 0], o[s * Q:(s + 1) * Q], rtol=1e-12,
                                    atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# windows of different lengths (query_start_loc)
+# ---------------------------------------------------------------------------
+
+def test_full_windows_through_query_start_loc_equal_the_uniform_step():
+    case = _case(padding_frac=0.2, no_record_frac=0.2)
+    B, Q = case["B"], case["Q"]
+    uni = _run(case)
+    var = _run(case, query_start_loc=np.arange(B + 1, dtype=np.int32) * Q)
+    for key in ("out", "state", "corr", "key_gate"):
+        np.testing.assert_array_equal(var[key], uni[key], err_msg=key)
+
+
+def test_short_windows_are_prefixes_of_the_full_window():
+    # The recurrence is causal: a request's first q_b outputs and corrections
+    # do not depend on its later tokens, so verifying only the packed first
+    # q_b tokens gives the full window's first q_b results; records past q_b
+    # are left as they were, and the replay does not depend on the window.
+    case = _case(B=7, H=2, Q=4, padding_frac=0.15, no_record_frac=0.15)
+    B, Q, K = case["B"], case["Q"], case["k"].shape[-1]
+    q_lens = np.array([0, 4, 1, 3, 2, 0, 4], dtype=np.int32)
+    uni = _run(case)
+    packed = synth.pack_windows(case, q_lens)
+    vcase = dict(case)
+    vcase.update(packed)
+    qsl = packed["query_start_loc"]
+    assert qsl[-1] == q_lens.sum() == vcase["q"].shape[0]
+    var = _run(vcase, query_start_loc=qsl)
+    np.testing.assert_array_equal(var["state"], uni["state"])
+    for b in range(B):
+        qb = int(q_lens[b])
+        np.testing.assert_array_equal(var["out"][qsl[b]:qsl[b + 1]],
+                                      uni["out"][b * Q:b * Q + qb], err_msg=f"request {b}")
+        rec = int(case["record_rows"][b])
+        if rec < 0:
+            continue
+        if case["state_slots"][b] > 0:
+            np.testing.assert_array_equal(var["corr"][rec, :, :qb], uni["corr"][rec, :, :qb])
+            np.testing.assert_array_equal(var["key_gate"][rec, :, :qb],
+                                          uni["key_gate"][rec, :, :qb])
+        np.testing.assert_array_equal(var["corr"][rec, :, qb:], case["corr"][rec, :, qb:])
+        np.testing.assert_array_equal(var["key_gate"][rec, :, qb:],
+                                      case["key_gate"][rec, :, qb:])
+    assert K == 8
+
+
+def test_invalid_window_leaves_the_request_untouched():
+    case = _case(B=4, H=2, Q=3)
+    case["pending"][:] = 2
+    B, Q = case["B"], case["Q"]
+    q_lens = np.array([2, 3, 1, 3], dtype=np.int32)
+    packed = synth.pack_windows(case, q_lens)
+    vcase = dict(case)
+    vcase.update(packed)
+    qsl = packed["query_start_loc"].copy()
+    qsl[1] = qsl[2] - (Q + 1)  # request 1: a window longer than Q
+    qsl[4] = vcase["q"].shape[0] + 1  # request 3: past the activations
+    var = _run(vcase, query_start_loc=qsl)
+    for b in (1, 3):
+        slot, rec = int(case["state_slots"][b]), int(case["record_rows"][b])
+        assert slot > 0 and rec >= 0
+        np.testing.assert_array_equal(var["state"][slot], case["state"][slot])
+        np.testing.assert_array_equal(var["corr"][rec], case["corr"][rec])
+        np.testing.assert_array_equal(var["key_gate"][rec], case["key_gate"][rec])
+    # the valid requests are still served (their checkpoints replayed)
+    for b in (0, 2):
+        slot = int(case["state_slots"][b])
+        assert not np.array_equal(var["state"][slot], case["state"][slot])
