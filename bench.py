@@ -466,16 +466,19 @@ def measure_rows(dev, stream, peak, cpu_seconds):
     c = synth.make(name)
     d = {n: dt(c[n]) for n in names + ("query_start_loc",)}
     out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
+    st_v = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step_varlen():
         kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"],
                           d["dt_bias"], d["state"], d["state_slots"], d["record_rows"],
                           d["pending"], d["corr"], d["key_gate"], out, Q=c["Q"],
                           lower_bound=c["lower_bound"], q_scale=c["q_scale"], split=0,
-                          query_start_loc=d["query_start_loc"], stream=stream)
+                          query_start_loc=d["query_start_loc"], status=st_v, stream=stream)
     for _ in range(5):
         step_varlen()
     ms = _event_ms(stream, step_varlen, 50)
+    if int(st_v.item()) != 0:
+        raise RuntimeError(f"variable-window step: device status {int(st_v.item())}")
     ab_v = algorithmic_bytes(c)
     rows["replay_verify_varlen"] = dict(
         workload=name, ms=ms, tok_s=ab_v["live_tokens"] / (ms / 1e3),

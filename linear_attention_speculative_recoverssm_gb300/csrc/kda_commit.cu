@@ -496,7 +496,17 @@ __global__ void __launch_bounds__(kCommitThreads, 1)
     const int n = op.meta[1], m = op.meta[2];
     const unsigned long long dst = op.dst, bnd = op.bnd;
     if (!live) {
-      stage_read(j, next_src);  // the stage's phase completed when the item was issued
+      // The stage phase of an item that is not live is an arrival without a
+      // copy, made when the item was issued, after all eight reads of the
+      // stage's previous item; waiting for it keeps this warp (up to
+      // kCmOps - 1 items ahead of the slowest) from counting its read among
+      // that previous item's, which would issue a page twice or never.
+      ok = mbar_wait_bounded(&sm.full[j % NS], (uint32_t)((j / NS) & 1));
+      if (__any_sync(0xffffffffu, !ok)) {
+        failed = true;
+        break;
+      }
+      stage_read(j, next_src);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.opempty[j % kCmOps]);
       consumed = j + 1;

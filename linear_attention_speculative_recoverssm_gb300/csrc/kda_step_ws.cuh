@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // Raw per-request values of an item (no branch on them, so the loads stay
     // in flight) and its pending count, loaded a step later from its row.
     struct Raw {
-      int slot = -1, rec = -1, bslot = -1, blen = 0, pend = 0, q0 = 0, q1 = 0;
+      int slot = -1, rec = -1, bslot = -1, blen = 0, pend = 0;
     };
     Raw r2, r3;  // items j + 2 (row and pending loaded) and j + 3 (row loaded)
     auto publish_next = [&](const ItemMeta &m) {  // item j + 1, read by thread 0
@@ -517,10 +517,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         r.blen = p.bnd_lens[b];
       }
       r.pend = 0;
-      if constexpr (VARLEN) {
-        r.q0 = p.qsl[b];
-        r.q1 = p.qsl[b + 1];
-      }
     };
     auto load_pending = [&](Raw &r) {
       r.pend = 0;
@@ -542,9 +538,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       it.tok0 = it.b * Q;
       it.qb = Q;
       if constexpr (VARLEN) {
-        if (window_ok(p, r.q0, r.q1, Q)) {
-          it.tok0 = r.q0;
-          it.qb = r.q1 - r.q0;
+        const int q0 = p.qsl[it.b], q1 = p.qsl[it.b + 1];
+        if (window_ok(p, q0, q1, Q)) {
+          it.tok0 = q0;
+          it.qb = q1 - q0;
         } else {  // nothing of the request is read or written
           report(p.status, KDA_ERR_ARG);
           it.slot = -1;
@@ -929,12 +926,29 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const Ops &op = sm.ops[j % kWsOpsBufs];
     const int h = op.meta[1], slot = op.meta[2], rec = op.meta[3];
     const int n = op.meta[4], bslot = op.meta[5], m = op.meta[6];
-    const int qb = VARLEN ? op.meta[7] : Q;
-    const long long tok0 = VARLEN ? (long long)op.meta[0] : (long long)op.meta[0] * Q;
+    // (the window is re-read from the ops buffer where it is used: fewer
+    // registers live across the passes)
+    auto window = [&](long long &tok0, int &qb) {
+      tok0 = VARLEN ? (long long)op.meta[0] : (long long)op.meta[0] * Q;
+      qb = VARLEN ? op.meta[7] : Q;
+    };
 
     if (slot < 0) {
-      // inert item: zero outputs (lane c: token c of its 4 rows); the
-      // stage's phase was completed when the item was issued
+      // inert item: zero outputs (lane c: token c of its 4 rows).  Its
+      // stage phase is an arrival without a copy, made when the item was
+      // issued, i.e. after all eight reads of the stage's previous item.
+      // Waiting for it keeps this warp from counting its read before a
+      // slower warp has counted that previous item's (a warp can run up to
+      // kWsOpsBufs - 1 items ahead), which would mix the two items' counts
+      // and issue a page twice or never.
+      ok = mbar_wait_bounded(&sm.full[j % NS], (uint32_t)((j / NS) & 1));
+      if (__any_sync(0xffffffffu, !ok)) {
+        failed = true;
+        break;
+      }
+      long long tok0;
+      int qb;
+      window(tok0, qb);
       if (c < qb)
         *reinterpret_cast<uint2 *>(p.out + ((tok0 + c) * p.H + h) * kDim + R0) = make_uint2(0, 0);
       stage_read(j, next_slot);
@@ -981,6 +995,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     ws_dots<NG>(st, &op.x[0][0], c, d);
 
     // ---------------- row solve, outputs, corrections --------------------
+    long long tok0;
+    int qb;
+    window(tok0, qb);
     ws_solve<Q, NG, VARLEN>(d, op, p, tok0, qb, h, rec, R0, c, lane);
     warp_arrive(&sm.opempty[j % kWsOpsBufs]);
   }

@@ -168,3 +168,37 @@ def test_deferred_then_flushed_equals_eager_on_gpu():
     commit(deferred_state, plan[0], plan[1], plan[2], plan[3])
     torch.cuda.synchronize()
     assert torch.equal(deferred_state, eager_state)
+
+
+def test_commit_mostly_dead_back_to_back():
+    """FP32 pools (two stages), half the requests with a null source and
+    many zero lengths, twenty launches back to back: each main warp waits
+    for a dead item's stage phase before counting its read, so the read
+    counts of two items sharing a stage never mix.  Every destination is a
+    fresh slot, so every launch writes the same pages."""
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import KDA_STATE_F32, kda_commit, layer_tables
+    c = synth.commit_case(L=2, B=96, H=16, Q=8, slots=400, seed=62, state_dtype="f32",
+                          null_frac=0.5, in_place_frac=0.0, boundary_frac=0.25)
+    orig = [{k: v.copy() for k, v in lay.items()} for lay in c["layers"]]
+    dev = "cuda"
+    states = [tu.to_torch(lay["state"], dev) for lay in c["layers"]]
+    corrs = [tu.to_torch(lay["corr"], dev) for lay in c["layers"]]
+    kgs = [tu.to_torch(lay["key_gate"], dev) for lay in c["layers"]]
+    tabs = layer_tables(states, corrs, kgs, dev)
+    t = lambda a: tu.to_torch(a, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    args = [t(c[k]) for k in ("A_log", "dt_bias", "sources", "commit_lens", "destinations")]
+    for _ in range(20):
+        kda_commit(*tabs, *args, state_dtype=KDA_STATE_F32, lower_bound=c["lower_bound"],
+                   L=c["L"], H=c["H"], B=c["B"], Q=c["Q"], n_slots=states[0].shape[0],
+                   n_rows=corrs[0].shape[0], boundaries=t(c["boundaries"]),
+                   boundary_lens=t(c["boundary_lens"]), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_layers = [{k: v.copy() for k, v in lay.items()} for lay in c["layers"]]
+    ko.commit(layers=ref_layers, A_log=c["A_log"], dt_bias=c["dt_bias"], sources=c["sources"],
+              commit_lens=c["commit_lens"], destinations=c["destinations"],
+              lower_bound=c["lower_bound"], Q=c["Q"], B=c["B"], H=c["H"],
+              boundaries=c["boundaries"], boundary_lens=c["boundary_lens"])
+    _compare_pools([tu.to_numpy(s) for s in states], ref_layers, orig)

@@ -325,3 +325,22 @@ def test_gate_bound_extremes(lower_bound):
     case = synth.replay_verify_case(B=16, H=4, Q=8, slots=24, seed=61)
     case["lower_bound"] = lower_bound
     _run_and_compare(case, split=1)
+
+
+def test_mostly_inert_back_to_back():
+    """Half the requests inert, twenty launches back to back.  Each main warp
+    waits for an inert item's stage phase before counting its read of the
+    stage, so the read counts of two items sharing a stage never mix (a
+    mixed count would issue a page twice or never: a device fault or a
+    timeout).  Nothing is pending, so every launch computes the same step."""
+    import torch
+    case = synth.replay_verify_case(B=192, H=16, Q=8, slots=200, seed=61, padding_frac=0.5)
+    case["pending"][:] = 0
+    before = tu.copy_case(case)
+    ref = tu.copy_case(case)
+    tu.oracle_step(ref, replay=True)
+    d = tu.device_case(case)
+    for _ in range(20):
+        tu.gpu_step(case, d, replay=True, split=1)
+    torch.cuda.synchronize()
+    tu.compare_step(ref, d, before)

@@ -169,3 +169,21 @@ def test_varlen_full_size_sampled():
                 tu.assert_corr_close(tu.to_numpy(d["corr"][r, h, :qb]), case["corr"][r, h, :qb])
                 np.testing.assert_array_equal(tu.to_numpy(d["key_gate"][r, h, :qb]),
                                               case["key_gate"][r, h, :qb])
+
+
+def test_varlen_mostly_inert_back_to_back():
+    """Windows from query_start_loc, half the requests inert, twenty launches
+    back to back (nothing pending: every launch computes the same step)."""
+    import torch
+    case = synth.varlen_case(B=192, H=16, Q=8, slots=200, seed=63, padding_frac=0.5)
+    case["pending"][:] = 0
+    qsl = case["query_start_loc"]
+    before = tu.copy_case(case)
+    ref = tu.copy_case(case)
+    _oracle(ref, qsl, True)
+    d = tu.device_case(case)
+    dq = tu.to_torch(qsl, "cuda")
+    for _ in range(20):
+        _gpu(case, d, dq, True, 1)
+    torch.cuda.synchronize()
+    _compare(ref, d, before, qsl)
