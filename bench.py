@@ -104,18 +104,18 @@ PROFILED = {
     "step": dict(
         sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
                  "kda_step_q8.cu"),
-        sha256="cd3fdf1792a091ed3caa9b60ed40e06f33cc42d20a185ba7db096d56313f548c",
+        sha256="83618a216df65d8ecfd744b51e7f8df3fa3aa32ba1615d0799cfe394cb848082",
         workload=WORKLOAD,
-        bytes_per_launch=(608.2 + 464.3) * 1e6 * 31104 / 7808,
+        bytes_per_launch=(608.2 + 464.1) * 1e6 * 31104 / 7808,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
-            "replay-verify-f32-h64-b128-q8 (608.2 + 464.3 MB, 7808 live items), scaled by "
+            "replay-verify-f32-h64-b128-q8 (608.2 + 464.1 MB, 7808 live items), scaled by "
             "live items to this workload's 31104"),
     # one kda_commit_ws launch of the standalone-commit workload itself
     "commit": dict(
         sources=("kda_commit.cu", "kda_device.cuh"),
-        sha256="8040a2430119aa7890c25ff2f24dcb67a01bb6657a4bb6d1d1c84f98cd4fa7d9",
+        sha256="6a303dbb34b5c4ce6e98b74c4aeeddeb72b140f63249e592ff8443683000fdb7",
         workload="commit-bf16-l4-h32-b64-q4-align",
-        bytes_per_launch=(194.7 + 167.2) * 1e6,
+        bytes_per_launch=(194.8 + 167.1) * 1e6,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_commit_ws launch of "
             "this workload"),
 }
@@ -356,186 +356,197 @@ def _event_ms(stream, fn, iters):
     return e0.elapsed_time(e1) / iters
 
 
-def measure_rows(dev, stream, peak, cpu_seconds):
+ROW_GROUPS = ("commit", "mid_batch", "varlen", "latency", "bookkeeping", "decode_loop")
+
+
+def measure_rows(dev, stream, peak, cpu_seconds, only=None):
     """Timings of the step's other rows (CUDA events on the launching stream;
     every pool below is larger than L2 except the latency sweep's, which is a
-    latency measurement by design)."""
+    latency measurement by design).  ``only``: the row groups to run (all
+    when None)."""
+    want = lambda group: only is None or group in only
     import torch
     from linear_attention_speculative_recoverssm_gb300 import (KDA_STATE_BF16, kda_commit,
                                                                kda_defer_commit, kda_flush_plan,
                                                                kda_replay_verify, layer_tables,
                                                                synth)
     rows = {}
+    names = ("q", "k", "v", "raw_g", "raw_beta", "A_log", "dt_bias", "state", "state_slots",
+             "record_rows", "pending", "corr", "key_gate")
 
     def dt(a):
         return (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
                 else torch.from_numpy(a)).to(dev)
 
-    # standalone commit, BF16 pools, 4 layers
-    name = "commit-bf16-l4-h32-b64-q4-align"
-    c = synth.make(name)
-    states = [dt(lay["state"]) for lay in c["layers"]]
-    corrs = [dt(lay["corr"]) for lay in c["layers"]]
-    kgs = [dt(lay["key_gate"]) for lay in c["layers"]]
-    tabs = layer_tables(states, corrs, kgs, dev)
-    ct = {k: dt(c[k]) for k in ("A_log", "dt_bias", "sources", "commit_lens", "destinations",
-                                "boundaries", "boundary_lens")}
+    if want('commit'):
+        # standalone commit, BF16 pools, 4 layers
+        name = "commit-bf16-l4-h32-b64-q4-align"
+        c = synth.make(name)
+        states = [dt(lay["state"]) for lay in c["layers"]]
+        corrs = [dt(lay["corr"]) for lay in c["layers"]]
+        kgs = [dt(lay["key_gate"]) for lay in c["layers"]]
+        tabs = layer_tables(states, corrs, kgs, dev)
+        ct = {k: dt(c[k]) for k in ("A_log", "dt_bias", "sources", "commit_lens", "destinations",
+                                    "boundaries", "boundary_lens")}
 
-    def commit():
-        kda_commit(*tabs, ct["A_log"], ct["dt_bias"], ct["sources"], ct["commit_lens"],
-                   ct["destinations"], state_dtype=KDA_STATE_BF16, lower_bound=c["lower_bound"],
-                   L=c["L"], H=c["H"], B=c["B"], Q=c["Q"], n_slots=states[0].shape[0],
-                   n_rows=corrs[0].shape[0], boundaries=ct["boundaries"],
-                   boundary_lens=ct["boundary_lens"], stream=stream)
-    for _ in range(5):
-        commit()
-    ms = _event_ms(stream, commit, 50)
-    nbytes = commit_algorithmic_bytes(c)
-    row = dict(workload=name, ms=ms, bytes_per_launch=nbytes,
-               roofline=dict(bound="hbm", achieved=nbytes / ms / 1e6, peak=peak, unit="GB/s",
-                             frac=nbytes / ms / 1e6 / peak,
-                             traffic=profiled_traffic("commit", name)))
-    if cpu_seconds > 0:
-        from oracle import kda_oracle as ko
-        L, B, H = c["L"], c["B"], c["H"]
-        items = np.random.default_rng(0).permutation(L * B * H)
-        ref = [{k: v.copy() for k, v in lay.items()} for lay in c["layers"]]
-        t0, done = time.perf_counter(), 0
-        while done < len(items) and time.perf_counter() - t0 < cpu_seconds:
-            ko.commit(layers=ref, A_log=c["A_log"], dt_bias=c["dt_bias"], sources=c["sources"],
-                      commit_lens=c["commit_lens"], destinations=c["destinations"],
-                      lower_bound=c["lower_bound"], Q=c["Q"], B=B, H=H,
-                      boundaries=c["boundaries"], boundary_lens=c["boundary_lens"],
-                      items=items[done:done + 64])
-            done += len(items[done:done + 64])
-        secs = time.perf_counter() - t0
-        row["cpu_baseline"] = dict(ms=1e3 * secs * len(items) / done, cores=1, kind="oracle",
-                                   sample=f"{done} of {len(items)} (layer, request, head) items, "
-                                          f"{secs:.1f} s on one core, scaled to the launch")
-    rows["commit"] = row
-    del states, corrs, kgs, tabs
+        def commit():
+            kda_commit(*tabs, ct["A_log"], ct["dt_bias"], ct["sources"], ct["commit_lens"],
+                       ct["destinations"], state_dtype=KDA_STATE_BF16, lower_bound=c["lower_bound"],
+                       L=c["L"], H=c["H"], B=c["B"], Q=c["Q"], n_slots=states[0].shape[0],
+                       n_rows=corrs[0].shape[0], boundaries=ct["boundaries"],
+                       boundary_lens=ct["boundary_lens"], stream=stream)
+        for _ in range(5):
+            commit()
+        ms = _event_ms(stream, commit, 50)
+        nbytes = commit_algorithmic_bytes(c)
+        row = dict(workload=name, ms=ms, bytes_per_launch=nbytes,
+                   roofline=dict(bound="hbm", achieved=nbytes / ms / 1e6, peak=peak, unit="GB/s",
+                                 frac=nbytes / ms / 1e6 / peak,
+                                 traffic=profiled_traffic("commit", name)))
+        if cpu_seconds > 0:
+            from oracle import kda_oracle as ko
+            L, B, H = c["L"], c["B"], c["H"]
+            items = np.random.default_rng(0).permutation(L * B * H)
+            ref = [{k: v.copy() for k, v in lay.items()} for lay in c["layers"]]
+            t0, done = time.perf_counter(), 0
+            while done < len(items) and time.perf_counter() - t0 < cpu_seconds:
+                ko.commit(layers=ref, A_log=c["A_log"], dt_bias=c["dt_bias"], sources=c["sources"],
+                          commit_lens=c["commit_lens"], destinations=c["destinations"],
+                          lower_bound=c["lower_bound"], Q=c["Q"], B=B, H=H,
+                          boundaries=c["boundaries"], boundary_lens=c["boundary_lens"],
+                          items=items[done:done + 64])
+                done += len(items[done:done + 64])
+            secs = time.perf_counter() - t0
+            row["cpu_baseline"] = dict(ms=1e3 * secs * len(items) / done, cores=1, kind="oracle",
+                                       sample=f"{done} of {len(items)} (layer, request, head) items, "
+                                              f"{secs:.1f} s on one core, scaled to the launch")
+        rows["commit"] = row
+        del states, corrs, kgs, tabs
 
-    # fused step on the mid-size batch
-    name = "replay-verify-f32-h32-b128-q4"
-    c = synth.make(name)
-    names = ("q", "k", "v", "raw_g", "raw_beta", "A_log", "dt_bias", "state", "state_slots",
-             "record_rows", "pending", "corr", "key_gate")
-    d = {n: dt(c[n]) for n in names}
-    out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
+    if want('mid_batch'):
+        # fused step on the mid-size batch
+        name = "replay-verify-f32-h32-b128-q4"
+        c = synth.make(name)
+        d = {n: dt(c[n]) for n in names}
+        out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
 
-    def step():
-        kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"],
-                          d["dt_bias"], d["state"], d["state_slots"], d["record_rows"],
-                          d["pending"], d["corr"], d["key_gate"], out, Q=c["Q"],
-                          lower_bound=c["lower_bound"], q_scale=c["q_scale"], split=0,
-                          stream=stream)
-    for _ in range(5):
-        step()
-    ms = _event_ms(stream, step, 50)
-    ab = algorithmic_bytes(c)
-    row = dict(workload=name, ms=ms, tok_s=ab["live_tokens"] / (ms / 1e3),
-               bytes_per_launch=ab["total"],
-               roofline=dict(bound="hbm", achieved=ab["total"] / ms / 1e6, peak=peak, unit="GB/s",
-                             frac=ab["total"] / ms / 1e6 / peak))
-    if cpu_seconds > 0:
-        rate, items, secs = oracle_rate(c, cpu_seconds)
-        row["cpu_baseline"] = dict(value=rate, unit="tok/s", cores=1, kind="oracle",
-                                   sample=f"{items} live items, {secs:.1f} s on one core")
-    rows["replay_verify_mid_batch"] = row
+        def step():
+            kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"],
+                              d["dt_bias"], d["state"], d["state_slots"], d["record_rows"],
+                              d["pending"], d["corr"], d["key_gate"], out, Q=c["Q"],
+                              lower_bound=c["lower_bound"], q_scale=c["q_scale"], split=0,
+                              stream=stream)
+        for _ in range(5):
+            step()
+        ms = _event_ms(stream, step, 50)
+        ab = algorithmic_bytes(c)
+        row = dict(workload=name, ms=ms, tok_s=ab["live_tokens"] / (ms / 1e3),
+                   bytes_per_launch=ab["total"],
+                   roofline=dict(bound="hbm", achieved=ab["total"] / ms / 1e6, peak=peak, unit="GB/s",
+                                 frac=ab["total"] / ms / 1e6 / peak))
+        if cpu_seconds > 0:
+            rate, items, secs = oracle_rate(c, cpu_seconds)
+            row["cpu_baseline"] = dict(value=rate, unit="tok/s", cores=1, kind="oracle",
+                                       sample=f"{items} live items, {secs:.1f} s on one core")
+        rows["replay_verify_mid_batch"] = row
 
-    # the stock verify (checkpoint read-only) on the same batch
-    from linear_attention_speculative_recoverssm_gb300 import kda_verify
+        # the stock verify (checkpoint read-only) on the same batch
+        from linear_attention_speculative_recoverssm_gb300 import kda_verify
 
-    def verify():
-        kda_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"], d["dt_bias"],
-                   d["state"], d["state_slots"], d["corr"], d["key_gate"], out, Q=c["Q"],
-                   lower_bound=c["lower_bound"], q_scale=c["q_scale"],
-                   record_rows=d["record_rows"], stream=stream)
-    for _ in range(5):
-        verify()
-    ms = _event_ms(stream, verify, 50)
-    nbytes = verify_algorithmic_bytes(c)
-    rows["verify_mid_batch"] = dict(
-        workload=name, ms=ms, tok_s=ab["live_tokens"] / (ms / 1e3), bytes_per_launch=nbytes,
-        roofline=dict(bound="hbm", achieved=nbytes / ms / 1e6, peak=peak, unit="GB/s",
-                      frac=nbytes / ms / 1e6 / peak))
-    del d, out
+        def verify():
+            kda_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"], d["dt_bias"],
+                       d["state"], d["state_slots"], d["corr"], d["key_gate"], out, Q=c["Q"],
+                       lower_bound=c["lower_bound"], q_scale=c["q_scale"],
+                       record_rows=d["record_rows"], stream=stream)
+        for _ in range(5):
+            verify()
+        ms = _event_ms(stream, verify, 50)
+        nbytes = verify_algorithmic_bytes(c)
+        rows["verify_mid_batch"] = dict(
+            workload=name, ms=ms, tok_s=ab["live_tokens"] / (ms / 1e3), bytes_per_launch=nbytes,
+            roofline=dict(bound="hbm", achieved=nbytes / ms / 1e6, peak=peak, unit="GB/s",
+                          frac=nbytes / ms / 1e6 / peak))
+        del d, out
 
-    # the large batch with windows of 1..8 tokens (query_start_loc)
-    name = "replay-verify-varlen-f32-h64-b512-q8"
-    c = synth.make(name)
-    d = {n: dt(c[n]) for n in names + ("query_start_loc",)}
-    out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
-    st_v = torch.zeros(1, dtype=torch.int32, device=dev)
+    if want('varlen'):
+        # the large batch with windows of 1..8 tokens (query_start_loc)
+        name = "replay-verify-varlen-f32-h64-b512-q8"
+        c = synth.make(name)
+        d = {n: dt(c[n]) for n in names + ("query_start_loc",)}
+        out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
+        st_v = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def step_varlen():
-        kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"],
-                          d["dt_bias"], d["state"], d["state_slots"], d["record_rows"],
-                          d["pending"], d["corr"], d["key_gate"], out, Q=c["Q"],
-                          lower_bound=c["lower_bound"], q_scale=c["q_scale"], split=0,
-                          query_start_loc=d["query_start_loc"], status=st_v, stream=stream)
-    for _ in range(5):
-        step_varlen()
-    ms = _event_ms(stream, step_varlen, 50)
-    if int(st_v.item()) != 0:
-        raise RuntimeError(f"variable-window step: device status {int(st_v.item())}")
-    ab_v = algorithmic_bytes(c)
-    rows["replay_verify_varlen"] = dict(
-        workload=name, ms=ms, tok_s=ab_v["live_tokens"] / (ms / 1e3),
-        mean_window=float(c["q_lens"][c["state_slots"] > c["null_slot"]].mean()),
-        bytes_per_launch=ab_v["total"],
-        roofline=dict(bound="hbm", achieved=ab_v["total"] / ms / 1e6, peak=peak, unit="GB/s",
-                      frac=ab_v["total"] / ms / 1e6 / peak))
-    del d, out, c
+        def step_varlen():
+            kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"],
+                              d["dt_bias"], d["state"], d["state_slots"], d["record_rows"],
+                              d["pending"], d["corr"], d["key_gate"], out, Q=c["Q"],
+                              lower_bound=c["lower_bound"], q_scale=c["q_scale"], split=0,
+                              query_start_loc=d["query_start_loc"], status=st_v, stream=stream)
+        for _ in range(5):
+            step_varlen()
+        ms = _event_ms(stream, step_varlen, 50)
+        if int(st_v.item()) != 0:
+            raise RuntimeError(f"variable-window step: device status {int(st_v.item())}")
+        ab_v = algorithmic_bytes(c)
+        rows["replay_verify_varlen"] = dict(
+            workload=name, ms=ms, tok_s=ab_v["live_tokens"] / (ms / 1e3),
+            mean_window=float(c["q_lens"][c["state_slots"] > c["null_slot"]].mean()),
+            bytes_per_launch=ab_v["total"],
+            roofline=dict(bound="hbm", achieved=ab_v["total"] / ms / 1e6, peak=peak, unit="GB/s",
+                          frac=ab_v["total"] / ms / 1e6 / peak))
+        del d, out, c
 
-    # small batches: per-launch device time (a CUDA graph of 20 launches)
-    lat = {}
-    for B in (1, 4, 16):
-        for Q in (1, 2, 4, 8):
-            c = synth.latency_case(B=B, Q=Q)
-            d = {n: dt(c[n]) for n in names}
-            out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
-            res = {}
-            for split in (1, 2, 4):
-                def one(split=split):
-                    kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"],
-                                      d["A_log"], d["dt_bias"], d["state"], d["state_slots"],
-                                      d["record_rows"], d["pending"], d["corr"], d["key_gate"],
-                                      out, Q=Q, lower_bound=c["lower_bound"],
-                                      q_scale=c["q_scale"], split=split,
-                                      stream=torch.cuda.current_stream())
-                for _ in range(3):
-                    one()
-                torch.cuda.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    for _ in range(20):
+    if want('latency'):
+        # small batches: per-launch device time (a CUDA graph of 20 launches)
+        lat = {}
+        for B in (1, 4, 16):
+            for Q in (1, 2, 4, 8):
+                c = synth.latency_case(B=B, Q=Q)
+                d = {n: dt(c[n]) for n in names}
+                out = torch.zeros(c["v"].shape, dtype=torch.bfloat16, device=dev)
+                res = {}
+                for split in (1, 2, 4):
+                    def one(split=split):
+                        kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"],
+                                          d["A_log"], d["dt_bias"], d["state"], d["state_slots"],
+                                          d["record_rows"], d["pending"], d["corr"], d["key_gate"],
+                                          out, Q=Q, lower_bound=c["lower_bound"],
+                                          q_scale=c["q_scale"], split=split,
+                                          stream=torch.cuda.current_stream())
+                    for _ in range(3):
                         one()
-                g.replay()
-                torch.cuda.synchronize()
-                res[f"split{split}"] = 1e3 * _event_ms(torch.cuda.current_stream(), g.replay,
-                                                       10) / 20
-            lat[f"B{B}_q{Q}"] = res
-    rows["latency_us_h32"] = lat
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        for _ in range(20):
+                            one()
+                    g.replay()
+                    torch.cuda.synchronize()
+                    res[f"split{split}"] = 1e3 * _event_ms(torch.cuda.current_stream(), g.replay,
+                                                           10) / 20
+                lat[f"B{B}_q{Q}"] = res
+        rows["latency_us_h32"] = lat
 
-    # bookkeeping (defer, then flush plan) for 512 requests
-    rng = np.random.default_rng(7)
-    B = 512
-    slots = torch.from_numpy(rng.integers(-1, 1024, B).astype(np.int32)).to(dev)
-    rrows = torch.from_numpy(rng.permutation(B).astype(np.int32)).to(dev)
-    pend = torch.zeros(B, dtype=torch.int32, device=dev)
-    lens = torch.from_numpy(rng.integers(0, 9, B).astype(np.int32)).to(dev)
-    plan = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(4)]
+    if want('bookkeeping'):
+        # bookkeeping (defer, then flush plan) for 512 requests
+        rng = np.random.default_rng(7)
+        B = 512
+        slots = torch.from_numpy(rng.integers(-1, 1024, B).astype(np.int32)).to(dev)
+        rrows = torch.from_numpy(rng.permutation(B).astype(np.int32)).to(dev)
+        pend = torch.zeros(B, dtype=torch.int32, device=dev)
+        lens = torch.from_numpy(rng.integers(0, 9, B).astype(np.int32)).to(dev)
+        plan = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(4)]
 
-    def book():
-        kda_defer_commit(slots, lens, rrows, pend, stream=stream)
-        kda_flush_plan(slots, rrows, pend, *plan, Q=8, stream=stream)
-    for _ in range(5):
-        book()
-    rows["bookkeeping_us_b512"] = 1e3 * _event_ms(stream, book, 50)
-    del slots, rrows, pend, lens, plan
+        def book():
+            kda_defer_commit(slots, lens, rrows, pend, stream=stream)
+            kda_flush_plan(slots, rrows, pend, *plan, Q=8, stream=stream)
+        for _ in range(5):
+            book()
+        rows["bookkeeping_us_b512"] = 1e3 * _event_ms(stream, book, 50)
+        del slots, rrows, pend, lens, plan
 
-    rows["decode_loop"] = measure_decode_loop(dev, dt, peak)
+    if want("decode_loop"):
+        rows["decode_loop"] = measure_decode_loop(dev, dt, peak)
     return rows
 
 
@@ -781,7 +792,8 @@ def run_ours(args):
 
     rows = None
     if rank == 0 and not args.no_rows:
-        rows = measure_rows(dev, stream, peak, 0.0 if args.no_cpu_baseline else 3.0)
+        rows = measure_rows(dev, stream, peak, 0.0 if args.no_cpu_baseline else 3.0,
+                            only=None if args.rows is None else set(args.rows.split(",")))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -824,6 +836,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the commit / mid-batch / latency / bookkeeping timings")
+    ap.add_argument("--rows", default=None,
+                    help="comma-separated row groups to run (default all): "
+                         + ", ".join(ROW_GROUPS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--traffic", type=float, default=None,
