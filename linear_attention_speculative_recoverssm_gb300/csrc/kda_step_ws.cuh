@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // Raw per-request values of an item (no branch on them, so the loads stay
     // in flight) and its pending count, loaded a step later from its row.
     struct Raw {
-      int slot = -1, rec = -1, bslot = -1, blen = 0, pend = 0;
+      int slot = -1, rec = -1, bslot = -1, blen = 0, pend = 0, q0 = 0, q1 = 0;
     };
     Raw r2, r3;  // items j + 2 (row and pending loaded) and j + 3 (row loaded)
     auto publish_next = [&](const ItemMeta &m) {  // item j + 1, read by thread 0
@@ -518,10 +518,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       r.pend = 0;
     };
-    auto load_pending = [&](Raw &r) {
+    // item i's pending count and (VARLEN) window bounds, a step after its row
+    auto load_pending = [&](int i, Raw &r) {
       r.pend = 0;
       if (REPLAY && r.rec >= 0 && r.rec < p.n_rows && r.slot > p.null_slot && r.slot < p.n_slots)
         r.pend = p.pending[r.rec];
+      if constexpr (VARLEN) {
+        const int b = (first + i * stride) / p.H;
+        r.q0 = p.qsl[b];
+        r.q1 = p.qsl[b + 1];
+      }
     };
     auto resolve = [&](int i, const Raw &r) {  // item_meta from the loaded raw values
       const int rs_slot = r.slot, rs_rec = r.rec, rs_bslot = r.bslot, rs_blen = r.blen,
@@ -538,10 +544,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       it.tok0 = it.b * Q;
       it.qb = Q;
       if constexpr (VARLEN) {
-        const int q0 = p.qsl[it.b], q1 = p.qsl[it.b + 1];
-        if (window_ok(p, q0, q1, Q)) {
-          it.tok0 = q0;
-          it.qb = q1 - q0;
+        if (window_ok(p, r.q0, r.q1, Q)) {
+          it.tok0 = r.q0;
+          it.qb = r.q1 - r.q0;
         } else {  // nothing of the request is read or written
           report(p.status, KDA_ERR_ARG);
           it.slot = -1;
@@ -641,7 +646,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (c == 0) {
         Raw r0;
         load_raw(0, r0);
-        load_pending(r0);
+        load_pending(0, r0);
         publish_next(resolve(0, r0));
       }
       named_bar(kBarPro, 128);  // next_meta published
@@ -651,11 +656,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (c == 0 && count > 1) {
         Raw r1;
         load_raw(1, r1);
-        load_pending(r1);
+        load_pending(1, r1);
         publish_next(resolve(1, r1));
         if (count > 2) {
           load_raw(2, r2);
-          load_pending(r2);
+          load_pending(2, r2);
         }
         if (count > 3) load_raw(3, r3);
       }
@@ -734,7 +739,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (c == 0 && j + 2 < count) {
         publish_next(resolve(j + 2, r2));
         r2 = r3;
-        if (j + 3 < count) load_pending(r2);
+        if (j + 3 < count) load_pending(j + 3, r2);
         if (j + 4 < count) load_raw(j + 4, r3);
       }
 
