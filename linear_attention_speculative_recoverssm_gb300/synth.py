@@ -164,6 +164,43 @@ def varlen_case(*, B, H, Q, slots, seed, q_min=0, **kw):
     return case
 
 
+def layer_case(*, B, H, Q, slots, seed, bias=True, eps=1e-6, **kw):
+    """Operands of the model layer around one step: the step's own operands
+    (``replay_verify_case``; its q, k, v, raw_g are what the layer prologue
+    produces) plus synthetic layer weights and inputs:
+
+    * x [B*Q, 3*H*128] BF16 ~ N(0, 1): q | k | v channels before the
+      convolution; conv_weight [3, 4, H*128] BF16 ~ N(0, 0.5^2) (tap 3 is
+      the current token); conv_bias [3*H*128] BF16 ~ N(0, 0.1^2) or None;
+      conv_state [slots, 3*H*128, RQ + 2] BF16 ~ N(0, 1) on the slots in use;
+    * f_a [B*Q, 128] BF16 ~ N(0, 1), f_b [H*128, 128] BF16 ~ N(0, 1/128)
+      (so the raw gates come out ~ N(0, 1));
+    * gate [B*Q, H*128] BF16 ~ N(0, 1), norm_weight [128] FP32 ~ 1 + N(0,
+      0.1^2), eps.
+    """
+    case = replay_verify_case(B=B, H=H, Q=Q, slots=slots, seed=seed, **kw)
+    rng = np.random.default_rng(seed + 15485863)
+    D = H * 128
+    T = B * Q
+    RQ = case["RQ"]
+    conv_state = np.zeros((slots, 3 * D, RQ + 2), dtype=np.uint16)
+    used = np.sort(case["state_slots"][case["state_slots"] > NULL_SLOT])
+    for s_ in used:
+        conv_state[s_] = to_bf16_bits(_normal(rng, (3 * D, RQ + 2)))
+    case.update(
+        x=to_bf16_bits(_normal(rng, (T, 3 * D))),
+        conv_weight=to_bf16_bits(_normal(rng, (3, 4, D), 0.5)),
+        conv_bias=to_bf16_bits(_normal(rng, (3 * D,), 0.1)) if bias else None,
+        conv_state=conv_state,
+        f_a=to_bf16_bits(_normal(rng, (T, 128))),
+        f_b=to_bf16_bits(_normal(rng, (D, 128), 128 ** -0.5)),
+        gate=to_bf16_bits(_normal(rng, (T, D))),
+        norm_weight=(1.0 + _normal(rng, (128,), 0.1)).astype(np.float32),
+        eps=eps,
+    )
+    return case
+
+
 def decode_loop_case(*, B, H, Q, slots, steps, seed, windows=None, K=128, V=128,
                      padding_frac=0.0, accept_min=0, eager_frac=0.0):
     """Operands of a multi-step speculative decode of one layer.
@@ -283,6 +320,10 @@ WORKLOADS = {
     "replay-verify-f32-h64-b512-q8": dict(kind="replay_verify", B=512, H=64,
                                           Q=8, slots=1024, seed=3,
                                           padding_frac=0.05),
+    # the model layer around the large-batch step (convolution, gate
+    # projection, the step, gated norm), synthetic weights
+    "layer-f32-h64-b512-q8": dict(kind="layer", B=512, H=64, Q=8, slots=1024,
+                                  seed=9, padding_frac=0.05),
     # the large-batch step with windows of 1..8 tokens per request
     "replay-verify-varlen-f32-h64-b512-q8": dict(kind="varlen", B=512, H=64, Q=8,
                                                  slots=1024, seed=8, q_min=1,
@@ -312,6 +353,8 @@ def make(name, **overrides):
         return decode_loop_case(**spec)
     if kind == "varlen":
         return varlen_case(**spec)
+    if kind == "layer":
+        return layer_case(**spec)
     return replay_verify_case(**spec)
 
 

@@ -35,6 +35,12 @@ What it computes, and where the pages define it (page titles as printed):
 * ``defer_commit`` / ``flush_plan`` -- the two bookkeeping steps, as integer
   code (page "...recoverssm.kernels", ``_defer_commit_kernel`` and
   ``_prepare_flush_plan_kernel``).
+* ``layer_prologue`` / ``layer_epilogue`` -- the model layer around the
+  step (page "...cutedsl.kda.fused", ``KdaFused.kernel``): the depthwise
+  convolution of q, k, v over the window rolled by n - 1, SiLU, the gate
+  projection f_b . f_a, the window rewritten; and the gated RMSNorm of the
+  outputs.  BF16 at the stock points (convolution / SiLU outputs, raw
+  gates, recurrence outputs, the window).
 * ``decode_stock`` -- several decode steps of one layer by the stock
   recurrence alone (verify every window from the state, then advance the
   state by the accepted tokens, ``advance_item``): the result the deferred
@@ -419,6 +425,100 @@ def decode_stock(*, windows, window_of_step, accepted, A_log, dt_bias,
             S = advance_item(S, k, v, g, beta, a, a_log, bias, lower_bound)
         finals[(b, h)] = S
     return outs, finals
+
+
+# --------------------------------------------------------------------------
+# the model layer around the step: convolution, gate projection, gated norm
+# --------------------------------------------------------------------------
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """The convolution's SiLU, z / (1 + e^-z), in FP64."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def conv_window_taps(window, n):
+    """The three history values before this window's first token.  The
+    stored window is [tap 1, tap 2, x_0 .. x_{RQ-1}] of the previous verify;
+    after n accepted tokens the history starts at n - 1 (0 when none is
+    pending) (page "...cutedsl.kda.fused", the convolution operands)."""
+    off = n - 1 if n > 0 else 0
+    return window[off:off + 3]
+
+
+def layer_prologue(*, x, conv_weight, conv_bias, conv_state, f_a, f_b,
+                   state_slots, record_rows, pending, B, H, Q, null_slot=0,
+                   items=None):
+    """The layer's prologue for every live (request, head) item (page
+    "...cutedsl.kda.fused", ``KdaFused.kernel``: convolution operands,
+    convolution and SiLU, gate projection; the convolution window written
+    last).
+
+    x [B*Q, 3*H*128] BF16 bits (q | k | v channels before the convolution);
+    conv_weight [3, 4, H*128] BF16 bits (tap i = 3 is the current token);
+    conv_bias [3*H*128] BF16 bits or None; conv_state [slots, 3*H*128, RQ+2]
+    BF16 bits, rewritten in place to [tap 2, tap 3, x_0 .. x_{Q-1}] (entries
+    past 2 + Q kept); f_a [B*Q, 128], f_b [H*128, 128] BF16 bits; pending
+    None for the stock verify (no replay).  For channel ch of part p (0 q,
+    1 k, 2 v) and token t: acc = bias + sum_i w[p, i, ch] * s[t + i] over the
+    sequence s = taps + x, then BF16(silu(acc)); raw_g[t, f] =
+    BF16(sum_j f_b[h*128 + f, j] * f_a[t, j]).  Returns q, k, v, raw_g
+    [B*Q, H, 128] BF16 bits (zero on inert items, which are skipped).
+    """
+    RQ = conv_state.shape[2] - 2
+    D = H * 128
+    q = np.zeros((B * Q, H, 128), dtype=np.uint16)
+    k = np.zeros_like(q)
+    v = np.zeros_like(q)
+    g = np.zeros_like(q)
+    outs = (q, k, v)
+    fa = bf16_to_f64(f_a)
+    fb = bf16_to_f64(f_b)
+    w = bf16_to_f64(conv_weight)
+    bias = None if conv_bias is None else bf16_to_f64(conv_bias)
+    for b, h in _items(B, H, items):
+        slot = int(state_slots[b])
+        if slot <= null_slot:
+            continue
+        rec = int(record_rows[b]) if record_rows is not None else b
+        n = 0
+        if pending is not None and rec >= 0:
+            n = min(max(int(pending[rec]), 0), RQ)
+        tok = slice(b * Q, (b + 1) * Q)
+        for part in range(3):
+            chans = part * D + h * 128 + np.arange(128)
+            window = bf16_to_f64(conv_state[slot, chans])       # [128, RQ+2]
+            taps = np.stack([conv_window_taps(window[c], n) for c in range(128)])
+            xs = bf16_to_f64(x[tok][:, chans]).T                 # [128, Q]
+            seq = np.concatenate([taps, xs], axis=1)             # [128, 3 + Q]
+            for t in range(Q):
+                acc = np.zeros(128) if bias is None else bias[chans].copy()
+                for i in range(4):
+                    acc = acc + w[part, i, h * 128:(h + 1) * 128] * seq[:, t + i]
+                outs[part][b * Q + t, h] = f64_to_bf16(silu(acc))
+            new = conv_state[slot, chans].copy()
+            new[:, 0] = f64_to_bf16(taps[:, 1])
+            new[:, 1] = f64_to_bf16(taps[:, 2])
+            new[:, 2:2 + Q] = x[tok][:, chans].T
+            conv_state[slot, chans] = new
+        proj = fb[h * 128:(h + 1) * 128] @ fa[tok].T             # [128 features, Q]
+        g[tok, h] = f64_to_bf16(proj.T)
+    return q, k, v, g
+
+
+def layer_epilogue(*, o, gate, norm_weight, eps):
+    """The gated RMSNorm of the step's outputs (page "...cutedsl.kda.fused",
+    kernel end): per (token, head), over its 128 value rows,
+    out = BF16(o * rsqrt(mean(o^2) + eps) * norm_weight * sigmoid(gate)).
+    o [T, H, 128] BF16 bits (the recurrence outputs, BF16 at the stock
+    point); gate [T, H*128] BF16 bits; norm_weight [128] FP32.  Returns
+    [T, H*128] BF16 bits."""
+    T, H, V = o.shape
+    of = bf16_to_f64(o)
+    rstd = 1.0 / np.sqrt(np.mean(of * of, axis=-1, keepdims=True) + eps)
+    gf = bf16_to_f64(gate).reshape(T, H, V)
+    res = of * rstd * norm_weight.astype(np.float64)[None, None, :] * sigmoid(gf)
+    return f64_to_bf16(res).reshape(T, H * V)
 
 
 # --------------------------------------------------------------------------

@@ -664,3 +664,139 @@ def test_invalid_window_leaves_the_request_untouched():
     for b in (0, 2):
         slot = int(case["state_slots"][b])
         assert not np.array_equal(var["state"][slot], case["state"][slot])
+
+
+# ---------------------------------------------------------------------------
+# the model layer: convolution and SiLU, gate projection, gated RMSNorm
+# ---------------------------------------------------------------------------
+
+def _layer(**kw):
+    base = dict(B=3, H=2, Q=4, slots=8, seed=71)
+    base.update(kw)
+    return synth.layer_case(**base)
+
+
+def _prologue(c, pending=True, conv_state=None):
+    state = (c["conv_state"] if conv_state is None else conv_state).copy()
+    out = ko.layer_prologue(x=c["x"], conv_weight=c["conv_weight"], conv_bias=c["conv_bias"],
+                            conv_state=state, f_a=c["f_a"], f_b=c["f_b"],
+                            state_slots=c["state_slots"], record_rows=c["record_rows"],
+                            pending=c["pending"] if pending else None, B=c["B"], H=c["H"],
+                            Q=c["Q"])
+    return out, state
+
+
+def _one_hot_taps(c, i):
+    w = np.zeros(c["conv_weight"].shape, dtype=np.float32)
+    w[:, i, :] = 1.0
+    c["conv_weight"] = _bits(w)
+    c["conv_bias"] = None
+
+
+@pytest.mark.parametrize("n", [0, 1, 3])
+def test_conv_taps_and_window_roll(n):
+    # With only tap 0 (the oldest) the output at t is SiLU of s[t], the
+    # sequence s = window[n-1 .. n+1] (from 0 when n = 0) followed by x; with
+    # only tap 3 (the current token) it is SiLU of x_t.  So the tap-0 layer
+    # on x equals the tap-3 layer on the sequence written out as inputs.
+    c = _layer()
+    c["pending"][:] = n
+    B, H, Q, D = c["B"], c["H"], c["Q"], c["H"] * 128
+    _one_hot_taps(c, 0)
+    (q0, k0, v0, _), _ = _prologue(c)
+    shifted = dict(c)
+    _one_hot_taps(shifted, 3)
+    x2 = c["x"].copy()
+    off = n - 1 if n > 0 else 0
+    for b in range(B):
+        slot = int(c["state_slots"][b])
+        if slot <= 0:
+            continue
+        window = c["conv_state"][slot]                       # [3D, RQ + 2]
+        seq = np.concatenate([window[:, off:off + 3], c["x"][b * Q:(b + 1) * Q].T], axis=1)
+        x2[b * Q:(b + 1) * Q] = seq[:, :Q].T
+    shifted["x"] = x2
+    (q3, k3, v3, _), _ = _prologue(shifted)
+    for a, b_ in ((q0, q3), (k0, k3), (v0, v3)):
+        np.testing.assert_array_equal(a, b_)
+    assert D == 256
+
+
+def test_silu_is_odd_up_to_the_identity():
+    # silu(z) - silu(-z) = z: negating x flips every current-tap output by
+    # the input itself (within the BF16 rounding of both outputs).
+    c = _layer(bias=False)
+    _one_hot_taps(c, 3)
+    (q, k, v, _), _ = _prologue(c)
+    neg = dict(c)
+    neg["x"] = c["x"] ^ np.uint16(0x8000)  # exact negation of BF16 bits
+    (qn, kn, vn, _), _ = _prologue(neg)
+    B, H, Q, D = c["B"], c["H"], c["Q"], c["H"] * 128
+    xs = ko.bf16_to_f64(c["x"]).reshape(B * Q, 3, H, 128)
+    live = np.repeat(c["state_slots"] > 0, Q)
+    for part, (a, b_) in enumerate(((q, qn), (k, kn), (v, vn))):
+        diff = ko.bf16_to_f64(a) - ko.bf16_to_f64(b_)
+        ref = xs[:, part]
+        err = np.abs(diff - ref)[live]
+        bound = 2 * 2.0 ** -8 * np.abs(ref)[live] + 1e-30
+        assert np.all(err <= bound + 2 * 2.0 ** -8 * np.abs(diff)[live])
+
+
+def test_new_window_is_taps_then_inputs():
+    c = _layer()
+    c["pending"][:] = 2
+    _, state = _prologue(c)
+    Q, RQ = c["Q"], c["RQ"]
+    for b in range(c["B"]):
+        slot = int(c["state_slots"][b])
+        if slot <= 0:
+            continue
+        old = c["conv_state"][slot]
+        np.testing.assert_array_equal(state[slot][:, 0], old[:, 2])   # window[n-1+1], n = 2
+        np.testing.assert_array_equal(state[slot][:, 1], old[:, 3])
+        np.testing.assert_array_equal(state[slot][:, 2:2 + Q], c["x"][b * Q:(b + 1) * Q].T)
+        np.testing.assert_array_equal(state[slot][:, 2 + Q:], old[:, 2 + Q:])
+    assert RQ == Q
+
+
+def test_gate_projection_with_unit_rows_copies_the_activations():
+    # Row f of head h's f_b block is the unit vector at column (f + 1 + h) mod
+    # 128, so raw_g[t, h, f] = f_a[t, (f + 1 + h) mod 128] exactly: a
+    # transposed product or a head mix-up picks other columns.
+    c = _layer()
+    fb = np.zeros((c["H"] * 128, 128), dtype=np.float32)
+    f = np.arange(128)
+    for h in range(c["H"]):
+        fb[h * 128 + f, (f + 1 + h) % 128] = 1.0
+    c["f_b"] = _bits(fb)
+    (_, _, _, g), _ = _prologue(c)
+    Q = c["Q"]
+    for b in range(c["B"]):
+        if c["state_slots"][b] <= 0:
+            assert not g[b * Q:(b + 1) * Q].any()
+            continue
+        for h in range(c["H"]):
+            np.testing.assert_array_equal(g[b * Q:(b + 1) * Q, h],
+                                          c["f_a"][b * Q:(b + 1) * Q][:, (f + 1 + h) % 128])
+
+
+def test_gated_norm_closed_form_and_scale_invariance():
+    T, H = 3, 2
+    w = np.linspace(0.5, 1.5, 128).astype(np.float32)
+    c0 = 0.75
+    o = np.full((T, H, 128), c0, dtype=np.float32)
+    gate0 = np.zeros((T, H * 128), dtype=np.float32)
+    out = ko.layer_epilogue(o=_bits(o), gate=_bits(gate0), norm_weight=w, eps=1e-6)
+    expect = c0 / math.sqrt(c0 * c0 + 1e-6) * w.astype(np.float64) * 0.5
+    np.testing.assert_array_equal(out.reshape(T, H, 128), np.broadcast_to(ko.f64_to_bf16(expect),
+                                                                         (T, H, 128)))
+    rng = np.random.default_rng(3)
+    o = _bits(np.ldexp(np.round(rng.standard_normal((T, H, 128)) * 64), -6).astype(np.float32))
+    gate = _bits(np.round(rng.standard_normal((T, H * 128)) * 8).astype(np.float32) / 8)
+    a = ko.layer_epilogue(o=o, gate=gate, norm_weight=w, eps=0.0)
+    doubled = _bits(ko.bf16_to_f64(o).astype(np.float32) * 2)
+    b = ko.layer_epilogue(o=doubled, gate=gate, norm_weight=w, eps=0.0)
+    np.testing.assert_array_equal(a, b)
+    minus_inf = np.full(gate.shape, 0xFF80, dtype=np.uint16)
+    z = ko.layer_epilogue(o=o, gate=minus_inf, norm_weight=w, eps=1e-6)
+    assert not np.any(ko.bf16_to_f64(z))
