@@ -356,7 +356,7 @@ def _event_ms(stream, fn, iters):
     return e0.elapsed_time(e1) / iters
 
 
-ROW_GROUPS = ("commit", "mid_batch", "varlen", "latency", "bookkeeping", "decode_loop")
+ROW_GROUPS = ("commit", "mid_batch", "varlen", "latency", "bookkeeping", "decode_loop", "layer")
 
 
 def measure_rows(dev, stream, peak, cpu_seconds, only=None):
@@ -547,7 +547,83 @@ def measure_rows(dev, stream, peak, cpu_seconds, only=None):
 
     if want("decode_loop"):
         rows["decode_loop"] = measure_decode_loop(dev, dt, peak)
+    if want("layer"):
+        rows["layer"] = measure_layer(dev, stream, dt, peak)
     return rows
+
+
+def layer_algorithmic_bytes(c):
+    """Bytes the layer's prologue and epilogue must move for one step (the
+    step's own are ``algorithmic_bytes``).  Prologue, per live (request,
+    head) item: its q, k, v input channels (3 * Q * 256 B), three window
+    values read and Q + 2 written per channel (384 channels, BF16), and the
+    step inputs q, k, v, raw_g written (4 * Q * 256 B); once: f_a, f_b and
+    the convolution weights.  Epilogue, per (token, head): the step output
+    and the gate read and the layer output written (3 * 256 B)."""
+    B, H, Q = c["B"], c["H"], c["Q"]
+    live = int((c["state_slots"] > c["null_slot"]).sum()) * H
+    per_item = 3 * Q * 256 + 384 * (3 + Q + 2) * 2 + 4 * Q * 256
+    once = c["f_a"].nbytes + c["f_b"].nbytes + c["conv_weight"].nbytes
+    once += 0 if c["conv_bias"] is None else c["conv_bias"].nbytes
+    prologue = live * per_item + once
+    epilogue = B * Q * H * 3 * 256 + c["norm_weight"].nbytes
+    return prologue, epilogue
+
+
+def measure_layer(dev, stream, dt, peak):
+    """The model layer around the large-batch step: the prologue
+    (convolution + SiLU, gate projection, window rewrite), the fused
+    replay + verify on its outputs, and the gated-norm epilogue."""
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import (kda_layer_epilogue,
+                                                               kda_layer_prologue,
+                                                               kda_replay_verify, synth)
+    name = "layer-f32-h64-b512-q8"
+    c = synth.make(name)
+    keys = ("x", "conv_weight", "conv_bias", "conv_state", "f_a", "f_b", "gate", "norm_weight",
+            "raw_beta", "A_log", "dt_bias", "state", "state_slots", "record_rows", "pending",
+            "corr", "key_gate")
+    d = {k: None if c[k] is None else dt(c[k]) for k in keys}
+    T = c["B"] * c["Q"]
+    shape = (T, c["H"], 128)
+    for k in ("q", "k", "v", "raw_g", "o"):
+        d[k] = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    out = torch.zeros((T, c["H"] * 128), dtype=torch.bfloat16, device=dev)
+
+    def prologue():
+        kda_layer_prologue(d["x"], d["conv_weight"], d["conv_bias"], d["conv_state"], d["f_a"],
+                           d["f_b"], d["state_slots"], d["record_rows"], d["pending"], d["q"],
+                           d["k"], d["v"], d["raw_g"], Q=c["Q"], stream=stream)
+
+    def core():
+        kda_replay_verify(d["q"], d["k"], d["v"], d["raw_g"], d["raw_beta"], d["A_log"],
+                          d["dt_bias"], d["state"], d["state_slots"], d["record_rows"],
+                          d["pending"], d["corr"], d["key_gate"], d["o"], Q=c["Q"],
+                          lower_bound=c["lower_bound"], q_scale=c["q_scale"], split=0,
+                          stream=stream)
+
+    def epilogue():
+        kda_layer_epilogue(d["o"], d["gate"], d["norm_weight"], out, eps=c["eps"],
+                           stream=stream)
+
+    def layer():
+        prologue()
+        core()
+        epilogue()
+    for _ in range(3):
+        layer()
+    ms = {"layer": _event_ms(stream, layer, 20), "prologue": _event_ms(stream, prologue, 20),
+          "step": _event_ms(stream, core, 20), "epilogue": _event_ms(stream, epilogue, 20)}
+    pro_b, epi_b = layer_algorithmic_bytes(c)
+    step_b = algorithmic_bytes(c)
+    total = pro_b + step_b["total"] + epi_b
+    gbs = total / ms["layer"] / 1e6
+    return dict(
+        workload=name, ms=ms, tok_s=step_b["live_tokens"] / (ms["layer"] / 1e3),
+        bytes_per_launch=dict(prologue=pro_b, step=step_b["total"], epilogue=epi_b),
+        roofline=dict(bound="hbm", achieved=gbs, peak=peak, unit="GB/s", frac=gbs / peak),
+        prologue_roofline_frac=pro_b / ms["prologue"] / 1e6 / peak,
+        epilogue_roofline_frac=epi_b / ms["epilogue"] / 1e6 / peak)
 
 
 def decode_loop_bytes(c, eager):

@@ -244,6 +244,58 @@ int kda_flush_plan(const int32_t *state_slots, const int32_t *record_rows,
  */
 int kda_selftest_wait_timeout(int32_t *status, void *stream);
 
+/*
+ * kda_layer_prologue -- the model layer's operands for the step ("kda.fused"
+ * page, KdaFused.kernel: the convolution operands, convolution and SiLU,
+ * gate projection, the window written last).  Per (request b, head h) with
+ * slot = state_slots[b] > null_slot, r = record_rows[b] (or b when NULL) and
+ * n = (pending && r >= 0) ? clamp(pending[r], 0, rq) : 0, for each channel
+ * ch = part*D + h*128 + c of q (part 0), k (1) and v (2), D = H*128:
+ *   s = [W[off], W[off+1], W[off+2], x_0 .. x_{Q-1}], W = conv_state[slot, ch],
+ *       off = n - 1 when n > 0 else 0, x_t = x[b*Q + t, ch];
+ *   out_t = BF16(silu(bias[ch] + sum_{i<4} conv_weight[part, i, h*128 + c] *
+ *           s[t + i])), silu(z) = z / (1 + e^-z), written to q / k / v
+ *           [b*Q + t, h, c];
+ *   raw_g[b*Q + t, h, f] = BF16(sum_j f_b[h*128 + f, j] * f_a[b*Q + t, j]);
+ *   W <- [W[off+1], W[off+2], x_0 .. x_{Q-1}] (entries from 2 + Q kept).
+ * Inert requests are skipped (nothing read or written; the step writes
+ * their zero outputs); a slot >= n_slots is reported as KDA_ERR_ARG in
+ * status and skipped.  The sums run in FP32 (the convolution in tap order,
+ * the projection in column order) and round once to BF16.
+ *
+ *   x             [B*Q, 3*D] BF16 (q | k | v channels before the convolution)
+ *   conv_weight   [3, 4, D] BF16 (tap 3 multiplies the current token)
+ *   conv_bias     [3*D] BF16 or NULL
+ *   conv_state    [n_slots, 3*D, rq + 2] BF16, slot stride conv_slot_stride
+ *                 elements (>= 3*D*(rq+2), a multiple of 8); 16-byte
+ *                 aligned; read and rewritten
+ *   f_a           [B*Q, 128] BF16;  f_b [D, 128] BF16, 16-byte aligned
+ *   q, k, v, raw_g  [B*Q, H, 128] BF16 outputs (the step's inputs)
+ *   pending       [n_rows] int32 or NULL (no replay pending: off = 0)
+ *   1 <= Q <= rq <= 8.
+ */
+int kda_layer_prologue(const kda_bf16 *x, const kda_bf16 *conv_weight,
+                       const kda_bf16 *conv_bias, kda_bf16 *conv_state,
+                       int64_t conv_slot_stride, const kda_bf16 *f_a,
+                       const kda_bf16 *f_b, const int32_t *state_slots,
+                       const int32_t *record_rows, const int32_t *pending,
+                       int n_slots, int n_rows, int rq, kda_bf16 *q, kda_bf16 *k,
+                       kda_bf16 *v, kda_bf16 *raw_g, int B, int H, int Q,
+                       int null_slot, int32_t *status, void *stream);
+
+/*
+ * kda_layer_epilogue -- the gated RMSNorm of the step's outputs ("kda.fused"
+ * page, the kernel's end).  For every token t and head h, over the 128
+ * value rows r of o[t, h, :] (the step's BF16 outputs):
+ *   out[t, h*128 + r] = BF16(o * rsqrt(sum_r o^2 / 128 + eps) * norm_weight[r]
+ *                            * sigmoid(gate[t, h*128 + r]))
+ * in FP32.  o [n_tokens, H, 128] BF16; gate, out [n_tokens, H*128] BF16;
+ * norm_weight [128] FP32; eps >= 0.  All four pointers 16-byte aligned.
+ */
+int kda_layer_epilogue(const kda_bf16 *o, const kda_bf16 *gate,
+                       const float *norm_weight, float eps, kda_bf16 *out,
+                       int n_tokens, int H, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

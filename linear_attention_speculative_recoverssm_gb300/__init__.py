@@ -21,6 +21,8 @@ from ._lib import (  # noqa: F401
     kda_commit,
     kda_defer_commit,
     kda_flush_plan,
+    kda_layer_epilogue,
+    kda_layer_prologue,
     kda_replay_verify,
     kda_selftest_wait_timeout,
     kda_verify,

@@ -25,7 +25,8 @@ KDA_STATE_F32 = 0
 KDA_STATE_BF16 = 1
 
 EXPORTS = ("kda_abi_version", "kda_error_string", "kda_verify", "kda_replay_verify",
-           "kda_commit", "kda_defer_commit", "kda_flush_plan", "kda_selftest_wait_timeout")
+           "kda_commit", "kda_defer_commit", "kda_flush_plan", "kda_selftest_wait_timeout",
+           "kda_layer_prologue", "kda_layer_epilogue")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -44,6 +45,9 @@ _SIGS = {
     "kda_defer_commit": ([_P] * 5 + [_I, _I, _I, _P, _P], _I),
     "kda_flush_plan": ([_P] * 7 + [_I, _I, _I, _I, _P, _P], _I),
     "kda_selftest_wait_timeout": ([_P, _P], _I),
+    "kda_layer_prologue": ([_P] * 4 + [_I64] + [_P] * 5 + [_I, _I, _I] + [_P] * 4
+                           + [_I, _I, _I, _I, _P, _P], _I),
+    "kda_layer_epilogue": ([_P, _P, _P, _F, _P, _I, _I, _P], _I),
 }
 
 _lib = None
@@ -212,3 +216,40 @@ def kda_selftest_wait_timeout(status, *, stream=None, raise_on_error=True):
     KDA_ERR_TIMEOUT to ``status`` (device int32)."""
     rc = load().kda_selftest_wait_timeout(_ptr(status), _stream(stream))
     return _check("kda_selftest_wait_timeout", rc, raise_on_error)
+
+
+def kda_layer_prologue(x, conv_weight, conv_bias, conv_state, f_a, f_b, state_slots,
+                       record_rows, pending, q, k, v, raw_g, *, Q, rq=None, null_slot=0,
+                       status=None, stream=None, raise_on_error=True):
+    """The layer's convolution + SiLU, gate projection and window rewrite
+    (shapes as in include/kda_recoverssm.h; conv_state [slots, 3*H*128,
+    rq + 2])."""
+    import torch
+    for name, t in (("x", x), ("conv_weight", conv_weight), ("conv_bias", conv_bias),
+                    ("conv_state", conv_state), ("f_a", f_a), ("f_b", f_b), ("q", q), ("k", k),
+                    ("v", v), ("raw_g", raw_g)):
+        _expect(t, torch.bfloat16, name)
+    for name, t in (("state_slots", state_slots), ("record_rows", record_rows),
+                    ("pending", pending)):
+        _expect(t, torch.int32, name)
+    rq = conv_state.shape[2] - 2 if rq is None else rq
+    rc = load().kda_layer_prologue(
+        _ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state), conv_state.stride(0),
+        _ptr(f_a), _ptr(f_b), _ptr(state_slots), _ptr(record_rows), _ptr(pending),
+        conv_state.shape[0], 0 if pending is None else pending.shape[0], rq, _ptr(q), _ptr(k),
+        _ptr(v), _ptr(raw_g), state_slots.shape[0], q.shape[1], Q, null_slot, _ptr(status),
+        _stream(stream))
+    return _check("kda_layer_prologue", rc, raise_on_error)
+
+
+def kda_layer_epilogue(o, gate, norm_weight, out, *, eps, stream=None, raise_on_error=True):
+    """The gated RMSNorm of the step's outputs o [T, H, 128] into out
+    [T, H*128]."""
+    import torch
+    _expect(o, torch.bfloat16, "o")
+    _expect(gate, torch.bfloat16, "gate")
+    _expect(out, torch.bfloat16, "out")
+    _expect(norm_weight, torch.float32, "norm_weight")
+    rc = load().kda_layer_epilogue(_ptr(o), _ptr(gate), _ptr(norm_weight), eps, _ptr(out),
+                                   o.shape[0], o.shape[1], _stream(stream))
+    return _check("kda_layer_epilogue", rc, raise_on_error)

@@ -108,3 +108,25 @@ def test_commit_and_bookkeeping_host_checks(lib):
     assert lib.kda_defer_commit(A, A, A, A, None, 0, 0, 2, None, None) == _lib.KDA_OK
     assert lib.kda_flush_plan(A, A, A, A, A, A, A, 2, 9, 0, 2, None, None) == _lib.KDA_ERR_ARG
     assert lib.kda_flush_plan(A, A, A, A, A, A, A, 0, 4, 0, 2, None, None) == _lib.KDA_OK
+
+
+def test_layer_host_checks(lib):
+    # kda_layer_prologue(x, w, bias, conv_state, stride, f_a, f_b, slots, rows, pending,
+    #                    n_slots, n_rows, rq, q, k, v, g, B, H, Q, null, status, stream)
+    def pro(**over):
+        a = dict(x=A, w=A, bias=None, cs=A, stride=3 * 2 * 128 * 6, fa=A, fb=A, slots=A,
+                 rows=None, pending=None, n_slots=4, n_rows=2, rq=4, q=A, k=A, v=A, g=A, B=2,
+                 H=2, Q=4, null=0, status=None, stream=None)
+        a.update(over)
+        return lib.kda_layer_prologue(*a.values())
+    assert pro(Q=0) == _lib.KDA_ERR_ARG
+    assert pro(Q=5) == _lib.KDA_ERR_ARG            # Q > rq
+    assert pro(stride=100) == _lib.KDA_ERR_ARG     # window smaller than 3 * D * (rq + 2)
+    assert pro(x=None) == _lib.KDA_ERR_ARG
+    assert pro(fb=A + 2) == _lib.KDA_ERR_ALIGN
+    assert pro(B=0) == _lib.KDA_OK
+    # kda_layer_epilogue(o, gate, w, eps, out, n_tokens, H, stream)
+    assert lib.kda_layer_epilogue(A, A, A, -1.0, A, 4, 2, None) == _lib.KDA_ERR_ARG
+    assert lib.kda_layer_epilogue(A, A, A + 4, 1e-6, A, 4, 2, None) == _lib.KDA_ERR_ALIGN
+    assert lib.kda_layer_epilogue(A, A, A, 1e-6, A, 0, 2, None) == _lib.KDA_OK
+    assert lib.kda_layer_epilogue(None, A, A, 1e-6, A, 4, 2, None) == _lib.KDA_ERR_ARG
