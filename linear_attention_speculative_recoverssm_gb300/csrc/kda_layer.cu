@@ -14,7 +14,7 @@
 namespace kda {
 namespace {
 
-constexpr int kConvThreads = 128;  // thread = channel of one part (q, k or v) of a head
+constexpr int kConvThreads = 128;  // threads of a convolution CTA
 constexpr int kGateTokens = 128;   // tokens per gate-projection CTA (8 warps x 16)
 
 struct LayerParams {
@@ -32,76 +32,99 @@ struct LayerParams {
   int32_t *status;
 };
 
-// One CTA per (request, head, part): thread c convolves channel c of q, k
-// or v over the sequence [window[off .. off+2], x_0 .. x_{Q-1}] (off = n - 1
-// after n pending tokens, 0 without), applies SiLU, rounds to BF16, and
-// rewrites its window to [window[off+1], window[off+2], x_0 ..].  The loads
-// that do not depend on the slot are issued first, the slot and the record
-// row together.  The CTA's 128 windows are one contiguous block of 128 *
-// (rq + 2) BF16, moved between HBM and shared memory with 16-byte accesses.
+// CTAs over (request, slice of channels); each thread takes groups of 8
+// consecutive channels (one part, one head), so every access is 16 bytes:
+// the Q inputs of the group are one uint4 per token, the group's 8 windows
+// (8 * (rq + 2) BF16, contiguous) are rq + 2 uint4, the outputs one uint4
+// per token.  The slot and pending count are loaded once per CTA.  Channel
+// j of a group is convolved over [window[off .. off+2], x_0 .. x_{Q-1}]
+// (off = n - 1 after n pending tokens, 0 without), SiLU-ed, rounded to BF16,
+// and its window rewritten to [window[off+1], window[off+2], x_0 ..]; the
+// windows pass through a thread-private shared-memory block.
+constexpr int kConvCtas = 8;  // CTAs per request
+
 template <int Q>
 __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams p) {
-  __shared__ __align__(16) uint16_t wins[kConvThreads * (kMaxQ + 2)];
-  const int item = blockIdx.x / 3, part = blockIdx.x - 3 * (blockIdx.x / 3);
-  const int b = item / p.H, h = item - b * p.H;
-  const int c = threadIdx.x;
-  const int D = p.H * kDim;
-  const long long tok0 = (long long)b * Q;
-  const long long ch = (long long)part * D + h * kDim + c;
+  __shared__ __align__(16) uint16_t wins[kConvThreads][8 * (kMaxQ + 2)];
+  const int b = blockIdx.x;
   const int slot = p.state_slots[b];
   const int rec = p.pending != nullptr ? (p.record_rows != nullptr ? p.record_rows[b] : b) : -1;
-  uint16_t xb[Q];
-#pragma unroll
-  for (int t = 0; t < Q; ++t) xb[t] = p.x[(tok0 + t) * (3LL * D) + ch];
-  float w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    w[i] = bf16_bits_to_f32(p.conv_w[(long long)(part * 4 + i) * D + h * kDim + c]);
-  const float bias = p.conv_b != nullptr ? bf16_bits_to_f32(p.conv_b[ch]) : 0.f;
   if (slot >= p.n_slots) {
-    if (c == 0 && part == 0) report(p.status, KDA_ERR_ARG);
+    if (threadIdx.x == 0 && blockIdx.y == 0) report(p.status, KDA_ERR_ARG);
     return;
   }
   if (slot <= p.null_slot) return;  // inert: the step writes its zero outputs
-  const int W = p.rq + 2;
-  uint4 *blk = reinterpret_cast<uint4 *>(p.conv_state + (long long)slot * p.conv_slot_stride +
-                                         (ch - c) * W);
-  const int nvec = kConvThreads * W / 8;  // 16-byte vectors in the block
-  uint4 *sv = reinterpret_cast<uint4 *>(wins);
-  for (int e = c; e < nvec; e += kConvThreads) sv[e] = blk[e];
   int n = 0;  // pending tokens (their count sets the window offset)
   if (rec >= p.n_rows) {
-    if (c == 0 && part == 0) report(p.status, KDA_ERR_ARG);
+    if (threadIdx.x == 0 && blockIdx.y == 0) report(p.status, KDA_ERR_ARG);
   } else if (rec >= 0) {
     n = p.pending[rec];
     n = n < 0 ? 0 : (n > p.rq ? p.rq : n);
   }
   const int off = n > 0 ? n - 1 : 0;
-  __syncthreads();
-  uint16_t *win = wins + c * W;
-  const uint16_t t0 = win[off], t1 = win[off + 1], t2 = win[off + 2];
-  float seq[Q + 3];
-  seq[0] = bf16_bits_to_f32(t0);
-  seq[1] = bf16_bits_to_f32(t1);
-  seq[2] = bf16_bits_to_f32(t2);
+  const int D = p.H * kDim;
+  const int W = p.rq + 2;
+  const int groups = 3 * D / 8;
+  const long long tok0 = (long long)b * Q;
+  uint16_t *mine = wins[threadIdx.x];
+  for (int g = blockIdx.y * kConvThreads + threadIdx.x; g < groups;
+       g += kConvCtas * kConvThreads) {
+    const int ch = 8 * g, part = ch / D, hc = ch - part * D;  // hc = h * 128 + c0
+    uint4 xv[Q];
 #pragma unroll
-  for (int t = 0; t < Q; ++t) seq[3 + t] = bf16_bits_to_f32(xb[t]);
-  uint16_t *out = part == 0 ? p.q : (part == 1 ? p.k : p.v);
+    for (int t = 0; t < Q; ++t)
+      xv[t] = *reinterpret_cast<const uint4 *>(p.x + (tok0 + t) * (3LL * D) + ch);
+    uint4 wv[4];
 #pragma unroll
-  for (int t = 0; t < Q; ++t) {
-    float acc = bias;
+    for (int i = 0; i < 4; ++i)
+      wv[i] = *reinterpret_cast<const uint4 *>(p.conv_w + (long long)(part * 4 + i) * D + hc);
+    uint4 bv = make_uint4(0, 0, 0, 0);
+    if (p.conv_b != nullptr) bv = *reinterpret_cast<const uint4 *>(p.conv_b + ch);
+    uint4 *blk = reinterpret_cast<uint4 *>(p.conv_state + (long long)slot * p.conv_slot_stride +
+                                           (long long)ch * W);
+    uint4 *sv = reinterpret_cast<uint4 *>(mine);
+    for (int e = 0; e < W; ++e) sv[e] = blk[e];
+    const uint16_t *xh[Q];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc = fmaf(seq[t + i], w[i], acc);
-    const float sval = acc / (1.f + expf(-acc));
-    out[((tok0 + t) * p.H + h) * kDim + c] = (uint16_t)f32_to_bf16_bits(sval);
+    for (int t = 0; t < Q; ++t) xh[t] = reinterpret_cast<const uint16_t *>(&xv[t]);
+    const uint16_t *wh[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) wh[i] = reinterpret_cast<const uint16_t *>(&wv[i]);
+    const uint16_t *bh = reinterpret_cast<const uint16_t *>(&bv);
+    uint32_t res[Q][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint16_t *win = mine + j * W;
+      const uint16_t t0 = win[off], t1 = win[off + 1], t2 = win[off + 2];
+      float seq[Q + 3];
+      seq[0] = bf16_bits_to_f32(t0);
+      seq[1] = bf16_bits_to_f32(t1);
+      seq[2] = bf16_bits_to_f32(t2);
+#pragma unroll
+      for (int t = 0; t < Q; ++t) seq[3 + t] = bf16_bits_to_f32(xh[t][j]);
+      const float bias = bf16_bits_to_f32(bh[j]);
+#pragma unroll
+      for (int t = 0; t < Q; ++t) {
+        float acc = bias;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = fmaf(seq[t + i], bf16_bits_to_f32(wh[i][j]), acc);
+        const uint32_t bits = f32_to_bf16_bits(acc / (1.f + expf(-acc)));
+        if (j & 1) res[t][j >> 1] |= bits << 16;
+        else res[t][j >> 1] = bits;
+      }
+      win[0] = t1;  // entries from 2 + Q on (rq > Q) are kept
+      win[1] = t2;
+#pragma unroll
+      for (int t = 0; t < Q; ++t) win[2 + t] = xh[t][j];
+    }
+    uint16_t *out = part == 0 ? p.q : (part == 1 ? p.k : p.v);
+    const int h = hc / kDim, c0 = hc - h * kDim;
+#pragma unroll
+    for (int t = 0; t < Q; ++t)
+      *reinterpret_cast<uint4 *>(out + ((tok0 + t) * p.H + h) * kDim + c0) =
+          make_uint4(res[t][0], res[t][1], res[t][2], res[t][3]);
+    for (int e = 0; e < W; ++e) blk[e] = sv[e];
   }
-  // the window for the next step (this thread's channel only: read above)
-  win[0] = t1;
-  win[1] = t2;
-#pragma unroll
-  for (int t = 0; t < Q; ++t) win[2 + t] = xb[t];
-  __syncthreads();
-  for (int e = c; e < nvec; e += kConvThreads) blk[e] = sv[e];
 }
 
 // D[16 x 8] += A[16 x 16] . B[16 x 8]: BF16 operands, FP32 accumulation
@@ -200,7 +223,7 @@ __global__ void __launch_bounds__(256) kda_layer_epilogue(const uint16_t *__rest
 
 template <int Q>
 int launch_prologue_q(const LayerParams &p, int items, cudaStream_t stream) {
-  kda_layer_conv<Q><<<3 * items, kConvThreads, 0, stream>>>(p);
+  kda_layer_conv<Q><<<dim3(p.B, kConvCtas), kConvThreads, 0, stream>>>(p);
   const int n_tokens = p.B * Q;
   const dim3 grid((n_tokens + kGateTokens - 1) / kGateTokens, p.H);
   kda_layer_gate<<<grid, 256, 0, stream>>>(p, Q, n_tokens);
@@ -230,8 +253,10 @@ int kda_layer_prologue(const kda_bf16 *x, const kda_bf16 *conv_weight, const kda
   if (conv_slot_stride < 3LL * H * KDA_HEAD_DIM * (rq + 2)) return KDA_ERR_ARG;
   if ((long long)B * H * 3 > 0x7fffffffLL || (long long)B * Q > 0x7fffffffLL || H > 65535)
     return KDA_ERR_ARG;
-  if (!kda::aligned16(f_a) || !kda::aligned16(f_b) || !kda::aligned16(conv_state) ||
-      conv_slot_stride % 8 != 0)
+  if (!kda::aligned16(x) || !kda::aligned16(conv_weight) ||
+      (conv_bias != nullptr && !kda::aligned16(conv_bias)) || !kda::aligned16(f_a) ||
+      !kda::aligned16(f_b) || !kda::aligned16(conv_state) || !kda::aligned16(q) ||
+      !kda::aligned16(k) || !kda::aligned16(v) || conv_slot_stride % 8 != 0)
     return KDA_ERR_ALIGN;
   kda::LayerParams p;
   p.x = x;

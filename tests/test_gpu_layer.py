@@ -103,12 +103,14 @@ def _compare_prologue(case, d, ref, ref_state, items=None):
                     np.testing.assert_array_equal(got_state[s, chans], ref_state[s, chans])
 
 
-@pytest.mark.parametrize("Q,bias,pending", [(8, True, True), (4, False, True), (1, True, True),
-                                            (5, True, False), (3, False, False)])
-def test_layer_prologue(Q, bias, pending):
+@pytest.mark.parametrize("Q,bias,pending,RQ", [(8, True, True, 8), (4, False, True, 4),
+                                               (1, True, True, 1), (5, True, False, 5),
+                                               (3, False, False, 3), (4, True, True, 7)])
+def test_layer_prologue(Q, bias, pending, RQ):
+    """RQ > Q: the window is longer than the new one, whose tail is kept."""
     import torch
     case = synth.layer_case(B=14, H=3, Q=Q, slots=40, seed=80 + Q, bias=bias,
-                            padding_frac=0.2)
+                            padding_frac=0.2, RQ=RQ)
     d = _device_layer(case)
     _gpu_prologue(case, d, pending)
     torch.cuda.synchronize()
