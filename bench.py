@@ -104,11 +104,11 @@ PROFILED = {
     "step": dict(
         sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
                  "kda_step_q8.cu"),
-        sha256="83618a216df65d8ecfd744b51e7f8df3fa3aa32ba1615d0799cfe394cb848082",
+        sha256="9288e146e1e84243e63686268ea5b5ed48d893f42106f1bb7906d2714e9134e2",
         workload=WORKLOAD,
-        bytes_per_launch=(608.2 + 464.1) * 1e6 * 31104 / 7808,
+        bytes_per_launch=(608.2 + 464.2) * 1e6 * 31104 / 7808,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
-            "replay-verify-f32-h64-b128-q8 (608.2 + 464.1 MB, 7808 live items), scaled by "
+            "replay-verify-f32-h64-b128-q8 (608.2 + 464.2 MB, 7808 live items), scaled by "
             "live items to this workload's 31104"),
     # one kda_commit_ws launch of the standalone-commit workload itself
     "commit": dict(
