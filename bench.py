@@ -104,7 +104,7 @@ PROFILED = {
     "step": dict(
         sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
                  "kda_step_q8.cu"),
-        sha256="9288e146e1e84243e63686268ea5b5ed48d893f42106f1bb7906d2714e9134e2",
+        sha256="591e88a51bb73e5f0cec8cda69dfcfddb0c9907a711de87ff2e7bb6e73f5cc1e",
         workload=WORKLOAD,
         bytes_per_launch=(608.2 + 464.2) * 1e6 * 31104 / 7808,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "

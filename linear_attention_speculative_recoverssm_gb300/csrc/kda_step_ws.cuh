@@ -7,8 +7,8 @@
 // One CTA per SM, 384 threads, items (request, head) strided over the grid.
 //
 //  * Prologue warpgroup (warps 0-3, thread c <-> key channel c) builds each
-//    item's operands into one of two shared "ops" buffers, one item ahead of
-//    the main warpgroups: the decays of this window and of the recorded
+//    item's operands into one of three shared "ops" buffers, up to three
+//    items ahead of the main warpgroups: the decays of this window and of the recorded
 //    tokens, Gamma_t * k_t and Gamma_t * q_t, the replay coefficients
 //    k_t * P_t and D_n, the squared norms of q_t and of the recorded keys
 //    reduced over the 128 channels, beta, v, and the recorded corrections
@@ -36,6 +36,13 @@
 //        group, the outputs o_t = y_t + sum_s B_ts u_s (BF16) and the
 //        corrections u_t (FP32).
 //    Main warps synchronise only through mbarriers, never a CTA barrier.
+//    An inert item's stage phase is a bare arrival; the main warps still
+//    wait for it before counting their read of the stage, so a warp that
+//    runs ahead cannot count its read among the previous item's.
+//  * Windows: request b's window is tokens b*Q .. b*Q + Q - 1, or, in the
+//    VARLEN instances, the q_b <= Q tokens query_start_loc[b] .. whose
+//    bounds the index chain loads and checks; only the window's tokens get
+//    outputs and records.
 //  * Hand-offs: mbarriers full[stage] (bulk copy landed), opfull[buf] (ops
 //    ready), opempty[buf] (ops consumed by every main warp), and a counter
 //    per stage whose eighth reader requests the next page into it.  Every
