@@ -59,12 +59,15 @@ class DeferredRecoverSSM:
                    record_rows=self.record_rows, null_slot=self.null_slot, status=self.status,
                    stream=self.stream)
 
-    def verify(self, q, k, v, raw_g, raw_beta, out):
-        """Verify this step's window (q, k, v, raw_g BF16 [B*Q, H, 128],
-        raw_beta BF16 [B*Q, H]) into out BF16 [B*Q, H, 128], writing the
-        window's records."""
+    def verify(self, q, k, v, raw_g, raw_beta, out, query_start_loc=None):
+        """Verify this step's window (q, k, v, raw_g BF16 [T, H, 128],
+        raw_beta BF16 [T, H]; T = B*Q, or packed windows of q_b <= Q tokens
+        given by query_start_loc [B + 1]) into out BF16 [T, H, 128], writing
+        the window's records.  With windows of different lengths the counts
+        passed to ``accept`` must not exceed each request's q_b."""
         common = dict(Q=self.Q, lower_bound=self.lower_bound, q_scale=self.q_scale,
-                      null_slot=self.null_slot, status=self.status, stream=self.stream)
+                      null_slot=self.null_slot, status=self.status, stream=self.stream,
+                      query_start_loc=query_start_loc)
         if self.flushed:
             kda_verify(q, k, v, raw_g, raw_beta, self.A_log, self.dt_bias, self.state_pool,
                        self.state_slots, self.corr, self.key_gate, out,

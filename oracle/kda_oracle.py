@@ -388,7 +388,7 @@ def flush_plan(*, state_slots, record_rows, pending, commit_lens, final_slots,
 
 def decode_stock(*, windows, window_of_step, accepted, A_log, dt_bias,
                  lower_bound, q_scale, state, state_slots, B, H, Q,
-                 null_slot=0, items=None):
+                 null_slot=0, items=None, query_start_loc=None):
     """Speculative decoding of one layer over several steps by the stock
     recurrence alone, with no records, deferral or flush: per live item an
     FP64 state starts from its pool page; at every step the window is
@@ -399,13 +399,16 @@ def decode_stock(*, windows, window_of_step, accepted, A_log, dt_bias,
 
     windows: q, k, v, raw_g [W, B*Q, H, K|V] and raw_beta [W, B*Q, H] (BF16
     bits), step s using window ``window_of_step[s]``; accepted [steps, B],
-    clamped to [0, Q].  Returns (outs, finals): outs [steps, B*Q, H, V] FP64
-    (zero on inert rows) and finals, a dict (b, h) -> the FP64 state after
-    the last step.
+    clamped to [0, q_b].  With ``query_start_loc`` [steps, B + 1] the
+    windows are packed: step s's request b has the q_b tokens
+    query_start_loc[s, b] .. query_start_loc[s, b+1] - 1.  Returns (outs,
+    finals): outs [steps, T, H, V] FP64 (zero on inert rows) and finals, a
+    dict (b, h) -> the FP64 state after the last step.
     """
     steps = accepted.shape[0]
     V = state.shape[2]
-    outs = np.zeros((steps, B * Q, H, V))
+    T = windows["q"].shape[1]
+    outs = np.zeros((steps, T, H, V))
     finals = {}
     for b, h in _items(B, H, items):
         slot = int(state_slots[b])
@@ -413,15 +416,19 @@ def decode_stock(*, windows, window_of_step, accepted, A_log, dt_bias,
             continue
         a_log = float(A_log[h])
         bias = dt_bias[h].astype(np.float64)
-        tok = slice(b * Q, (b + 1) * Q)
         S = state_to_f64(state[slot, h])
         for s in range(steps):
+            if query_start_loc is None:
+                tok, qb = slice(b * Q, (b + 1) * Q), Q
+            else:
+                t0, t1 = int(query_start_loc[s, b]), int(query_start_loc[s, b + 1])
+                tok, qb = slice(t0, t1), t1 - t0
             w = int(window_of_step[s])
             q, k, v, g, beta = (bf16_to_f64(windows[key][w, tok, h])
                                 for key in ("q", "k", "v", "raw_g", "raw_beta"))
             _, outs[s, tok, h] = verify_item(S, q, k, v, g, beta, a_log, bias,
                                              lower_bound, q_scale)
-            a = min(max(int(accepted[s, b]), 0), Q)
+            a = min(max(int(accepted[s, b]), 0), qb)
             S = advance_item(S, k, v, g, beta, a, a_log, bias, lower_bound)
         finals[(b, h)] = S
     return outs, finals

@@ -148,3 +148,63 @@ def test_decode_loop_full_size_graph_sampled():
     worst = max(float(np.abs(pool_rows[key].astype(np.float64) - S).max() / np.abs(S).max())
                 for key, S in finals.items())
     print(f"\ndecode drift full size, {cycles * steps} steps: max|dS|/max|S| = {worst:.2e}")
+
+
+def _varlen_steps(case, seed):
+    """Each step's window repacked to q_b ~ U{1..Q} tokens per request
+    (query_start_loc [steps, B + 1]), padded with zero rows to B*Q; the
+    accepted counts limited to q_b."""
+    B, Q, steps = case["B"], case["Q"], case["steps"]
+    rng = np.random.default_rng(seed)
+    q_lens = rng.integers(1, Q + 1, size=(steps, B)).astype(np.int32)
+    packed = {key: np.zeros((steps,) + case["windows"][key].shape[1:], dtype=np.uint16)
+              for key in WINDOW_KEYS}
+    qsl = np.zeros((steps, B + 1), dtype=np.int32)
+    for s in range(steps):
+        w = int(case["window_of_step"][s])
+        step = {key: case["windows"][key][w] for key in WINDOW_KEYS}
+        step.update(B=B, Q=Q)
+        pk = synth.pack_windows(step, q_lens[s])
+        qsl[s] = pk["query_start_loc"]
+        for key in WINDOW_KEYS:
+            packed[key][s, :pk[key].shape[0]] = pk[key]
+    case = dict(case)
+    case["windows"] = packed
+    case["window_of_step"] = np.arange(steps)
+    case["accepted"] = np.minimum(case["accepted"], q_lens)
+    return case, qsl
+
+
+def test_decode_loop_variable_windows():
+    """The deferred loop with each step's windows of 1..Q tokens."""
+    import torch
+    B, H, Q, steps = 12, 3, 6, 9
+    case = synth.decode_loop_case(B=B, H=H, Q=Q, slots=2 * B + 4, steps=steps, seed=77,
+                                  padding_frac=0.15, eager_frac=0.2)
+    case, qsl = _varlen_steps(case, 78)
+    ref_outs, finals = ko.decode_stock(
+        windows=case["windows"], window_of_step=case["window_of_step"],
+        accepted=case["accepted"], A_log=case["A_log"], dt_bias=case["dt_bias"],
+        lower_bound=case["lower_bound"], q_scale=case["q_scale"], state=case["state"],
+        state_slots=case["state_slots"], B=B, H=H, Q=Q, query_start_loc=qsl)
+    d = tu.device_case(case)
+    win = {key: tu.to_torch(case["windows"][key], "cuda") for key in WINDOW_KEYS}
+    dq = tu.to_torch(qsl, "cuda")
+    accepted = tu.to_torch(case["accepted"], "cuda")
+    eager = tu.to_torch(case["eager"], "cuda")
+    loop = _loop(case, d)
+    for s in range(steps):
+        out = torch.zeros((B * Q, H, 128), dtype=torch.bfloat16, device="cuda")
+        loop.verify(*(win[key][s] for key in WINDOW_KEYS), out, query_start_loc=dq[s])
+        loop.accept(accepted[s].clone(), eager[s])
+        if (s + 1) % 4 == 0 or s == steps - 1:
+            loop.flush()
+        torch.cuda.synchronize()
+        got = tu.to_numpy(out)
+        n_tok = int(qsl[s, -1])
+        tu.assert_out_close(got[:n_tok], ko.f64_to_bf16(ref_outs[s][:n_tok]), what=f"step {s}")
+        assert not got[n_tok:].any()  # rows past the windows are never written
+    assert int(tu.to_numpy(d["status"])[0]) == 0
+    pool = tu.to_numpy(d["state"])
+    for (b, h), S in finals.items():
+        tu.assert_state_close(pool[case["state_slots"][b], h], S, what=f"item {(b, h)}")

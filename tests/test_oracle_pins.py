@@ -800,3 +800,15 @@ def test_gated_norm_closed_form_and_scale_invariance():
     minus_inf = np.full(gate.shape, 0xFF80, dtype=np.uint16)
     z = ko.layer_epilogue(o=o, gate=minus_inf, norm_weight=w, eps=1e-6)
     assert not np.any(ko.bf16_to_f64(z))
+
+
+def test_decode_stock_uniform_windows_through_query_start_loc():
+    case = _decode_case(padding_frac=0.2)
+    B, Q, steps = case["B"], case["Q"], case["steps"]
+    qsl = np.tile(np.arange(B + 1, dtype=np.int32) * Q, (steps, 1))
+    a_outs, a_fin = _stock(case)
+    b_outs, b_fin = _stock(case, query_start_loc=qsl)
+    np.testing.assert_array_equal(a_outs, b_outs)
+    assert a_fin.keys() == b_fin.keys()
+    for key in a_fin:
+        np.testing.assert_array_equal(a_fin[key], b_fin[key])
