@@ -20,14 +20,14 @@ int launch_step_q5(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q6(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q7(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q8(const StepParams &, int, int, int, cudaStream_t);
-int launch_step_varlen_q1(const StepParams &, int, int, cudaStream_t);
-int launch_step_varlen_q2(const StepParams &, int, int, cudaStream_t);
-int launch_step_varlen_q3(const StepParams &, int, int, cudaStream_t);
-int launch_step_varlen_q4(const StepParams &, int, int, cudaStream_t);
-int launch_step_varlen_q5(const StepParams &, int, int, cudaStream_t);
-int launch_step_varlen_q6(const StepParams &, int, int, cudaStream_t);
-int launch_step_varlen_q7(const StepParams &, int, int, cudaStream_t);
-int launch_step_varlen_q8(const StepParams &, int, int, cudaStream_t);
+int launch_step_varlen_q1(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_varlen_q2(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_varlen_q3(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_varlen_q4(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_varlen_q5(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_varlen_q6(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_varlen_q7(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_varlen_q8(const StepParams &, int, int, int, cudaStream_t);
 
 namespace {
 std::atomic<int> g_sm_count[64];
@@ -46,18 +46,17 @@ int device_sm_count(int dev) {
 
 int launch_step(const StepParams &p, int n_items, int Q, int variant, int split,
                 cudaStream_t stream) {
-  // windows from query_start_loc on the persistent kernel: its own instances
-  // (the cluster split reads the windows at run time)
-  if (p.qsl != nullptr && split == 1) {
+  // windows from query_start_loc: instances of their own
+  if (p.qsl != nullptr) {
     switch (Q) {
-      case 1: return launch_step_varlen_q1(p, n_items, variant, stream);
-      case 2: return launch_step_varlen_q2(p, n_items, variant, stream);
-      case 3: return launch_step_varlen_q3(p, n_items, variant, stream);
-      case 4: return launch_step_varlen_q4(p, n_items, variant, stream);
-      case 5: return launch_step_varlen_q5(p, n_items, variant, stream);
-      case 6: return launch_step_varlen_q6(p, n_items, variant, stream);
-      case 7: return launch_step_varlen_q7(p, n_items, variant, stream);
-      case 8: return launch_step_varlen_q8(p, n_items, variant, stream);
+      case 1: return launch_step_varlen_q1(p, n_items, variant, split, stream);
+      case 2: return launch_step_varlen_q2(p, n_items, variant, split, stream);
+      case 3: return launch_step_varlen_q3(p, n_items, variant, split, stream);
+      case 4: return launch_step_varlen_q4(p, n_items, variant, split, stream);
+      case 5: return launch_step_varlen_q5(p, n_items, variant, split, stream);
+      case 6: return launch_step_varlen_q6(p, n_items, variant, split, stream);
+      case 7: return launch_step_varlen_q7(p, n_items, variant, split, stream);
+      case 8: return launch_step_varlen_q8(p, n_items, variant, split, stream);
       default: return KDA_ERR_ARG;
     }
   }

@@ -67,7 +67,7 @@ __device__ __forceinline__ bool window_ok(const StepParams &p, int q0, int q1, i
   return q0 >= 0 && q1 >= q0 && q1 <= p.n_tokens && q1 - q0 <= Q;
 }
 
-template <bool REPLAY, bool BOUNDARY>
+template <bool REPLAY, bool BOUNDARY, bool VARLEN>
 __device__ __forceinline__ ItemMeta item_meta(const StepParams &p, int item, int Q,
                                               bool report_errors) {
   ItemMeta it;
@@ -81,7 +81,7 @@ __device__ __forceinline__ ItemMeta item_meta(const StepParams &p, int item, int
   it.slot = slot > p.null_slot ? slot : -1;
   it.tok0 = it.b * Q;
   it.qb = Q;
-  if (p.qsl != nullptr) {
+  if constexpr (VARLEN) {
     const int q0 = p.qsl[it.b], q1 = p.qsl[it.b + 1];
     if (window_ok(p, q0, q1, Q)) {
       it.tok0 = q0;

@@ -85,7 +85,9 @@ __device__ __forceinline__ void st_peer_f32(float *local, uint32_t rank, float v
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
-template <int Q, int SPLIT, bool BOUNDARY>
+// VARLEN: windows from query_start_loc (p.qsl, non-null), each of q_b <= Q
+// tokens; otherwise request b's window is tokens b*Q .. b*Q + Q - 1.
+template <int Q, int SPLIT, bool BOUNDARY, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_step_cluster(const StepParams p) {
   using Smem = ClusterSmem<Q, SPLIT, BOUNDARY>;
@@ -112,10 +114,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   cluster_arrive_relaxed();  // waited before the first store into a peer
 
-  const ItemMeta it = item_meta<true, BOUNDARY>(p, item, Q, tid == 0 && rank == 0);
-  const long long tok0 = it.tok0;
+  const ItemMeta it = item_meta<true, BOUNDARY, VARLEN>(p, item, Q, tid == 0 && rank == 0);
+  const long long tok0 = VARLEN ? (long long)it.tok0 : (long long)it.b * Q;
+  const int qb = VARLEN ? it.qb : Q;  // window length (Q without VARLEN)
   if (it.slot < 0) {
-    for (int e = tid; e < it.qb * ROWS; e += kThreads) {
+    for (int e = tid; e < qb * ROWS; e += kThreads) {
       const int t = e / ROWS, r = e - t * ROWS;
       p.out[((tok0 + t) * p.H + it.h) * kDim + row0 + r] = 0;
     }
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long off = ((tok0 + t) * p.H + it.h) * kDim + c;
       uint16_t qbits = 0;
       kbits[t] = gbits[t] = 0;
-      if (t < it.qb) {
+      if (t < qb) {
         kbits[t] = p.k[off];
         gbits[t] = p.g[off];
         qbits = p.q[off];
@@ -238,11 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (c < ROWS) {
 #pragma unroll
       for (int t = 0; t < Q; ++t)
-        sm.vv[t][c] = t < it.qb ? bf16_bits_to_f32(p.v[voff + (long long)t * p.H * kDim]) : 0.f;
+        sm.vv[t][c] = t < qb ? bf16_bits_to_f32(p.v[voff + (long long)t * p.H * kDim]) : 0.f;
     }
     if (c < Q)
       sm.beta[c] =
-          c < it.qb ? sigmoidf_fast(bf16_bits_to_f32(p.beta[(tok0 + c) * p.H + it.h])) : 0.f;
+          c < qb ? sigmoidf_fast(bf16_bits_to_f32(p.beta[(tok0 + c) * p.H + it.h])) : 0.f;
   }
   __syncthreads();
 
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (long long)it.h * p.rq * (2 * kDim) + c;
 #pragma unroll
     for (int t = 0; t < Q; ++t) {
-      if (t < it.qb) {
+      if (t < qb) {
         p.kg[kbase + t * 2 * kDim] = kbits[t];
         p.kg[kbase + t * 2 * kDim + kDim] = gbits[t];
       }
@@ -397,14 +400,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       float o = sm.dots[Q + t][r] * sm.scal[Q + t];
 #pragma unroll
       for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sm.scal[2 * Q + t * Q + s2], uu[s2], o);
-      if (t < it.qb) p.out[((tok0 + t) * p.H + it.h) * kDim + row] = f32_to_bf16_bits(o);
+      if (t < qb) p.out[((tok0 + t) * p.H + it.h) * kDim + row] = f32_to_bf16_bits(o);
     }
     if (it.rec >= 0) {
       const long long cbase = (long long)it.rec * p.corr_row_stride +
                               (long long)it.h * p.rq * kDim + row;
 #pragma unroll
       for (int t = 0; t < Q; ++t)
-        if (t < it.qb) p.corr[cbase + t * kDim] = uu[t];
+        if (t < qb) p.corr[cbase + t * kDim] = uu[t];
     }
   }
 }

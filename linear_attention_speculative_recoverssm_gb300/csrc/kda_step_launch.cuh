@@ -75,9 +75,9 @@ int launch_ws(const StepParams &p, int n_items, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-template <int Q, int SPLIT, bool BOUNDARY>
+template <int Q, int SPLIT, bool BOUNDARY, bool VARLEN>
 int launch_cluster(const StepParams &p, int n_items, cudaStream_t stream) {
-  auto kern = kda_step_cluster<Q, SPLIT, BOUNDARY>;
+  auto kern = kda_step_cluster<Q, SPLIT, BOUNDARY, VARLEN>;
   constexpr size_t smem = sizeof(ClusterSmem<Q, SPLIT, BOUNDARY>);
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -118,21 +118,22 @@ int launch_ws_variant(const StepParams &p, int n_items, int variant, cudaStream_
   }
 }
 
-// Uniform windows (split 1: the persistent kernel; 2 or 4: the cluster
-// split, which also serves windows from query_start_loc).
-template <int Q>
+// One window kind (VARLEN: windows from query_start_loc; its instances live
+// in kda_step_varlen_q<Q>.cu, the uniform ones in kda_step_q<Q>.cu).  Split
+// 1 is the persistent kernel; 2 or 4 the cluster split, which serves the
+// fused FP32 replay + verify.
+template <int Q, bool VARLEN>
 int launch_step_q(const StepParams &p, int n_items, int variant, int split,
                   cudaStream_t stream) {
-  if (split == 1) return launch_ws_variant<Q, false>(p, n_items, variant, stream);
-  // the cluster split serves the fused FP32 replay + verify
+  if (split == 1) return launch_ws_variant<Q, VARLEN>(p, n_items, variant, stream);
   if (variant != 2 && variant != 3) return KDA_ERR_UNSUPPORTED;
   const bool bnd = variant == 3;
   if (split == 2)
-    return bnd ? launch_cluster<Q, 2, true>(p, n_items, stream)
-               : launch_cluster<Q, 2, false>(p, n_items, stream);
+    return bnd ? launch_cluster<Q, 2, true, VARLEN>(p, n_items, stream)
+               : launch_cluster<Q, 2, false, VARLEN>(p, n_items, stream);
   if (split == 4)
-    return bnd ? launch_cluster<Q, 4, true>(p, n_items, stream)
-               : launch_cluster<Q, 4, false>(p, n_items, stream);
+    return bnd ? launch_cluster<Q, 4, true, VARLEN>(p, n_items, stream)
+               : launch_cluster<Q, 4, false, VARLEN>(p, n_items, stream);
   return KDA_ERR_ARG;
 }
 

@@ -4,6 +4,6 @@
 namespace kda {
 int launch_step_q2(const StepParams &p, int n_items, int variant, int split,
                     cudaStream_t stream) {
-  return launch_step_q<2>(p, n_items, variant, split, stream);
+  return launch_step_q<2, false>(p, n_items, variant, split, stream);
 }
 }  // namespace kda

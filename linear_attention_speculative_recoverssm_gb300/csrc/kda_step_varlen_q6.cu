@@ -1,9 +1,9 @@
-// Persistent step kernels for windows of at most 6 token(s) given by
-// query_start_loc.
+// Step kernels for windows of at most 6 token(s) given by query_start_loc.
 #include "kda_step_launch.cuh"
 
 namespace kda {
-int launch_step_varlen_q6(const StepParams &p, int n_items, int variant, cudaStream_t stream) {
-  return launch_ws_variant<6, true>(p, n_items, variant, stream);
+int launch_step_varlen_q6(const StepParams &p, int n_items, int variant, int split,
+                           cudaStream_t stream) {
+  return launch_step_q<6, true>(p, n_items, variant, split, stream);
 }
 }  // namespace kda
