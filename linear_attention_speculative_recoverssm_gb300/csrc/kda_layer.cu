@@ -45,7 +45,7 @@ constexpr int kConvCtas = 8;  // CTAs per request
 
 template <int Q>
 __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams p) {
-  __shared__ __align__(16) uint16_t wins[kConvThreads][8 * (kMaxQ + 2)];
+  __shared__ __align__(16) uint16_t wins[kConvThreads * 8 * (kMaxQ + 2)];
   const int b = blockIdx.x;
   const int slot = p.state_slots[b];
   const int rec = p.pending != nullptr ? (p.record_rows != nullptr ? p.record_rows[b] : b) : -1;
@@ -66,64 +66,76 @@ __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams
   const int W = p.rq + 2;
   const int groups = 3 * D / 8;
   const long long tok0 = (long long)b * Q;
-  uint16_t *mine = wins[threadIdx.x];
-  for (int g = blockIdx.y * kConvThreads + threadIdx.x; g < groups;
-       g += kConvCtas * kConvThreads) {
-    const int ch = 8 * g, part = ch / D, hc = ch - part * D;  // hc = h * 128 + c0
-    uint4 xv[Q];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the warp's 32 window blocks lie back to back, as in HBM, so both copies
+  // move 512 contiguous bytes per instruction
+  uint16_t *area = wins + warp * 32 * 8 * (kMaxQ + 2);
+  uint4 *sw = reinterpret_cast<uint4 *>(area);
+  uint16_t *mine = area + lane * 8 * W;
+  for (int base = blockIdx.y * kConvThreads + warp * 32; base < groups;
+       base += kConvCtas * kConvThreads) {  // warp-uniform trip count
+    const int g = base + lane;
+    const bool active = g < groups;
+    const int nvec = (groups - base < 32 ? groups - base : 32) * W;  // the active lanes' blocks
+    uint4 *gw = reinterpret_cast<uint4 *>(p.conv_state + (long long)slot * p.conv_slot_stride +
+                                          8LL * base * W);
+    for (int j = lane; j < nvec; j += 32) sw[j] = gw[j];
+    __syncwarp();
+    if (active) {
+      const int ch = 8 * g, part = ch / D, hc = ch - part * D;  // hc = h * 128 + c0
+      uint4 xv[Q];
 #pragma unroll
-    for (int t = 0; t < Q; ++t)
-      xv[t] = *reinterpret_cast<const uint4 *>(p.x + (tok0 + t) * (3LL * D) + ch);
-    uint4 wv[4];
+      for (int t = 0; t < Q; ++t)
+        xv[t] = *reinterpret_cast<const uint4 *>(p.x + (tok0 + t) * (3LL * D) + ch);
+      uint4 wv[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      wv[i] = *reinterpret_cast<const uint4 *>(p.conv_w + (long long)(part * 4 + i) * D + hc);
-    uint4 bv = make_uint4(0, 0, 0, 0);
-    if (p.conv_b != nullptr) bv = *reinterpret_cast<const uint4 *>(p.conv_b + ch);
-    uint4 *blk = reinterpret_cast<uint4 *>(p.conv_state + (long long)slot * p.conv_slot_stride +
-                                           (long long)ch * W);
-    uint4 *sv = reinterpret_cast<uint4 *>(mine);
-    for (int e = 0; e < W; ++e) sv[e] = blk[e];
-    const uint16_t *xh[Q];
+      for (int i = 0; i < 4; ++i)
+        wv[i] = *reinterpret_cast<const uint4 *>(p.conv_w + (long long)(part * 4 + i) * D + hc);
+      uint4 bv = make_uint4(0, 0, 0, 0);
+      if (p.conv_b != nullptr) bv = *reinterpret_cast<const uint4 *>(p.conv_b + ch);
+      const uint16_t *xh[Q];
 #pragma unroll
-    for (int t = 0; t < Q; ++t) xh[t] = reinterpret_cast<const uint16_t *>(&xv[t]);
-    const uint16_t *wh[4];
+      for (int t = 0; t < Q; ++t) xh[t] = reinterpret_cast<const uint16_t *>(&xv[t]);
+      const uint16_t *wh[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) wh[i] = reinterpret_cast<const uint16_t *>(&wv[i]);
-    const uint16_t *bh = reinterpret_cast<const uint16_t *>(&bv);
-    uint32_t res[Q][4];
+      for (int i = 0; i < 4; ++i) wh[i] = reinterpret_cast<const uint16_t *>(&wv[i]);
+      const uint16_t *bh = reinterpret_cast<const uint16_t *>(&bv);
+      uint32_t res[Q][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint16_t *win = mine + j * W;
-      const uint16_t t0 = win[off], t1 = win[off + 1], t2 = win[off + 2];
-      float seq[Q + 3];
-      seq[0] = bf16_bits_to_f32(t0);
-      seq[1] = bf16_bits_to_f32(t1);
-      seq[2] = bf16_bits_to_f32(t2);
+      for (int j = 0; j < 8; ++j) {
+        uint16_t *win = mine + j * W;
+        const uint16_t t0 = win[off], t1 = win[off + 1], t2 = win[off + 2];
+        float seq[Q + 3];
+        seq[0] = bf16_bits_to_f32(t0);
+        seq[1] = bf16_bits_to_f32(t1);
+        seq[2] = bf16_bits_to_f32(t2);
 #pragma unroll
-      for (int t = 0; t < Q; ++t) seq[3 + t] = bf16_bits_to_f32(xh[t][j]);
-      const float bias = bf16_bits_to_f32(bh[j]);
+        for (int t = 0; t < Q; ++t) seq[3 + t] = bf16_bits_to_f32(xh[t][j]);
+        const float bias = bf16_bits_to_f32(bh[j]);
 #pragma unroll
-      for (int t = 0; t < Q; ++t) {
-        float acc = bias;
+        for (int t = 0; t < Q; ++t) {
+          float acc = bias;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc = fmaf(seq[t + i], bf16_bits_to_f32(wh[i][j]), acc);
-        const uint32_t bits = f32_to_bf16_bits(acc / (1.f + expf(-acc)));
-        if (j & 1) res[t][j >> 1] |= bits << 16;
-        else res[t][j >> 1] = bits;
+          for (int i = 0; i < 4; ++i) acc = fmaf(seq[t + i], bf16_bits_to_f32(wh[i][j]), acc);
+          const uint32_t bits = f32_to_bf16_bits(acc / (1.f + expf(-acc)));
+          if (j & 1) res[t][j >> 1] |= bits << 16;
+          else res[t][j >> 1] = bits;
+        }
+        win[0] = t1;  // entries from 2 + Q on (rq > Q) are kept
+        win[1] = t2;
+#pragma unroll
+        for (int t = 0; t < Q; ++t) win[2 + t] = xh[t][j];
       }
-      win[0] = t1;  // entries from 2 + Q on (rq > Q) are kept
-      win[1] = t2;
+      uint16_t *out = part == 0 ? p.q : (part == 1 ? p.k : p.v);
+      const int h = hc / kDim, c0 = hc - h * kDim;
 #pragma unroll
-      for (int t = 0; t < Q; ++t) win[2 + t] = xh[t][j];
+      for (int t = 0; t < Q; ++t)
+        *reinterpret_cast<uint4 *>(out + ((tok0 + t) * p.H + h) * kDim + c0) =
+            make_uint4(res[t][0], res[t][1], res[t][2], res[t][3]);
     }
-    uint16_t *out = part == 0 ? p.q : (part == 1 ? p.k : p.v);
-    const int h = hc / kDim, c0 = hc - h * kDim;
-#pragma unroll
-    for (int t = 0; t < Q; ++t)
-      *reinterpret_cast<uint4 *>(out + ((tok0 + t) * p.H + h) * kDim + c0) =
-          make_uint4(res[t][0], res[t][1], res[t][2], res[t][3]);
-    for (int e = 0; e < W; ++e) blk[e] = sv[e];
+    __syncwarp();
+    for (int j = lane; j < nvec; j += 32) gw[j] = sw[j];
+    __syncwarp();  // the area is refilled on the next trip
   }
 }
 
