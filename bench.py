@@ -104,7 +104,7 @@ PROFILED = {
     "step": dict(
         sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
                  "kda_step_q8.cu"),
-        sha256="591e88a51bb73e5f0cec8cda69dfcfddb0c9907a711de87ff2e7bb6e73f5cc1e",
+        sha256="0f2b408c77a0780838e294dc7a5892a379b0e60c8f5801831a1ae4df9bfef9f2",
         workload=WORKLOAD,
         bytes_per_launch=(608.2 + 464.2) * 1e6 * 31104 / 7808,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
