@@ -77,22 +77,23 @@ __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams
     const int g = base + lane;
     const bool active = g < groups;
     const int nvec = (groups - base < 32 ? groups - base : 32) * W;  // the active lanes' blocks
+    // this lane's inputs and weights first: they do not wait for the windows
+    const int ch = 8 * (active ? g : base), part = ch / D, hc = ch - part * D;  // hc = h*128 + c0
+    uint4 xv[Q];
+#pragma unroll
+    for (int t = 0; t < Q; ++t)
+      xv[t] = *reinterpret_cast<const uint4 *>(p.x + (tok0 + t) * (3LL * D) + ch);
+    uint4 wv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      wv[i] = *reinterpret_cast<const uint4 *>(p.conv_w + (long long)(part * 4 + i) * D + hc);
+    uint4 bv = make_uint4(0, 0, 0, 0);
+    if (p.conv_b != nullptr) bv = *reinterpret_cast<const uint4 *>(p.conv_b + ch);
     uint4 *gw = reinterpret_cast<uint4 *>(p.conv_state + (long long)slot * p.conv_slot_stride +
                                           8LL * base * W);
     for (int j = lane; j < nvec; j += 32) sw[j] = gw[j];
     __syncwarp();
     if (active) {
-      const int ch = 8 * g, part = ch / D, hc = ch - part * D;  // hc = h * 128 + c0
-      uint4 xv[Q];
-#pragma unroll
-      for (int t = 0; t < Q; ++t)
-        xv[t] = *reinterpret_cast<const uint4 *>(p.x + (tok0 + t) * (3LL * D) + ch);
-      uint4 wv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        wv[i] = *reinterpret_cast<const uint4 *>(p.conv_w + (long long)(part * 4 + i) * D + hc);
-      uint4 bv = make_uint4(0, 0, 0, 0);
-      if (p.conv_b != nullptr) bv = *reinterpret_cast<const uint4 *>(p.conv_b + ch);
       const uint16_t *xh[Q];
 #pragma unroll
       for (int t = 0; t < Q; ++t) xh[t] = reinterpret_cast<const uint16_t *>(&xv[t]);
@@ -204,33 +205,45 @@ __global__ void __launch_bounds__(256) kda_layer_gate(const LayerParams p, int Q
   }
 }
 
-// One warp per (token, head) row of 128 outputs, 4 per lane:
+// Half a warp per (token, head) row of 128 outputs, 8 per lane (16-byte
+// accesses; two rows per warp):
 // out = BF16(o * rsqrt(mean(o^2) + eps) * w * sigmoid(gate)).
 __global__ void __launch_bounds__(256) kda_layer_epilogue(const uint16_t *__restrict__ o,
                                                           const uint16_t *__restrict__ gate,
                                                           const float *__restrict__ w, float eps,
                                                           uint16_t *__restrict__ out, long long rows) {
-  const long long r = blockIdx.x * 8LL + (threadIdx.x >> 5);
-  if (r >= rows) return;
   const int lane = threadIdx.x & 31;
-  const long long base = r * kDim + 4 * lane;
-  const uint2 ob = *reinterpret_cast<const uint2 *>(o + base);
-  const uint2 gb = *reinterpret_cast<const uint2 *>(gate + base);
-  const float4 w4 = *reinterpret_cast<const float4 *>(w + 4 * lane);
-  const float ov[4] = {__uint_as_float(ob.x << 16), __uint_as_float(ob.x & 0xffff0000u),
-                       __uint_as_float(ob.y << 16), __uint_as_float(ob.y & 0xffff0000u)};
-  const float gv[4] = {__uint_as_float(gb.x << 16), __uint_as_float(gb.x & 0xffff0000u),
-                       __uint_as_float(gb.y << 16), __uint_as_float(gb.y & 0xffff0000u)};
-  const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
-  float ss = (ov[0] * ov[0] + ov[1] * ov[1]) + (ov[2] * ov[2] + ov[3] * ov[3]);
+  const long long r = (blockIdx.x * 8LL + (threadIdx.x >> 5)) * 2 + (lane >> 4);
+  const bool valid = r < rows;
+  const long long base = (valid ? r : 0) * kDim + 8 * (lane & 15);
+  const uint4 ob = *reinterpret_cast<const uint4 *>(o + base);
+  const uint4 gb = *reinterpret_cast<const uint4 *>(gate + base);
+  const float4 wa = *reinterpret_cast<const float4 *>(w + 8 * (lane & 15));
+  const float4 wb = *reinterpret_cast<const float4 *>(w + 8 * (lane & 15) + 4);
+  const uint32_t op[4] = {ob.x, ob.y, ob.z, ob.w}, gp[4] = {gb.x, gb.y, gb.z, gb.w};
+  const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+  float ov[8], gv[8];
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+  for (int i = 0; i < 4; ++i) {
+    ov[2 * i] = __uint_as_float(op[i] << 16);
+    ov[2 * i + 1] = __uint_as_float(op[i] & 0xffff0000u);
+    gv[2 * i] = __uint_as_float(gp[i] << 16);
+    gv[2 * i + 1] = __uint_as_float(gp[i] & 0xffff0000u);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss = fmaf(ov[i], ov[i], ss);
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);  // within the half
   const float rstd = 1.f / sqrtf(ss * (1.f / kDim) + eps);
-  float res[4];
+  uint32_t res[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) res[i] = ov[i] * rstd * wv[i] * (1.f / (1.f + expf(-gv[i])));
-  *reinterpret_cast<uint2 *>(out + base) =
-      make_uint2(pack_bf16x2(res[0], res[1]), pack_bf16x2(res[2], res[3]));
+  for (int i = 0; i < 4; ++i) {
+    const float a = ov[2 * i] * rstd * wv[2 * i] * (1.f / (1.f + expf(-gv[2 * i])));
+    const float c = ov[2 * i + 1] * rstd * wv[2 * i + 1] * (1.f / (1.f + expf(-gv[2 * i + 1])));
+    res[i] = pack_bf16x2(a, c);
+  }
+  if (valid) *reinterpret_cast<uint4 *>(out + base) = make_uint4(res[0], res[1], res[2], res[3]);
 }
 
 template <int Q>
@@ -316,7 +329,7 @@ int kda_layer_epilogue(const kda_bf16 *o, const kda_bf16 *gate, const float *nor
       !kda::aligned16(out))
     return KDA_ERR_ALIGN;
   const long long rows = (long long)n_tokens * H;
-  const long long blocks = (rows + 7) / 8;
+  const long long blocks = (rows + 15) / 16;  // 16 rows per block of 8 warps
   if (blocks > 0x7fffffffLL) return KDA_ERR_ARG;
   kda::kda_layer_epilogue<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       o, gate, norm_weight, eps, out, rows);
