@@ -118,7 +118,9 @@ __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams
           float acc = bias;
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc = fmaf(seq[t + i], bf16_bits_to_f32(wh[i][j]), acc);
-          const uint32_t bits = f32_to_bf16_bits(acc / (1.f + expf(-acc)));
+          // (the fast exp and divide are good to ~1e-6 relative; the result
+          // is rounded to BF16, 2^-9)
+          const uint32_t bits = f32_to_bf16_bits(__fdividef(acc, 1.f + __expf(-acc)));
           if (j & 1) res[t][j >> 1] |= bits << 16;
           else res[t][j >> 1] = bits;
         }
