@@ -238,11 +238,13 @@ __global__ void __launch_bounds__(256) kda_layer_epilogue(const uint16_t *__rest
 #pragma unroll
   for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);  // within the half
   const float rstd = 1.f / sqrtf(ss * (1.f / kDim) + eps);
+  // (the fast exp and divide are good to ~1e-6 relative; the result is BF16)
   uint32_t res[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float a = ov[2 * i] * rstd * wv[2 * i] * (1.f / (1.f + expf(-gv[2 * i])));
-    const float c = ov[2 * i + 1] * rstd * wv[2 * i + 1] * (1.f / (1.f + expf(-gv[2 * i + 1])));
+    const float a = ov[2 * i] * rstd * wv[2 * i] * __fdividef(1.f, 1.f + __expf(-gv[2 * i]));
+    const float c =
+        ov[2 * i + 1] * rstd * wv[2 * i + 1] * __fdividef(1.f, 1.f + __expf(-gv[2 * i + 1]));
     res[i] = pack_bf16x2(a, c);
   }
   if (valid) *reinterpret_cast<uint4 *>(out + base) = make_uint4(res[0], res[1], res[2], res[3]);
