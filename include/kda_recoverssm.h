@@ -261,7 +261,8 @@ int kda_selftest_wait_timeout(int32_t *status, void *stream);
  * Inert requests are skipped (nothing read or written; the step writes
  * their zero outputs); a slot >= n_slots is reported as KDA_ERR_ARG in
  * status and skipped.  The sums run in FP32 (the convolution in tap order,
- * the projection in column order) and round once to BF16.
+ * the projection on the tensor cores, in their order) and round once to
+ * BF16.
  *
  *   x             [B*Q, 3*D] BF16 (q | k | v channels before the convolution)
  *   conv_weight   [3, 4, D] BF16 (tap 3 multiplies the current token)
@@ -270,7 +271,8 @@ int kda_selftest_wait_timeout(int32_t *status, void *stream);
  *                 elements (>= 3*D*(rq+2), a multiple of 8); 16-byte
  *                 aligned; read and rewritten
  *   f_a           [B*Q, 128] BF16;  f_b [D, 128] BF16, 16-byte aligned
- *   q, k, v, raw_g  [B*Q, H, 128] BF16 outputs (the step's inputs)
+ *   q, k, v, raw_g  [B*Q, H, 128] BF16 outputs (the step's inputs), 16-byte
+ *                 aligned
  *   pending       [n_rows] int32 or NULL (no replay pending: off = 0)
  *   1 <= Q <= rq <= 8.
  */

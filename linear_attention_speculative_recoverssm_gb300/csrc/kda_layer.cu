@@ -5,7 +5,11 @@
 // the step: the prologue turns the layer's packed projections into the
 // step's q, k, v (the convolution kernel) and raw gates (the projection
 // kernel), and the epilogue normalises its outputs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "../../include/kda_recoverssm.h"
 #include "kda_device.cuh"
@@ -15,7 +19,6 @@ namespace kda {
 namespace {
 
 constexpr int kConvThreads = 128;  // threads of a convolution CTA
-constexpr int kGateTokens = 128;   // tokens per gate-projection CTA (8 warps x 16)
 
 struct LayerParams {
   const uint16_t *x;       // [B*Q, 3*D] q | k | v channels before the convolution
@@ -142,68 +145,202 @@ __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams
   }
 }
 
-// D[16 x 8] += A[16 x 16] . B[16 x 8]: BF16 operands, FP32 accumulation
-// (mma.sync m16n8k16, A row-major, B column-major).
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               uint32_t b0, uint32_t b1) {
+// ---------------------------------------------------------------------------
+// The gate projection on the fifth-generation tensor cores
+// ---------------------------------------------------------------------------
+// raw_g[t, h, f] = BF16(sum_j f_b[h*128 + f, j] f_a[t, j]) is a [T x 128] by
+// [128 x D] product (D = H*128) whose K is only 128.  One CTA per (128
+// tokens, head) tile:
+//  * thread 0 brings the tile's A (128 f_a rows) and B (the head's 128 f_b
+//    rows) into shared memory with four tensor copies, each 64 K-elements
+//    wide, in the 128-byte swizzled K-major layout (rows of 128 bytes,
+//    8-row groups 1024 bytes apart);
+//  * thread 0 then issues the eight K = 16 steps of one M = N = 128 BF16 MMA
+//    (tcgen05.mma, FP32 accumulation) into a 128-column TMEM accumulator and
+//    commits them to an mbarrier;
+//  * the four warps read the accumulator back (warp w owns TMEM lanes, i.e.
+//    tokens, 32 w .. 32 w + 31; 32 columns per load), round to BF16 and
+//    store 64 contiguous bytes per thread and load.
+// Tokens past the activations (zero rows from the tensor copy) and tokens
+// of inert requests are not written.  Every wait is bounded; the TMEM
+// columns are released on every path.
+
+constexpr int kGateTile = 128;   // tokens (M) and features (N) of a CTA's tile
+constexpr int kGateKBlock = 64;  // BF16 elements per 128-byte swizzled row
+constexpr uint32_t kGateBlockBytes = kGateTile * kGateKBlock * 2;  // 16 KB
+constexpr uint32_t kGateSmem = 4 * kGateBlockBytes + 1024;  // A0 A1 B0 B1 + alignment slack
+constexpr uint32_t kGateTmemCols = 128;  // FP32 accumulator columns (power of 2, >= 32)
+// Instruction descriptor of kind::f16: FP32 accumulator (bits 4-5 = 1), A
+// and B BF16 (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
+// at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kGateIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(kGateTile >> 3) << 17) |
+                                ((uint32_t)(kGateTile >> 4) << 24);
+
+// Tensor maps of f_a [T, 128] and f_b [D, 128] as 2-D BF16 tensors with a
+// (64, 128) box and the 128-byte swizzle.
+struct GateMaps {
+  CUtensorMap a, b;
+};
+
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
-// The gate projection raw_g[t, h, f] = BF16(sum_j f_b[h*128 + f, j] f_a[t, j])
-// on the tensor cores: one CTA per (128 tokens, head).  The head's f_b block
-// (128 features x 128 k, BF16) is staged once in shared memory with rows
-// padded by 16 bytes, so the 8 rows a B fragment spans fall in distinct
-// banks.  Warp w takes tokens 16 w .. 16 w + 15: their f_a rows are the A
-// fragments of all 8 k-steps, held in registers; the warp then walks the
-// 16 feature tiles of 8.  Tokens of inert requests are not written.
-constexpr int kGateRow = kDim + 8;  // padded f_b row in shared memory (BF16)
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout: start address >> 4 (bits 0-13), leading byte offset
+// (bits 16-29; not used by swizzled K-major operands), stride byte offset
+// 1024 >> 4 between 8-row groups (bits 32-45), the fixed 0b001 at bits
+// 46-48, swizzle mode 2 = 128 bytes (bits 61-63).  The 1024-byte aligned
+// tile base keeps the base-offset field at 0; a K step inside the 128-byte
+// row advances the start address by its 32 bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
 
-__global__ void __launch_bounds__(256) kda_layer_gate(const LayerParams p, int Q, int n_tokens) {
-  __shared__ __align__(16) uint16_t fbs[kDim * kGateRow];
-  const int h = blockIdx.y;
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[M x K] . B[N x K]^T for one K = 16 step.
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread issued has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 consecutive FP32 columns of this warp's 32 TMEM lanes, one lane per
+// thread; waits for the load.
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(128) kda_layer_gate(const LayerParams p,
+                                                      const __grid_constant__ GateMaps maps,
+                                                      int Q, int n_tokens) {
+  extern __shared__ uint8_t gate_raw[];
+  __shared__ uint64_t bars[2];  // [0]: tensor copies landed, [1]: MMAs done
+  __shared__ uint32_t tmem_slot;
+  __shared__ int copy_failed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = lane >> 2, tig = lane & 3;
-  {
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.f_b + (long long)h * kDim * kDim);
-    for (int e = threadIdx.x; e < kDim * kDim / 8; e += 256) {
-      const int row = e >> 4, col8 = e & 15;
-      *reinterpret_cast<uint4 *>(fbs + row * kGateRow + col8 * 8) = __ldg(src + e);
+  const int m0 = blockIdx.x * kGateTile, h = blockIdx.y;
+  // the four 16 KB blocks A0 A1 B0 B1 from a 1024-byte aligned base
+  const uint32_t pad = (1024u - (smem_u32(gate_raw) & 1023u)) & 1023u;
+  uint8_t *tiles = gate_raw + pad;
+  const uint32_t tiles_s = smem_u32(tiles);
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    copy_failed = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(&tmem_slot, kGateTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bars[0], 4 * kGateBlockBytes);
+    tma_load_2d(tiles, &maps.a, 0, m0, &bars[0]);
+    tma_load_2d(tiles + kGateBlockBytes, &maps.a, kGateKBlock, m0, &bars[0]);
+    tma_load_2d(tiles + 2 * kGateBlockBytes, &maps.b, 0, h * kGateTile, &bars[0]);
+    tma_load_2d(tiles + 3 * kGateBlockBytes, &maps.b, kGateKBlock, h * kGateTile, &bars[0]);
+    if (mbar_wait_bounded(&bars[0], 0)) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < kDim / 16; ++ks) {
+        // K step ks: 32 bytes into the 128-byte rows of k-block ks / 4
+        const uint32_t off = (uint32_t)(ks >> 2) * kGateBlockBytes + (uint32_t)(ks & 3) * 32u;
+        umma_bf16(tmem, umma_desc_sw128(tiles_s + off),
+                  umma_desc_sw128(tiles_s + 2 * kGateBlockBytes + off), kGateIdesc, ks > 0);
+      }
+      umma_commit(&bars[1]);
+    } else {
+      copy_failed = 1;
+      report(p.status, KDA_ERR_TIMEOUT);
+      mbar_arrive(&bars[1]);  // release the other threads without an accumulator
     }
   }
-  __syncthreads();
-  const int row0 = blockIdx.x * kGateTokens + warp * 16;
-  if (row0 >= n_tokens) return;
-  const int ra = row0 + grp, rb = row0 + grp + 8;
-  const bool va = ra < n_tokens, vb = rb < n_tokens;
-  const uint32_t *fa_a = reinterpret_cast<const uint32_t *>(p.f_a + (long long)(va ? ra : row0) * kDim);
-  const uint32_t *fa_b = reinterpret_cast<const uint32_t *>(p.f_a + (long long)(vb ? rb : row0) * kDim);
-  uint32_t a[8][4];
+  const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[1], 0));
+  tc_fence_after();
+  if (!done) {
+    if (lane == 0) report(p.status, KDA_ERR_TIMEOUT);
+  } else if (!copy_failed) {
+    const int t = m0 + warp * 32 + lane;
+    bool live = t < n_tokens;
+    if (live) {
+      const int s = p.state_slots[t / Q];
+      live = s > p.null_slot && s < p.n_slots;
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(p.g + ((long long)(live ? t : 0) * p.H + h) * kDim);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    a[ks][0] = fa_a[ks * 8 + tig];
-    a[ks][1] = fa_b[ks * 8 + tig];
-    a[ks][2] = fa_a[ks * 8 + 4 + tig];
-    a[ks][3] = fa_b[ks * 8 + 4 + tig];
+    for (int c = 0; c < kGateTile / 32; ++c) {
+      uint32_t r[32];
+      tmem_load32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[c * 4 + i] = make_uint4(
+              pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+              pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+              pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+              pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+      }
+    }
   }
-  const auto live = [&](int row) {
-    const int s = p.state_slots[row / Q];
-    return s > p.null_slot && s < p.n_slots;
-  };
-  const bool la = va && live(ra), lb = vb && live(rb);
-  uint16_t *ga = p.g + ((long long)ra * p.H + h) * kDim + 2 * tig;
-  uint16_t *gb = p.g + ((long long)rb * p.H + h) * kDim + 2 * tig;
-#pragma unroll 4
-  for (int nt = 0; nt < kDim / 8; ++nt) {
-    const uint32_t *fb = reinterpret_cast<const uint32_t *>(fbs + (nt * 8 + grp) * kGateRow);
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) mma_bf16_16816(d, a[ks], fb[ks * 8 + tig], fb[ks * 8 + 4 + tig]);
-    if (la) *reinterpret_cast<uint32_t *>(ga + nt * 8) = pack_bf16x2(d[0], d[1]);
-    if (lb) *reinterpret_cast<uint32_t *>(gb + nt * 8) = pack_bf16x2(d[2], d[3]);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kGateTmemCols);
   }
 }
 
@@ -250,12 +387,60 @@ __global__ void __launch_bounds__(256) kda_layer_epilogue(const uint16_t *__rest
   if (valid) *reinterpret_cast<uint4 *>(out + base) = make_uint4(res[0], res[1], res[2], res[3]);
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 gate_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// f_a [n_tokens, 128] and f_b [H*128, 128] (BF16, 256-byte rows) with a (64,
+// 128) box in the 128-byte swizzle; rows past the tensor arrive as zeros.
+int encode_gate_maps(const LayerParams &p, int n_tokens, GateMaps &maps) {
+  const auto encode = gate_map_encoder();
+  if (encode == nullptr) return KDA_ERR_CUDA;
+  const cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kGateKBlock, (cuuint32_t)kGateTile};
+  const cuuint32_t estride[2] = {1, 1};
+  const cuuint64_t dims_a[2] = {(cuuint64_t)kDim, (cuuint64_t)n_tokens};
+  const cuuint64_t dims_b[2] = {(cuuint64_t)kDim, (cuuint64_t)p.H * kDim};
+  if (encode(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(p.f_a), dims_a,
+             strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return KDA_ERR_CUDA;
+  if (encode(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(p.f_b), dims_b,
+             strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
 template <int Q>
 int launch_prologue_q(const LayerParams &p, int items, cudaStream_t stream) {
-  kda_layer_conv<Q><<<dim3(p.B, kConvCtas), kConvThreads, 0, stream>>>(p);
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(kda_layer_gate, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGateSmem) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    configured.fetch_or(bit);
+  }
   const int n_tokens = p.B * Q;
-  const dim3 grid((n_tokens + kGateTokens - 1) / kGateTokens, p.H);
-  kda_layer_gate<<<grid, 256, 0, stream>>>(p, Q, n_tokens);
+  GateMaps maps;
+  const int st = encode_gate_maps(p, n_tokens, maps);
+  if (st != KDA_OK) return st;
+  kda_layer_conv<Q><<<dim3(p.B, kConvCtas), kConvThreads, 0, stream>>>(p);
+  const dim3 grid((n_tokens + kGateTile - 1) / kGateTile, p.H);
+  kda_layer_gate<<<grid, 128, kGateSmem, stream>>>(p, maps, Q, n_tokens);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -285,7 +470,8 @@ int kda_layer_prologue(const kda_bf16 *x, const kda_bf16 *conv_weight, const kda
   if (!kda::aligned16(x) || !kda::aligned16(conv_weight) ||
       (conv_bias != nullptr && !kda::aligned16(conv_bias)) || !kda::aligned16(f_a) ||
       !kda::aligned16(f_b) || !kda::aligned16(conv_state) || !kda::aligned16(q) ||
-      !kda::aligned16(k) || !kda::aligned16(v) || conv_slot_stride % 8 != 0)
+      !kda::aligned16(k) || !kda::aligned16(v) || !kda::aligned16(raw_g) ||
+      conv_slot_stride % 8 != 0)
     return KDA_ERR_ALIGN;
   kda::LayerParams p;
   p.x = x;

@@ -124,6 +124,7 @@ def test_layer_host_checks(lib):
     assert pro(stride=100) == _lib.KDA_ERR_ARG     # window smaller than 3 * D * (rq + 2)
     assert pro(x=None) == _lib.KDA_ERR_ARG
     assert pro(fb=A + 2) == _lib.KDA_ERR_ALIGN
+    assert pro(g=A + 8) == _lib.KDA_ERR_ALIGN       # raw gates: 16-byte stores
     assert pro(B=0) == _lib.KDA_OK
     # kda_layer_epilogue(o, gate, w, eps, out, n_tokens, H, stream)
     assert lib.kda_layer_epilogue(A, A, A, -1.0, A, 4, 2, None) == _lib.KDA_ERR_ARG
