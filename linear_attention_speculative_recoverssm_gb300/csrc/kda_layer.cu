@@ -149,27 +149,35 @@ __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams
 // The gate projection on the fifth-generation tensor cores
 // ---------------------------------------------------------------------------
 // raw_g[t, h, f] = BF16(sum_j f_b[h*128 + f, j] f_a[t, j]) is a [T x 128] by
-// [128 x D] product (D = H*128) whose K is only 128.  One CTA per (128
-// tokens, head) tile:
-//  * thread 0 brings the tile's A (128 f_a rows) and B (the head's 128 f_b
-//    rows) into shared memory with four tensor copies, each 64 K-elements
-//    wide, in the 128-byte swizzled K-major layout (rows of 128 bytes,
-//    8-row groups 1024 bytes apart);
-//  * thread 0 then issues the eight K = 16 steps of one M = N = 128 BF16 MMA
-//    (tcgen05.mma, FP32 accumulation) into a 128-column TMEM accumulator and
-//    commits them to an mbarrier;
-//  * the four warps read the accumulator back (warp w owns TMEM lanes, i.e.
-//    tokens, 32 w .. 32 w + 31; 32 columns per load), round to BF16 and
-//    store 64 contiguous bytes per thread and load.
+// [128 x D] product (D = H*128) whose K is only 128.  A unit is one (128
+// tokens, head) tile, units u = m * H + h; a persistent CTA per SM takes
+// units blockIdx.x, blockIdx.x + gridDim.x, ... through a two-stage
+// pipeline, so one unit's read-back overlaps the next unit's copies and MMA:
+//  * warp 4, lane 0 (producer and MMA issuer): brings a unit's A (128 f_a
+//    rows) and B (the head's 128 f_b rows) into a shared stage with four
+//    tensor copies, each 64 K-elements wide, in the 128-byte swizzled
+//    K-major layout (rows of 128 bytes, 8-row groups 1024 bytes apart);
+//    issues the eight K = 16 steps of one M = N = 128 BF16 MMA
+//    (tcgen05.mma, FP32 accumulation) into the stage's 128-column TMEM
+//    accumulator; commits them to "accumulator full" and "stage free", and
+//    refills the stage with the unit two ahead once the MMA has read it;
+//  * warps 0-3 (read-back): warp w reads TMEM lanes (tokens) 32 w .. 32 w +
+//    31 of the accumulator, 32 columns per load, rounds to BF16, stores 64
+//    contiguous bytes per thread and load, and marks the accumulator free.
 // Tokens past the activations (zero rows from the tensor copy) and tokens
 // of inert requests are not written.  Every wait is bounded; the TMEM
 // columns are released on every path.
 
-constexpr int kGateTile = 128;   // tokens (M) and features (N) of a CTA's tile
+constexpr int kGateTile = 128;   // tokens (M) and features (N) of a unit
 constexpr int kGateKBlock = 64;  // BF16 elements per 128-byte swizzled row
+constexpr int kGateStages = 2;   // shared stages and TMEM accumulators
+constexpr int kGateThreads = 160;  // read-back warps 0-3, producer warp 4
 constexpr uint32_t kGateBlockBytes = kGateTile * kGateKBlock * 2;  // 16 KB
-constexpr uint32_t kGateSmem = 4 * kGateBlockBytes + 1024;  // A0 A1 B0 B1 + alignment slack
-constexpr uint32_t kGateTmemCols = 128;  // FP32 accumulator columns (power of 2, >= 32)
+constexpr uint32_t kGateStageBytes = 4 * kGateBlockBytes;          // A0 A1 B0 B1
+constexpr uint32_t kGateSmem = kGateStages * kGateStageBytes + 1024;  // + alignment slack
+// FP32 accumulator columns: 128 per stage (a power of 2, >= 32).  One CTA
+// fits on an SM (129 KB of shared memory), so an allocation never waits.
+constexpr uint32_t kGateTmemCols = kGateStages * kGateTile;
 // Instruction descriptor of kind::f16: FP32 accumulator (bits 4-5 = 1), A
 // and B BF16 (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
 // at bits 17-22, M >> 4 at bits 24-28.
@@ -263,23 +271,29 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(128) kda_layer_gate(const LayerParams p,
-                                                      const __grid_constant__ GateMaps maps,
-                                                      int Q, int n_tokens) {
+__global__ void __launch_bounds__(kGateThreads, 1)
+    kda_layer_gate(const LayerParams p, const __grid_constant__ GateMaps maps, int Q,
+                   int n_tokens, int n_units) {
   extern __shared__ uint8_t gate_raw[];
-  __shared__ uint64_t bars[2];  // [0]: tensor copies landed, [1]: MMAs done
+  __shared__ uint64_t full[kGateStages];        // the stage's copies landed
+  __shared__ uint64_t stage_free[kGateStages];  // the MMA has read the stage
+  __shared__ uint64_t acc_full[kGateStages];    // the accumulator holds its unit
+  __shared__ uint64_t acc_free[kGateStages];    // the read-back warps are done with it
   __shared__ uint32_t tmem_slot;
-  __shared__ int copy_failed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kGateTile, h = blockIdx.y;
-  // the four 16 KB blocks A0 A1 B0 B1 from a 1024-byte aligned base
+  const int n_mine =
+      (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  // the stages from a 1024-byte aligned base
   const uint32_t pad = (1024u - (smem_u32(gate_raw) & 1023u)) & 1023u;
   uint8_t *tiles = gate_raw + pad;
   const uint32_t tiles_s = smem_u32(tiles);
   if (threadIdx.x == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    copy_failed = 0;
+    for (int s = 0; s < kGateStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&stage_free[s], 1);
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_free[s], 4);
+    }
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(&tmem_slot, kGateTmemCols);
@@ -287,53 +301,82 @@ __global__ void __launch_bounds__(128) kda_layer_gate(const LayerParams p,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&bars[0], 4 * kGateBlockBytes);
-    tma_load_2d(tiles, &maps.a, 0, m0, &bars[0]);
-    tma_load_2d(tiles + kGateBlockBytes, &maps.a, kGateKBlock, m0, &bars[0]);
-    tma_load_2d(tiles + 2 * kGateBlockBytes, &maps.b, 0, h * kGateTile, &bars[0]);
-    tma_load_2d(tiles + 3 * kGateBlockBytes, &maps.b, kGateKBlock, h * kGateTile, &bars[0]);
-    if (mbar_wait_bounded(&bars[0], 0)) {
+  if (warp == 4) {
+    if (lane == 0) {
+      const auto load = [&](int i) {
+        const int u = (int)blockIdx.x + i * (int)gridDim.x;
+        const int m0 = (u / p.H) * kGateTile, h = u % p.H;
+        const int s = i & 1;
+        uint8_t *st = tiles + s * kGateStageBytes;
+        mbar_arrive_expect_tx(&full[s], kGateStageBytes);
+        tma_load_2d(st, &maps.a, 0, m0, &full[s]);
+        tma_load_2d(st + kGateBlockBytes, &maps.a, kGateKBlock, m0, &full[s]);
+        tma_load_2d(st + 2 * kGateBlockBytes, &maps.b, 0, h * kGateTile, &full[s]);
+        tma_load_2d(st + 3 * kGateBlockBytes, &maps.b, kGateKBlock, h * kGateTile, &full[s]);
+      };
+      for (int i = 0; i < n_mine && i < kGateStages; ++i) load(i);
+      bool ok = true;
+      for (int i = 0; i < n_mine; ++i) {
+        const int s = i & 1;
+        const uint32_t use = (uint32_t)(i >> 1) & 1u;  // parity of the stage's use
+        ok = mbar_wait_bounded(&full[s], use);
+        if (ok && i >= kGateStages) ok = mbar_wait_bounded(&acc_free[s], use ^ 1u);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a_s = tiles_s + s * kGateStageBytes, b_s = a_s + 2 * kGateBlockBytes;
+#pragma unroll
+        for (int ks = 0; ks < kDim / 16; ++ks) {
+          // K step ks: 32 bytes into the 128-byte rows of k-block ks / 4
+          const uint32_t off = (uint32_t)(ks >> 2) * kGateBlockBytes + (uint32_t)(ks & 3) * 32u;
+          umma_bf16(tmem + (uint32_t)(s * kGateTile), umma_desc_sw128(a_s + off),
+                    umma_desc_sw128(b_s + off), kGateIdesc, ks > 0);
+        }
+        umma_commit(&acc_full[s]);
+        umma_commit(&stage_free[s]);
+        if (i + kGateStages < n_mine) {
+          ok = mbar_wait_bounded(&stage_free[s], use);
+          if (!ok) break;
+          load(i + kGateStages);
+        }
+      }
+      // (a timeout leaves the read-back warps to time out on their own wait)
+      if (!ok) report(p.status, KDA_ERR_TIMEOUT);
+    }
+  } else {
+    for (int i = 0; i < n_mine; ++i) {
+      const int s = i & 1;
+      const bool ok =
+          __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[s], (uint32_t)(i >> 1) & 1u));
+      if (!ok) {
+        if (lane == 0) report(p.status, KDA_ERR_TIMEOUT);
+        break;
+      }
       tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < kDim / 16; ++ks) {
-        // K step ks: 32 bytes into the 128-byte rows of k-block ks / 4
-        const uint32_t off = (uint32_t)(ks >> 2) * kGateBlockBytes + (uint32_t)(ks & 3) * 32u;
-        umma_bf16(tmem, umma_desc_sw128(tiles_s + off),
-                  umma_desc_sw128(tiles_s + 2 * kGateBlockBytes + off), kGateIdesc, ks > 0);
-      }
-      umma_commit(&bars[1]);
-    } else {
-      copy_failed = 1;
-      report(p.status, KDA_ERR_TIMEOUT);
-      mbar_arrive(&bars[1]);  // release the other threads without an accumulator
-    }
-  }
-  const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[1], 0));
-  tc_fence_after();
-  if (!done) {
-    if (lane == 0) report(p.status, KDA_ERR_TIMEOUT);
-  } else if (!copy_failed) {
-    const int t = m0 + warp * 32 + lane;
-    bool live = t < n_tokens;
-    if (live) {
-      const int s = p.state_slots[t / Q];
-      live = s > p.null_slot && s < p.n_slots;
-    }
-    uint4 *dst = reinterpret_cast<uint4 *>(p.g + ((long long)(live ? t : 0) * p.H + h) * kDim);
-#pragma unroll
-    for (int c = 0; c < kGateTile / 32; ++c) {
-      uint32_t r[32];
-      tmem_load32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+      const int u = (int)blockIdx.x + i * (int)gridDim.x;
+      const int t = (u / p.H) * kGateTile + warp * 32 + lane, h = u % p.H;
+      bool live = t < n_tokens;
       if (live) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[c * 4 + i] = make_uint4(
-              pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
-              pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-              pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-              pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+        const int slot = p.state_slots[t / Q];
+        live = slot > p.null_slot && slot < p.n_slots;
       }
+      uint4 *dst = reinterpret_cast<uint4 *>(p.g + ((long long)(live ? t : 0) * p.H + h) * kDim);
+#pragma unroll
+      for (int c = 0; c < kGateTile / 32; ++c) {
+        uint32_t r[32];
+        tmem_load32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(s * kGateTile + c * 32), r);
+        if (live) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[c * 4 + j] = make_uint4(
+                pack_bf16x2(__uint_as_float(r[8 * j]), __uint_as_float(r[8 * j + 1])),
+                pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_free[s]);
     }
   }
   tc_fence_before();
@@ -439,8 +482,11 @@ int launch_prologue_q(const LayerParams &p, int items, cudaStream_t stream) {
   const int st = encode_gate_maps(p, n_tokens, maps);
   if (st != KDA_OK) return st;
   kda_layer_conv<Q><<<dim3(p.B, kConvCtas), kConvThreads, 0, stream>>>(p);
-  const dim3 grid((n_tokens + kGateTile - 1) / kGateTile, p.H);
-  kda_layer_gate<<<grid, 128, kGateSmem, stream>>>(p, maps, Q, n_tokens);
+  const long long units = (long long)((n_tokens + kGateTile - 1) / kGateTile) * p.H;
+  if (units > 0x7fffffffLL) return KDA_ERR_ARG;
+  const int sms = device_sm_count(dev);
+  const int grid = units < sms ? (int)units : sms;
+  kda_layer_gate<<<grid, kGateThreads, kGateSmem, stream>>>(p, maps, Q, n_tokens, (int)units);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
