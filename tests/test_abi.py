@@ -131,3 +131,35 @@ def test_layer_host_checks(lib):
     assert lib.kda_layer_epilogue(A, A, A + 4, 1e-6, A, 4, 2, None) == _lib.KDA_ERR_ALIGN
     assert lib.kda_layer_epilogue(A, A, A, 1e-6, A, 0, 2, None) == _lib.KDA_OK
     assert lib.kda_layer_epilogue(None, A, A, 1e-6, A, 4, 2, None) == _lib.KDA_ERR_ARG
+
+
+def test_missing_library_raises():
+    """The binding has no fallback: without the built library it raises."""
+    with pytest.raises(ImportError):
+        _lib.load(os.path.join(ROOT, "no_such_dir", "libkda_recoverssm.so"))
+
+
+def test_wrong_dtypes_are_rejected_before_any_call(lib):
+    """dtype checks run on the host before the C ABI is reached (CPU tensors:
+    nothing is launched)."""
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import kda_layer_epilogue
+    o = torch.zeros((2, 1, 128), dtype=torch.float32)
+    gate = torch.zeros((2, 128), dtype=torch.bfloat16)
+    w = torch.ones(128, dtype=torch.float32)
+    out = torch.zeros((2, 128), dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        kda_layer_epilogue(o, gate, w, out, eps=1e-6)
+
+
+def test_product_path_never_imports_the_oracle():
+    """The package (the product path) and its CUDA sources never reach the
+    oracle: parity would prove nothing if they did."""
+    pkg = os.path.join(ROOT, "linear_attention_speculative_recoverssm_gb300")
+    pattern = re.compile(r"^\s*(from\s+oracle\b|import\s+oracle\b|from\s+\.\.?oracle)|"
+                         r"#include\s+[<\"].*oracle", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not pattern.search(text), os.path.join(dirpath, f)
