@@ -20,9 +20,10 @@
  *  - K = V = 128 (key and value channels per head).  Other sizes return
  *    KDA_ERR_UNSUPPORTED.
  *  - Every pointer is DEVICE memory owned by the caller.  The library never
- *    allocates, frees or synchronises; each call enqueues its kernels on
- *    `stream` (a cudaStream_t passed as void*, NULL = the legacy default
- *    stream) and returns at once.
+ *    allocates or frees, and only kda_check_status synchronises (with its
+ *    own stream); every other call enqueues its kernels on `stream` (a
+ *    cudaStream_t passed as void*, NULL = the legacy default stream) and
+ *    returns at once.
  *  - BF16 tensors are passed as raw bit patterns (kda_bf16, uint16_t).
  *  - Activations are token-major, [n_tokens, H, 128].  Without
  *    query_start_loc, token b*Q + t is token t of request b's window and
@@ -86,9 +87,22 @@ int kda_abi_version(void);
 const char *kda_error_string(int status);
 
 /*
+ * kda_check_status -- reads back a device status word (the `status`
+ * argument of the other calls).  Enqueues a 4-byte device-to-host copy of
+ * *status on `stream`, waits for that stream, and returns the code it held
+ * (KDA_OK when no kernel reported a problem).  Unlike every other entry
+ * point it synchronises, with `stream` only; it allocates nothing and does
+ * not reset the word.  Returns KDA_ERR_ARG for a NULL status and
+ * KDA_ERR_CUDA if the copy or the wait fails (for instance after an earlier
+ * fault on the stream).
+ */
+int kda_check_status(const int32_t *status, void *stream);
+
+/*
  * kda_verify -- the stock RecoverSSM verify of one window, from the
- * checkpoint, which it never writes ("Verify a KDA speculative window
- * without modifying its checkpoint", kda_recoverssm_verify).
+ * checkpoint; the checkpoint is only read (page
+ * "vllm.models.kimi_k3.nvidia.specialized_decode.recoverssm.kernels",
+ * kda_recoverssm_verify docstring).
  *
  * Per (request b, head h) with slot = state_slots[b] > null_slot and
  * S = state_pool[slot, h] ([V=128 rows, K=128 columns]), for t < Q:
@@ -185,12 +199,21 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
  *                 corrections [rows, H, Q, 128] FP32 and key/gate records
  *                 [rows, H, Q, 256] BF16; each address 16-byte aligned
  *   state_strides, corr_strides, kg_strides  [L] device int64 tables:
- *                 elements per slot / per record row
+ *                 elements per slot / per record row, multiples of 16
+ *                 bytes and at least one slot's / row's extent:
+ *                 state >= H*128*128, corr >= H*Q*128, key/gate >= H*Q*256
  *   A_log [L, H], dt_bias [L, H, 128] FP32
  *   sources, commit_lens, destinations [B] int32
  *   boundaries, boundary_lens [B] int32 or both NULL (align off)
  *   record_rows [B] int32 or NULL
- *   state_dtype KDA_STATE_BF16 or KDA_STATE_F32; 1 <= Q <= 8.
+ *   state_dtype KDA_STATE_BF16 or KDA_STATE_F32; 1 <= Q <= 8;
+ *   -10 <= lower_bound <= 10 (the boundary state divides by a product of
+ *   up to Q decays, which must stay inside FP32; KDA_ERR_UNSUPPORTED
+ *   otherwise).
+ * The per-layer tables are device data, so they are checked by the kernel:
+ * a layer whose address or stride is misaligned (KDA_ERR_ALIGN) or whose
+ * stride is below the minimum or negative (KDA_ERR_ARG) is reported in
+ * status and its items are skipped, never written.
  */
 int kda_commit(const uint64_t *state_ptrs, const uint64_t *corr_ptrs,
                const uint64_t *kg_ptrs, const int64_t *state_strides,

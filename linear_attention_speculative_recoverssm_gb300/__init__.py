@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     KDA_STATE_BF16,
     KDA_STATE_F32,
     KdaError,
+    kda_check_status,
     kda_commit,
     kda_defer_commit,
     kda_flush_plan,

@@ -24,7 +24,8 @@ KDA_ERR_TIMEOUT = -5
 KDA_STATE_F32 = 0
 KDA_STATE_BF16 = 1
 
-EXPORTS = ("kda_abi_version", "kda_error_string", "kda_verify", "kda_replay_verify",
+EXPORTS = ("kda_abi_version", "kda_error_string", "kda_check_status", "kda_verify",
+           "kda_replay_verify",
            "kda_commit", "kda_defer_commit", "kda_flush_plan", "kda_selftest_wait_timeout",
            "kda_layer_prologue", "kda_layer_epilogue")
 
@@ -36,6 +37,7 @@ _F = ctypes.c_float
 _SIGS = {
     "kda_abi_version": ([], _I),
     "kda_error_string": ([_I], ctypes.c_char_p),
+    "kda_check_status": ([_P, _P], _I),
     "kda_verify": ([_P] * 7 + [_F, _F, _P, _I, _I64, _I, _P, _P, _I, _P, _P, _P, _I64, _I64,
                                _I, _I, _P, _I, _I, _I, _I, _P, _P], _I),
     "kda_replay_verify": ([_P] * 7 + [_F, _F, _P, _I64, _I, _P, _P, _I, _P, _P, _P, _P, _I64,
@@ -115,6 +117,15 @@ def _check_step_dtypes(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_slots, re
         _expect(t, torch.float32, name)
     for name, t in (("state_slots", state_slots), ("record_rows", record_rows)):
         _expect(t, torch.int32, name)
+
+
+def kda_check_status(status, *, stream=None):
+    """The code held by the device status word ``status`` (int32 tensor),
+    read back after the work already enqueued on the stream (this call waits
+    for that stream)."""
+    import torch
+    _expect(status, torch.int32, "status")
+    return load().kda_check_status(_ptr(status), _stream(stream))
 
 
 def kda_verify(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, state_slots, corr,

@@ -186,6 +186,17 @@ const char *kda_error_string(int status) {
   }
 }
 
+int kda_check_status(const int32_t *status, void *stream) {
+  if (!status) return KDA_ERR_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  // pageable destination: the copy completes before the call returns
+  if (cudaMemcpyAsync(&host, status, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+  return host;
+}
+
 int kda_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *raw_g,
                const kda_bf16 *raw_beta, const float *A_log, const float *dt_bias,
                float lower_bound, float q_scale, const void *state_pool, int state_dtype,
@@ -261,6 +272,9 @@ int kda_commit(const uint64_t *state_ptrs, const uint64_t *corr_ptrs, const uint
                int L, int H, int B, int Q, int n_slots, int n_rows, int32_t *status,
                void *stream) {
   if (state_dtype != KDA_STATE_F32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_UNSUPPORTED;
+  // the align boundary state divides the partial replay sum by
+  // prod_{m<=s<n} d_s, which must stay inside FP32
+  if (!gate_bound_ok(lower_bound)) return KDA_ERR_UNSUPPORTED;
   if (L < 0 || H < 1 || B < 0 || Q < 1 || Q > KDA_MAX_WINDOW || n_slots < 1 || n_rows < 0)
     return KDA_ERR_ARG;
   if (!state_ptrs || !corr_ptrs || !kg_ptrs || !state_strides || !corr_strides || !kg_strides ||

@@ -158,7 +158,11 @@ __device__ __forceinline__ CommitItem commit_resolve(const CommitParams &p, int 
   it.src = it.dst = it.bnd = it.kg = it.corr = 0;
   it.live = n > 0 && r.src > p.null_slot && r.dst > p.null_slot && r.row >= 0;
   if (!it.live) return it;
-  const bool bad = r.src >= p.n_slots || r.dst >= p.n_slots || r.row >= p.n_rows;
+  // a per-layer stride below one slot's / row's extent (or negative) would
+  // put this item's pages and records outside the layer's pool
+  const bool bad = r.src >= p.n_slots || r.dst >= p.n_slots || r.row >= p.n_rows ||
+                   r.ss < (int64_t)p.H * kDim * kDim || r.cs < (int64_t)p.H * p.Q * kDim ||
+                   r.ks < (int64_t)p.H * p.Q * 2 * kDim;
   const bool misaligned = ((r.sp | r.cp | r.kp) & 15) != 0 ||
                           ((r.ss * (int64_t)sizeof(ST)) & 15) != 0 || ((r.cs * 4) & 15) != 0 ||
                           ((r.ks * 2) & 15) != 0;

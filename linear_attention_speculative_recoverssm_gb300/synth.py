@@ -17,6 +17,10 @@ Distributions (one recipe for every workload):
   dt_bias ~ N(0, 0.1^2) per (head, key channel); lower_bound = -5;
 * records of the previous window: corrections u ~ N(0, 0.5^2) (FP32), keys
   drawn like k, raw gates ~ N(0, 1);
+* test-only option ``key_norms="spread"``: q, k and the recorded keys keep
+  their directions but take per-(token, head) norms spread over 1e-3 .. 1e2
+  (``_KeyDraws``), so a kernel that skipped or mis-indexed a normalisation
+  would be caught;
 * slots: distinct live slots in 1..slots-1 (slot 0 is the null slot),
   record rows a random permutation, counts uniform on their ranges.
 """
@@ -49,10 +53,47 @@ def _unit_directions(rng, shape):
     return x
 
 
+# Norms of the "spread" key draws: log10 |x| ~ U(-2, 2) per (token, head),
+# and a tenth of the vectors near sqrt(1e-6) = 1e-3 (log10 |x| ~ U(-3.5,
+# -2.5)), where the 1e-6 inside the normalisation's root is not negligible.
+SPREAD_LOG10 = (-2.0, 2.0)
+SPREAD_TINY_FRAC = 0.1
+SPREAD_TINY_LOG10 = (-3.5, -2.5)
+
+
+def _norm_factors(rng, lead_shape):
+    """Per-vector norms for the "spread" key draws (see SPREAD_*)."""
+    lg = rng.uniform(*SPREAD_LOG10, size=lead_shape)
+    tiny = rng.random(lead_shape) < SPREAD_TINY_FRAC
+    lg[tiny] = rng.uniform(*SPREAD_TINY_LOG10, size=int(tiny.sum()))
+    return (10.0 ** lg).astype(np.float32)[..., None]
+
+
+class _KeyDraws:
+    """Directions for q, k and the recorded keys: unit vectors (the
+    workloads' recipe), or with ``key_norms="spread"`` the same directions
+    scaled to per-(token, head) norms spread over 1e-3 .. 1e2 (a test-only
+    recipe: the kernels must normalise each vector by its own norm).  The
+    norms come from a generator of their own, so every other draw of a case
+    is the same either way."""
+
+    def __init__(self, key_norms, seed):
+        if key_norms not in ("unit", "spread"):
+            raise ValueError(f"key_norms must be 'unit' or 'spread', not {key_norms!r}")
+        self.spread = key_norms == "spread"
+        self.rng = np.random.default_rng(seed + 2_147_483_629) if self.spread else None
+
+    def __call__(self, rng, shape):
+        x = _unit_directions(rng, shape)
+        if self.spread:
+            x *= _norm_factors(self.rng, shape[:-1])
+        return x
+
+
 def replay_verify_case(*, B, H, Q, slots, seed, RQ=None, rows=None, K=128,
                        V=128, pending_max=None, padding_frac=0.0,
                        no_record_frac=0.0, state_dtype="f32",
-                       boundary_frac=0.0):
+                       boundary_frac=0.0, key_norms="unit"):
     """Operands of one RecoverSSM verify step (replay + verify).
 
     Returns a dict with q, k, v, raw_g [B*Q, H, K|V], raw_beta [B*Q, H] (BF16
@@ -67,6 +108,7 @@ def replay_verify_case(*, B, H, Q, slots, seed, RQ=None, rows=None, K=128,
     pending_max = RQ if pending_max is None else pending_max
     assert rows >= B and Q <= RQ
     rng = np.random.default_rng(seed)
+    keys = _KeyDraws(key_norms, seed)
 
     n_pad = int(round(padding_frac * B))
     order = rng.permutation(B)
@@ -106,8 +148,8 @@ def replay_verify_case(*, B, H, Q, slots, seed, RQ=None, rows=None, K=128,
     del draw
 
     T = B * Q
-    q = _unit_directions(rng, (T, H, K)) * np.float32(K ** -0.5)
-    k = _unit_directions(rng, (T, H, K))
+    q = keys(rng, (T, H, K)) * np.float32(K ** -0.5)
+    k = keys(rng, (T, H, K))
     case = dict(
         q=to_bf16_bits(q),
         k=to_bf16_bits(k),
@@ -122,7 +164,7 @@ def replay_verify_case(*, B, H, Q, slots, seed, RQ=None, rows=None, K=128,
         pending=pending,
         corr=_normal(rng, (rows, H, RQ, V), 0.5),
         key_gate=np.concatenate(
-            [to_bf16_bits(_unit_directions(rng, (rows, H, RQ, K))),
+            [to_bf16_bits(keys(rng, (rows, H, RQ, K))),
              to_bf16_bits(_normal(rng, (rows, H, RQ, K)))], axis=-1),
         boundary_slots=boundary_slots,
         boundary_lens=boundary_lens,
@@ -202,7 +244,7 @@ def layer_case(*, B, H, Q, slots, seed, bias=True, eps=1e-6, **kw):
 
 
 def decode_loop_case(*, B, H, Q, slots, steps, seed, windows=None, K=128, V=128,
-                     padding_frac=0.0, accept_min=0, eager_frac=0.0):
+                     padding_frac=0.0, accept_min=0, eager_frac=0.0, key_norms="unit"):
     """Operands of a multi-step speculative decode of one layer.
 
     The first step's operands are those of ``replay_verify_case`` with every
@@ -218,9 +260,10 @@ def decode_loop_case(*, B, H, Q, slots, steps, seed, windows=None, K=128, V=128,
       deferred, an ``eager_frac`` share of the requests per step.
     """
     case = replay_verify_case(B=B, H=H, Q=Q, slots=slots, seed=seed, K=K, V=V,
-                              padding_frac=padding_frac)
+                              padding_frac=padding_frac, key_norms=key_norms)
     case["pending"][:] = 0
     rng = np.random.default_rng(seed + 7919)
+    draw_keys = _KeyDraws(key_norms, seed + 7919)
     n_win = steps if windows is None else min(windows, steps)
     T = B * Q
     keys = ("q", "k", "v", "raw_g", "raw_beta")
@@ -228,9 +271,9 @@ def decode_loop_case(*, B, H, Q, slots, steps, seed, windows=None, K=128, V=128,
     for key in keys:
         stacks[key][0] = case[key]
     for w in range(1, n_win):
-        q = _unit_directions(rng, (T, H, K)) * np.float32(K ** -0.5)
+        q = draw_keys(rng, (T, H, K)) * np.float32(K ** -0.5)
         stacks["q"][w] = to_bf16_bits(q)
-        stacks["k"][w] = to_bf16_bits(_unit_directions(rng, (T, H, K)))
+        stacks["k"][w] = to_bf16_bits(draw_keys(rng, (T, H, K)))
         stacks["v"][w] = to_bf16_bits(_normal(rng, (T, H, V)))
         stacks["raw_g"][w] = to_bf16_bits(_normal(rng, (T, H, K)))
         stacks["raw_beta"][w] = to_bf16_bits(_normal(rng, (T, H)))
@@ -243,7 +286,7 @@ def decode_loop_case(*, B, H, Q, slots, steps, seed, windows=None, K=128, V=128,
 
 
 def commit_case(*, L, B, H, Q, slots, seed, K=128, V=128, state_dtype="bf16",
-                null_frac=0.10, in_place_frac=0.5, boundary_frac=0.25):
+                null_frac=0.10, in_place_frac=0.5, boundary_frac=0.25, key_norms="unit"):
     """Operands of the standalone commit over L layers.
 
     Per layer: state [slots, H, V, K] (BF16 bits or FP32), corr [B, H, Q, V]
@@ -256,6 +299,7 @@ def commit_case(*, L, B, H, Q, slots, seed, K=128, V=128, state_dtype="bf16",
     m ~ U{1..Q-1} tokens into a fresh boundary slot.
     """
     rng = np.random.default_rng(seed)
+    keys = _KeyDraws(key_norms, seed)
     order = rng.permutation(B)
     n_null = int(round(null_frac * B))
     null_rows = order[:n_null]
@@ -294,7 +338,7 @@ def commit_case(*, L, B, H, Q, slots, seed, K=128, V=128, state_dtype="bf16",
             state[used] = _normal(rng, (len(used), H, V, K), 0.05)
         corr = _normal(rng, (B, H, Q, V), 0.5)
         key_gate = np.concatenate(
-            [to_bf16_bits(_unit_directions(rng, (B, H, Q, K))),
+            [to_bf16_bits(keys(rng, (B, H, Q, K))),
              to_bf16_bits(_normal(rng, (B, H, Q, K)))], axis=-1)
         layers.append(dict(state=state, corr=corr, key_gate=key_gate))
     return dict(

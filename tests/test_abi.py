@@ -104,10 +104,19 @@ def test_commit_and_bookkeeping_host_checks(lib):
     P2[12] = None  # boundaries given without lengths
     assert lib.kda_commit(*P2, 1, -5.0, 0, 1, 2, 2, 2, 4, 2, None, None) == _lib.KDA_ERR_ARG
     assert lib.kda_commit(*P, 1, -5.0, 0, 1, 2, 0, 2, 4, 2, None, None) == _lib.KDA_OK
+    # the gate bound: the boundary state divides by a product of decays
+    assert lib.kda_commit(*P, 1, -11.0, 0, 1, 2, 2, 2, 4, 2, None, None) == \
+        _lib.KDA_ERR_UNSUPPORTED
+    assert lib.kda_commit(*P, 0, float("nan"), 0, 1, 2, 2, 2, 4, 2, None, None) == \
+        _lib.KDA_ERR_UNSUPPORTED
     assert lib.kda_defer_commit(A, A, None, A, None, 2, 0, 2, None, None) == _lib.KDA_ERR_ARG
     assert lib.kda_defer_commit(A, A, A, A, None, 0, 0, 2, None, None) == _lib.KDA_OK
     assert lib.kda_flush_plan(A, A, A, A, A, A, A, 2, 9, 0, 2, None, None) == _lib.KDA_ERR_ARG
     assert lib.kda_flush_plan(A, A, A, A, A, A, A, 0, 4, 0, 2, None, None) == _lib.KDA_OK
+
+
+def test_check_status_rejects_null(lib):
+    assert lib.kda_check_status(None, None) == _lib.KDA_ERR_ARG
 
 
 def test_layer_host_checks(lib):

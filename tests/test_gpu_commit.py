@@ -202,3 +202,54 @@ def test_commit_mostly_dead_back_to_back():
               lower_bound=c["lower_bound"], Q=c["Q"], B=c["B"], H=c["H"],
               boundaries=c["boundaries"], boundary_lens=c["boundary_lens"])
     _compare_pools([tu.to_numpy(s) for s in states], ref_layers, orig)
+
+
+def test_commit_at_the_gate_bound_with_align():
+    """lower_bound = -10, Q = 8, every request committing a full window with a
+    boundary: the boundary state divides the partial replay sum by a product
+    of up to seven decays of e^-10 each."""
+    c = synth.commit_case(L=2, B=24, H=4, Q=8, slots=96, seed=520, state_dtype="f32",
+                          boundary_frac=0.5)
+    c["lower_bound"] = -10.0
+    c["commit_lens"][:] = 8
+    for lay in c["layers"]:
+        lay["key_gate"][..., 128:] = synth.to_bf16_bits(
+            np.full(lay["key_gate"][..., 128:].shape, 30.0, np.float32))
+    got, ref = _commit_both(c, align=True)
+    _compare_pools(got, ref, c["layers"])
+
+
+def test_commit_undersized_layer_stride_is_reported_not_written():
+    """A per-layer stride below one slot's extent (or negative) is caught by
+    the kernel: KDA_ERR_ARG in the status word, that layer's items skipped
+    (its pool bit-identical), the other layers committed as usual."""
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import (KDA_ERR_ARG, KDA_STATE_F32,
+                                                               kda_commit, layer_tables)
+    c = synth.commit_case(L=3, B=16, H=2, Q=4, slots=48, seed=521, state_dtype="f32")
+    dev = "cuda"
+    states = [tu.to_torch(lay["state"], dev) for lay in c["layers"]]
+    corrs = [tu.to_torch(lay["corr"], dev) for lay in c["layers"]]
+    kgs = [tu.to_torch(lay["key_gate"], dev) for lay in c["layers"]]
+    t = lambda a: tu.to_torch(a, dev)
+    for bad_table, bad_value in ((3, 2 * 128 * 128 - 4), (4, -2 * 4 * 128), (5, 16)):
+        tabs = list(layer_tables(states, corrs, kgs, dev))
+        tabs[bad_table][1] = bad_value  # layer 1: state / corr / key-gate stride
+        pools = [s.clone() for s in states]
+        tabs[0] = torch.tensor([p.data_ptr() for p in pools], dtype=torch.int64, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        kda_commit(*tabs, t(c["A_log"]), t(c["dt_bias"]), t(c["sources"]),
+                   t(c["commit_lens"]), t(c["destinations"]), state_dtype=KDA_STATE_F32,
+                   lower_bound=c["lower_bound"], L=3, H=2, B=16, Q=4, n_slots=48,
+                   n_rows=corrs[0].shape[0], boundaries=t(c["boundaries"]),
+                   boundary_lens=t(c["boundary_lens"]), status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == KDA_ERR_ARG
+        np.testing.assert_array_equal(tu.to_numpy(pools[1]), c["layers"][1]["state"])
+        ref_layers = [{k: v.copy() for k, v in lay.items()} for lay in c["layers"]]
+        ko.commit(layers=ref_layers, A_log=c["A_log"], dt_bias=c["dt_bias"],
+                  sources=c["sources"], commit_lens=c["commit_lens"],
+                  destinations=c["destinations"], lower_bound=c["lower_bound"], Q=4, B=16, H=2,
+                  boundaries=c["boundaries"], boundary_lens=c["boundary_lens"])
+        for l in (0, 2):
+            _compare_pools([tu.to_numpy(pools[l])], [ref_layers[l]], [c["layers"][l]])

@@ -344,3 +344,75 @@ def test_mostly_inert_back_to_back():
         tu.gpu_step(case, d, replay=True, split=1)
     torch.cuda.synchronize()
     tu.compare_step(ref, d, before)
+
+
+# --------------------------------------------------------------------------
+# the latency sweep's own shapes: H = 32, B in {1, 4, 16}, q in {1, 2, 4, 8},
+# split in {1, 2, 4} and the automatic choice, every item against the oracle
+# --------------------------------------------------------------------------
+
+_LATENCY_REF = {}
+
+
+def _latency_ref(B, Q):
+    """The oracle's result for one latency-sweep shape (computed once and
+    shared by its four launch shapes)."""
+    if (B, Q) not in _LATENCY_REF:
+        case = synth.latency_case(B=B, Q=Q)
+        ref = tu.copy_case(case)
+        tu.oracle_step(ref, replay=True)
+        _LATENCY_REF[(B, Q)] = (case, ref)
+    return _LATENCY_REF[(B, Q)]
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 0])
+@pytest.mark.parametrize("Q", [1, 2, 4, 8])
+@pytest.mark.parametrize("B", [1, 4, 16])
+def test_latency_sweep_shapes(B, Q, split):
+    case, ref = _latency_ref(B, Q)
+    assert case["H"] == 32 and case["Q"] == Q and case["B"] == B
+    before = tu.copy_case(case)
+    d = tu.device_case(case)
+    tu.gpu_step(case, d, replay=True, split=split)
+    tu.compare_step(ref, d, before)
+
+
+# --------------------------------------------------------------------------
+# numerically extreme gates
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("split", [1, 2, 4])
+def test_boundary_states_at_the_gate_bound(split):
+    """lower_bound = -10 with boundary states: the boundary state is the
+    partial replay sum divided by prod_{m<=s<n} d_s, which reaches e^70 over
+    seven decays while S_0 D_n falls to ~1e-36; every request replays a full
+    record (n = Q = 8), with boundaries after 1..7 tokens."""
+    case = synth.replay_verify_case(B=24, H=4, Q=8, slots=64, seed=330 + split,
+                                    boundary_frac=0.5, padding_frac=0.1)
+    case["lower_bound"] = -10.0
+    case["pending"][:] = 8
+    # saturate the recorded gates towards the strongest decay
+    kg = case["key_gate"]
+    kg[..., 128:] = synth.to_bf16_bits(np.full(kg[..., 128:].shape, 30.0, np.float32))
+    _run_and_compare(case, boundary=True, split=split)
+
+
+@pytest.mark.parametrize("split", [1, 4])
+def test_saturating_gates_and_beta(split):
+    """Raw gates and raw betas with |exp(A_log) (raw_g + dt_bias)| and
+    |raw_beta| around 100: the kernels' sigmoid 1 / (1 + e^-z) overflows its
+    exponential to +inf (giving 0) or underflows it to 0 (giving 1)."""
+    case = synth.replay_verify_case(B=16, H=4, Q=8, slots=24, seed=340 + split)
+    rng = np.random.default_rng(341)
+    a = np.exp(case["A_log"].astype(np.float64))[None, :, None]
+    sign = np.where(rng.random(case["raw_g"].shape) < 0.5, -1.0, 1.0)
+    g = sign * rng.uniform(90.0, 110.0, size=case["raw_g"].shape) / a
+    case["raw_g"] = synth.to_bf16_bits(g.astype(np.float32))
+    kg = case["key_gate"]
+    sign = np.where(rng.random(kg[..., 128:].shape) < 0.5, -1.0, 1.0)
+    g = sign * rng.uniform(90.0, 110.0, size=kg[..., 128:].shape) / a[:, :, None]
+    kg[..., 128:] = synth.to_bf16_bits(g.astype(np.float32))
+    sign = np.where(rng.random(case["raw_beta"].shape) < 0.5, -1.0, 1.0)
+    case["raw_beta"] = synth.to_bf16_bits(
+        (sign * rng.uniform(90.0, 110.0, size=case["raw_beta"].shape)).astype(np.float32))
+    _run_and_compare(case, split=split)

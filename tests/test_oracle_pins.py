@@ -742,6 +742,36 @@ def test_silu_is_odd_up_to_the_identity():
         assert np.all(err <= bound + 2 * 2.0 ** -8 * np.abs(diff)[live])
 
 
+def test_conv_bias_indexed_by_part_head_and_channel():
+    # With every convolution weight zero the output is SiLU of the bias
+    # alone.  The bias of (part p, head h, channel c) is the exact BF16 value
+    # 2^(4 + p + 3 h) * (1 + c / 128): distinct for every (p, h, c), and at
+    # least 16, where silu(b) = b / (1 + e^-b) lies within 1.2e-7 b of b, far
+    # inside half a BF16 step (2^-9 b), so the output must be the bias bits
+    # exactly -- with no appeal to the oracle's SiLU.  A bias indexed without
+    # the part offset, by head only, or by channel only, gives other values.
+    c = _layer()
+    H, D = c["H"], c["H"] * 128
+    c["conv_weight"] = np.zeros_like(c["conv_weight"])
+    bias = np.zeros(3 * D, dtype=np.float32)
+    for part in range(3):
+        for h in range(H):
+            ch = np.arange(128)
+            bias[part * D + h * 128 + ch] = 2.0 ** (4 + part + 3 * h) * (1.0 + ch / 128.0)
+    c["conv_bias"] = _bits(bias)
+    assert len(np.unique(c["conv_bias"])) == 3 * D
+    for pending in (True, False):
+        (q, k, v, _), _ = _prologue(c, pending=pending)
+        B, Q = c["B"], c["Q"]
+        for b in range(B):
+            rows = slice(b * Q, (b + 1) * Q)
+            if c["state_slots"][b] <= 0:
+                continue
+            for part, out in enumerate((q, k, v)):
+                want = c["conv_bias"][part * D:(part + 1) * D].reshape(H, 128)
+                np.testing.assert_array_equal(out[rows], np.broadcast_to(want, (Q, H, 128)))
+
+
 def test_new_window_is_taps_then_inputs():
     c = _layer()
     c["pending"][:] = 2
