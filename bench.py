@@ -356,7 +356,8 @@ def _event_ms(stream, fn, iters):
     return e0.elapsed_time(e1) / iters
 
 
-ROW_GROUPS = ("commit", "mid_batch", "varlen", "latency", "bookkeeping", "decode_loop", "layer")
+ROW_GROUPS = ("commit", "mid_batch", "layers", "varlen", "latency", "bookkeeping", "decode_loop",
+              "layer")
 
 
 def measure_rows(dev, stream, peak, cpu_seconds, only=None):
@@ -468,6 +469,9 @@ def measure_rows(dev, stream, peak, cpu_seconds, only=None):
                           frac=nbytes / ms / 1e6 / peak))
         del d, out
 
+    if want('layers'):
+        rows["replay_verify_layers"] = measure_layers(dev, stream, dt, peak)
+
     if want('varlen'):
         # the large batch with windows of 1..8 tokens (query_start_loc)
         name = "replay-verify-varlen-f32-h64-b512-q8"
@@ -550,6 +554,56 @@ def measure_rows(dev, stream, peak, cpu_seconds, only=None):
     if want("layer"):
         rows["layer"] = measure_layer(dev, stream, dt, peak)
     return rows
+
+
+def measure_layers(dev, stream, dt, peak, L=4):
+    """The fused step over L = 4 layers of the mid-size batch's shapes (H=32,
+    B=128, q=4, a 512-slot FP32 pool per layer), as one multi-layer launch
+    and as L single-layer launches back to back; the bytes are the L
+    layers' algorithmic bytes."""
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import (kda_replay_verify,
+                                                               kda_replay_verify_layers, synth)
+    spec = dict(synth.WORKLOADS["replay-verify-f32-h32-b128-q4"])
+    spec.pop("kind")
+    c = synth.layers_case(L=L, **spec)
+    st = {key: dt(c[key]) for key in synth.LAYER_STACKED + synth.SHARED_INDEX}
+    pools = [dt(lay["state"]) for lay in c["layers"]]
+    corrs = [dt(lay["corr"]) for lay in c["layers"]]
+    kgs = [dt(lay["key_gate"]) for lay in c["layers"]]
+    out = torch.zeros(c["q"].shape, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    common = dict(Q=c["Q"], lower_bound=c["lower_bound"], q_scale=c["q_scale"], status=status,
+                  stream=stream)
+
+    def fused():
+        kda_replay_verify_layers(st["q"], st["k"], st["v"], st["raw_g"], st["raw_beta"],
+                                 st["A_log"], st["dt_bias"], pools, st["state_slots"],
+                                 st["record_rows"], st["pending"], corrs, kgs, out, **common)
+
+    def per_layer():
+        for l in range(L):
+            kda_replay_verify(st["q"][l], st["k"][l], st["v"][l], st["raw_g"][l],
+                              st["raw_beta"][l], st["A_log"][l], st["dt_bias"][l], pools[l],
+                              st["state_slots"], st["record_rows"], st["pending"], corrs[l],
+                              kgs[l], out[l], split=1, **common)
+    for _ in range(5):
+        fused()
+        per_layer()
+    ms_fused = _event_ms(stream, fused, 30)
+    ms_single = _event_ms(stream, per_layer, 30)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"multi-layer step: device status {int(status.item())}")
+    abs_ = [algorithmic_bytes(lay) for lay in c["layers"]]
+    nbytes = sum(a["total"] for a in abs_)
+    tokens = sum(a["live_tokens"] for a in abs_)
+    row = dict(workload=f"replay-verify-layers-f32-l{L}-h32-b128-q4", L=L, ms=ms_fused,
+               ms_single_layer_launches=ms_single, tok_s=tokens / (ms_fused / 1e3),
+               bytes_per_launch=nbytes,
+               roofline=dict(bound="hbm", achieved=nbytes / ms_fused / 1e6, peak=peak,
+                             unit="GB/s", frac=nbytes / ms_fused / 1e6 / peak))
+    del pools, corrs, kgs, st, out
+    return row
 
 
 def layer_algorithmic_bytes(c):

@@ -19,7 +19,9 @@
  * Conventions shared by every entry point
  *  - K = V = 128 (key and value channels per head).  Other sizes return
  *    KDA_ERR_UNSUPPORTED.
- *  - Every pointer is DEVICE memory owned by the caller.  The library never
+ *  - Every pointer is DEVICE memory owned by the caller (the one exception:
+ *    the per-layer address and stride arrays of kda_replay_verify_layers
+ *    are host arrays, read during the call).  The library never
  *    allocates or frees, and only kda_check_status synchronises (with its
  *    own stream); every other call enqueues its kernels on `stream` (a
  *    cudaStream_t passed as void*, NULL = the legacy default stream) and
@@ -77,6 +79,7 @@ extern "C" {
 
 #define KDA_HEAD_DIM 128
 #define KDA_MAX_WINDOW 8
+#define KDA_MAX_LAYERS 64
 
 typedef uint16_t kda_bf16;
 
@@ -180,6 +183,51 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                       const int32_t *boundary_lens, kda_bf16 *out, int B,
                       int H, int Q, int null_slot, int split, int32_t *status,
                       void *stream);
+
+/*
+ * kda_replay_verify_layers -- kda_replay_verify over L layers in one launch
+ * (persistent CTAs over the (layer, request, head) items, layer-major),
+ * with per-layer base addresses and strides as the commit page's KdaCommit
+ * takes them (its argument list: per-layer state / correction / key-gate
+ * bases and their slot / row strides).  Layer l computes exactly what
+ * kda_replay_verify computes on layer l's operands; the layers share the
+ * index arrays, as the layers of one model share a request's slot, record
+ * row and accepted count:
+ *
+ *   q, k, v, raw_g  [L, B*Q, H, 128] BF16, layer-stacked (layer l at
+ *                   l*B*Q*H*128 elements); raw_beta [L, B*Q, H] BF16
+ *   A_log [L, H]; dt_bias [L, H, 128] FP32
+ *   state_pools, corrs, key_gates  HOST arrays [L] of DEVICE addresses:
+ *                   layer l's FP32 pool [n_slots, H, 128, 128], corrections
+ *                   [n_rows, H, rq, 128] FP32 and key/gate records
+ *                   [n_rows, H, rq, 256] BF16, each 16-byte aligned
+ *   slot_strides, corr_row_strides, kg_row_strides  HOST arrays [L] of
+ *                   element strides (at least one slot's / row's extent,
+ *                   multiples of 16 bytes)
+ *   state_slots, record_rows [B], pending [n_rows] int32, device, shared
+ *   out             [L, B*Q, H, 128] BF16, layer-stacked
+ *   1 <= L <= KDA_MAX_LAYERS; 1 <= Q <= rq <= 8; uniform windows (b*Q + t);
+ *   no boundary states; -10 <= lower_bound <= 10.
+ * The host arrays are read during the call and their values become kernel
+ * parameters (so a captured launch keeps them); everything else is as in
+ * kda_replay_verify with split = 1.  Bad host values return KDA_ERR_ARG /
+ * KDA_ERR_ALIGN before any launch; device-side index errors go to status.
+ */
+int kda_replay_verify_layers(const kda_bf16 *q, const kda_bf16 *k,
+                             const kda_bf16 *v, const kda_bf16 *raw_g,
+                             const kda_bf16 *raw_beta, const float *A_log,
+                             const float *dt_bias, float lower_bound,
+                             float q_scale, float *const *state_pools,
+                             const int64_t *slot_strides, int n_slots,
+                             const int32_t *state_slots,
+                             const int32_t *record_rows,
+                             const int32_t *pending, float *const *corrs,
+                             kda_bf16 *const *key_gates,
+                             const int64_t *corr_row_strides,
+                             const int64_t *kg_row_strides, int n_rows,
+                             int rq, kda_bf16 *out, int L, int B, int H,
+                             int Q, int null_slot, int32_t *status,
+                             void *stream);
 
 /*
  * kda_commit -- the standalone closed-form commit over L layers (commit

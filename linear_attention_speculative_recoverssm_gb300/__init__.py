@@ -25,6 +25,7 @@ from ._lib import (  # noqa: F401
     kda_layer_epilogue,
     kda_layer_prologue,
     kda_replay_verify,
+    kda_replay_verify_layers,
     kda_selftest_wait_timeout,
     kda_verify,
     layer_tables,

@@ -25,7 +25,7 @@ KDA_STATE_F32 = 0
 KDA_STATE_BF16 = 1
 
 EXPORTS = ("kda_abi_version", "kda_error_string", "kda_check_status", "kda_verify",
-           "kda_replay_verify",
+           "kda_replay_verify", "kda_replay_verify_layers",
            "kda_commit", "kda_defer_commit", "kda_flush_plan", "kda_selftest_wait_timeout",
            "kda_layer_prologue", "kda_layer_epilogue")
 
@@ -43,6 +43,8 @@ _SIGS = {
     "kda_replay_verify": ([_P] * 7 + [_F, _F, _P, _I64, _I, _P, _P, _I, _P, _P, _P, _P, _I64,
                                       _I64, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
                           _I),
+    "kda_replay_verify_layers": ([_P] * 7 + [_F, _F, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I,
+                                             _I, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "kda_commit": ([_P] * 14 + [_I, _F, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "kda_defer_commit": ([_P] * 5 + [_I, _I, _I, _P, _P], _I),
     "kda_flush_plan": ([_P] * 7 + [_I, _I, _I, _I, _P, _P], _I),
@@ -176,6 +178,46 @@ def kda_replay_verify(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pool, stat
         corr.shape[2], _ptr(boundary_slots), _ptr(boundary_lens), _ptr(out), B, H, Q,
         null_slot, split, _ptr(status), _stream(stream))
     return _check("kda_replay_verify", rc, raise_on_error)
+
+
+def kda_replay_verify_layers(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pools, state_slots,
+                             record_rows, pending, corrs, key_gates, out, *, Q, lower_bound,
+                             q_scale, null_slot=0, status=None, stream=None,
+                             raise_on_error=True):
+    """Fused replay + verify over L layers in one launch: q, k, v, raw_g, out
+    [L, B*Q, H, 128] and raw_beta [L, B*Q, H] layer-stacked; A_log [L, H],
+    dt_bias [L, H, 128]; state_pools, corrs, key_gates lists of the L
+    layers' FP32 pools, FP32 corrections and BF16 key/gate records (their
+    addresses and strides are passed as host arrays); the index arrays are
+    shared by the layers."""
+    import torch
+    L = len(state_pools)
+    if not (len(corrs) == len(key_gates) == L):
+        raise ValueError("state_pools, corrs and key_gates must list the same layers")
+    for t in state_pools:
+        _expect(t, torch.float32, "state_pools[l]")
+    for t in corrs:
+        _expect(t, torch.float32, "corrs[l]")
+    if any(t.shape[2] != corrs[0].shape[2] for t in list(corrs) + list(key_gates)):
+        raise ValueError("every layer's records must hold the same number of tokens")
+    for t in key_gates:
+        _expect(t, torch.bfloat16, "key_gates[l]")
+    _check_step_dtypes(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_slots, record_rows,
+                       corrs[0], key_gates[0], out)
+    _expect(pending, torch.int32, "pending")
+    ptrs = lambda ts: (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
+    strides = lambda ts: (ctypes.c_int64 * L)(*[t.stride(0) for t in ts])
+    B = state_slots.shape[0]
+    H = q.shape[2]
+    rc = load().kda_replay_verify_layers(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(raw_g), _ptr(raw_beta), _ptr(A_log), _ptr(dt_bias),
+        lower_bound, q_scale, ptrs(state_pools), strides(state_pools),
+        min(t.shape[0] for t in state_pools), _ptr(state_slots), _ptr(record_rows),
+        _ptr(pending), ptrs(corrs), ptrs(key_gates), strides(corrs), strides(key_gates),
+        min(min(t.shape[0] for t in corrs), min(t.shape[0] for t in key_gates)),
+        corrs[0].shape[2], _ptr(out), L,
+        B, H, Q, null_slot, _ptr(status), _stream(stream))
+    return _check("kda_replay_verify_layers", rc, raise_on_error)
 
 
 def kda_commit(state_ptrs, corr_ptrs, kg_ptrs, state_strides, corr_strides, kg_strides, A_log,

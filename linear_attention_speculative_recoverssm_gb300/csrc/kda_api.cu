@@ -20,6 +20,14 @@ int launch_step_q5(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q6(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q7(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_q8(const StepParams &, int, int, int, cudaStream_t);
+int launch_step_layers_q1(const StepParams &, const LayerBases &, int, cudaStream_t);
+int launch_step_layers_q2(const StepParams &, const LayerBases &, int, cudaStream_t);
+int launch_step_layers_q3(const StepParams &, const LayerBases &, int, cudaStream_t);
+int launch_step_layers_q4(const StepParams &, const LayerBases &, int, cudaStream_t);
+int launch_step_layers_q5(const StepParams &, const LayerBases &, int, cudaStream_t);
+int launch_step_layers_q6(const StepParams &, const LayerBases &, int, cudaStream_t);
+int launch_step_layers_q7(const StepParams &, const LayerBases &, int, cudaStream_t);
+int launch_step_layers_q8(const StepParams &, const LayerBases &, int, cudaStream_t);
 int launch_step_varlen_q1(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_varlen_q2(const StepParams &, int, int, int, cudaStream_t);
 int launch_step_varlen_q3(const StepParams &, int, int, int, cudaStream_t);
@@ -69,6 +77,21 @@ int launch_step(const StepParams &p, int n_items, int Q, int variant, int split,
     case 6: return launch_step_q6(p, n_items, variant, split, stream);
     case 7: return launch_step_q7(p, n_items, variant, split, stream);
     case 8: return launch_step_q8(p, n_items, variant, split, stream);
+    default: return KDA_ERR_ARG;
+  }
+}
+
+int launch_step_layers(const StepParams &p, const LayerBases &lay, int n_items, int Q,
+                       cudaStream_t stream) {
+  switch (Q) {
+    case 1: return launch_step_layers_q1(p, lay, n_items, stream);
+    case 2: return launch_step_layers_q2(p, lay, n_items, stream);
+    case 3: return launch_step_layers_q3(p, lay, n_items, stream);
+    case 4: return launch_step_layers_q4(p, lay, n_items, stream);
+    case 5: return launch_step_layers_q5(p, lay, n_items, stream);
+    case 6: return launch_step_layers_q6(p, lay, n_items, stream);
+    case 7: return launch_step_layers_q7(p, lay, n_items, stream);
+    case 8: return launch_step_layers_q8(p, lay, n_items, stream);
     default: return KDA_ERR_ARG;
   }
 }
@@ -261,6 +284,65 @@ int kda_replay_verify(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
       null_slot, status);
   return kda::launch_step(p, items, Q, boundary_slots ? 3 : 2, split,
                           static_cast<cudaStream_t>(stream));
+}
+
+int kda_replay_verify_layers(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                             const kda_bf16 *raw_g, const kda_bf16 *raw_beta,
+                             const float *A_log, const float *dt_bias, float lower_bound,
+                             float q_scale, float *const *state_pools,
+                             const int64_t *slot_strides, int n_slots,
+                             const int32_t *state_slots, const int32_t *record_rows,
+                             const int32_t *pending, float *const *corrs,
+                             kda_bf16 *const *key_gates, const int64_t *corr_row_strides,
+                             const int64_t *kg_row_strides, int n_rows, int rq, kda_bf16 *out,
+                             int L, int B, int H, int Q, int null_slot, int32_t *status,
+                             void *stream) {
+  if (!gate_bound_ok(lower_bound)) return KDA_ERR_UNSUPPORTED;
+  if (L < 1 || L > KDA_MAX_LAYERS) return KDA_ERR_ARG;
+  if (!state_pools || !slot_strides || !corrs || !key_gates || !corr_row_strides ||
+      !kg_row_strides)
+    return KDA_ERR_ARG;
+  // every layer's pool and records, checked like the one-layer call's
+  // (layer 0's stand in for the pointers the shared checks look at)
+  const long long n_tok = (long long)B * Q;
+  int rc = check_step_args(q, k, v, raw_g, raw_beta, A_log, dt_bias, state_pools[0], 4,
+                           slot_strides[0], n_slots, state_slots, corrs[0], key_gates[0],
+                           corr_row_strides[0], kg_row_strides[0], n_rows, rq, out, B, H, Q,
+                           nullptr, (int)(n_tok > 0x7fffffffLL ? -1 : n_tok));
+  if (rc == kNothingToDo) return KDA_OK;
+  if (rc != KDA_OK) return rc;
+  if (!record_rows || !pending) return KDA_ERR_ARG;
+  if ((long long)L * B * H > 0x7fffffffLL) return KDA_ERR_ARG;
+  kda::LayerBases lay;
+  lay.L = L;
+  lay.act_stride = n_tok * H * KDA_HEAD_DIM;
+  lay.beta_stride = n_tok * H;
+  for (int l = 0; l < L; ++l) {
+    if (!state_pools[l] || !corrs[l] || !key_gates[l]) return KDA_ERR_ARG;
+    if (slot_strides[l] < (int64_t)H * KDA_HEAD_DIM * KDA_HEAD_DIM ||
+        corr_row_strides[l] < (int64_t)H * rq * KDA_HEAD_DIM ||
+        kg_row_strides[l] < (int64_t)H * rq * 2 * KDA_HEAD_DIM)
+      return KDA_ERR_ARG;
+    if (!aligned16(state_pools[l]) || !aligned16(corrs[l]) || !aligned16(key_gates[l]))
+      return KDA_ERR_ALIGN;
+    if (((slot_strides[l] * 4) & 15) != 0 || ((corr_row_strides[l] * 4) & 15) != 0 ||
+        ((kg_row_strides[l] * 2) & 15) != 0)
+      return KDA_ERR_ALIGN;
+    lay.state[l] = reinterpret_cast<uint64_t>(state_pools[l]);
+    lay.corr[l] = reinterpret_cast<uint64_t>(corrs[l]);
+    lay.kg[l] = reinterpret_cast<uint64_t>(key_gates[l]);
+    lay.slot_stride[l] = slot_strides[l];
+    lay.corr_stride[l] = corr_row_strides[l];
+    lay.kg_stride[l] = kg_row_strides[l];
+  }
+  // layer 0's pool and records are also the StepParams' (the kernel reads
+  // the layer bases for every layer)
+  const kda::StepParams p = make_params(
+      q, k, v, raw_g, raw_beta, A_log, dt_bias, lower_bound, q_scale, state_pools[0],
+      slot_strides[0], n_slots, state_slots, nullptr, (int)n_tok, record_rows, pending, corrs[0],
+      key_gates[0], corr_row_strides[0], kg_row_strides[0], n_rows, rq, nullptr, nullptr, out, B,
+      H, null_slot, status);
+  return kda::launch_step_layers(p, lay, L * B * H, Q, static_cast<cudaStream_t>(stream));
 }
 
 int kda_commit(const uint64_t *state_ptrs, const uint64_t *corr_ptrs, const uint64_t *kg_ptrs,

@@ -175,6 +175,17 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
       : "memory");
 }
 
+// The same for a 4-D box (coordinates x, y, z, w; x as in tma_load_3d).
+__device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, int x, int y, int z,
+                                            int w, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared through the load/store path
 // (not the bulk-copy engine).  Both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {

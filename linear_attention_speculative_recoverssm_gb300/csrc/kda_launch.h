@@ -8,6 +8,7 @@
 namespace kda {
 
 struct StepParams;
+struct LayerBases;
 
 // SMs of `dev`, cached after the first query.
 int device_sm_count(int dev);
@@ -18,6 +19,10 @@ int device_sm_count(int dev);
 //   split   1: persistent CTAs; 2 / 4: cluster of that many CTAs per item.
 int launch_step(const StepParams &p, int n_items, int Q, int variant, int split,
                 cudaStream_t stream);
+
+// The multi-layer replay + verify for window Q (1..8), persistent CTAs.
+int launch_step_layers(const StepParams &p, const LayerBases &lay, int n_items, int Q,
+                       cudaStream_t stream);
 
 int launch_commit(const uint64_t *state_ptrs, const uint64_t *corr_ptrs, const uint64_t *kg_ptrs,
                   const int64_t *state_strides, const int64_t *corr_strides,

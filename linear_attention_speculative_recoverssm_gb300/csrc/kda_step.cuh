@@ -37,6 +37,21 @@ struct StepParams {
   int32_t *status;
 };
 
+// The multi-layer step: one launch over L layers whose items are
+// (layer, request, head), layer-major.  Every layer has its own state pool,
+// corrections and key / gate records (addresses and strides, passed by value
+// as kernel parameters); the index arrays (state slots, record rows, pending
+// counts) are shared by the layers, and the activations and outputs of all
+// layers are stacked, layer l's at l * act_stride elements (raw_beta at
+// l * beta_stride).  A_log is [L, H] and dt_bias [L, H, 128].
+constexpr int kMaxLayers = KDA_MAX_LAYERS;
+struct LayerBases {
+  int L;
+  long long act_stride, beta_stride;
+  uint64_t state[kMaxLayers], corr[kMaxLayers], kg[kMaxLayers];
+  long long slot_stride[kMaxLayers], corr_stride[kMaxLayers], kg_stride[kMaxLayers];
+};
+
 // Number of scalars the token half reduces over channels: sum k_t^2,
 // sum q_t^2 (Q each) and the Q*Q raw pair products (B_ts at t*Q + s for
 // s <= t, A_ts at s*Q + t for s < t).
@@ -52,6 +67,7 @@ struct Red {
 
 struct ItemMeta {
   int b, h;
+  int l;      // layer (the multi-layer step; 0 otherwise)
   int tok0;   // first token of the window
   int qb;     // window length, 0 .. Q
   int slot;   // < 0: inert
@@ -73,6 +89,7 @@ __device__ __forceinline__ ItemMeta item_meta(const StepParams &p, int item, int
   ItemMeta it;
   it.b = item / p.H;
   it.h = item - it.b * p.H;
+  it.l = 0;
   int slot = p.state_slots[it.b];
   if (slot >= p.n_slots) {
     if (report_errors) report(p.status, KDA_ERR_ARG);

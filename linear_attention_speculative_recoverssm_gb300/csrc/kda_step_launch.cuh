@@ -52,9 +52,34 @@ int encode_token_maps(const StepParams &p, WsMaps &maps) {
   return KDA_OK;
 }
 
-template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN>
-int launch_ws(const StepParams &p, int n_items, cudaStream_t stream) {
-  auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY, VARLEN>;
+// The stacked inputs of the multi-layer step [L, n_tokens, H, 128] as 4-D
+// tensors (128, H, n_tokens, L) with a (128, 1, Q, 1) box.
+template <int Q>
+int encode_layer_token_maps(const StepParams &p, const LayerBases &lay, WsMaps &maps) {
+  const auto encode = tensor_map_encoder();
+  if (encode == nullptr) return KDA_ERR_CUDA;
+  const uint16_t *src[4] = {p.q, p.k, p.g, p.v};
+  const cuuint64_t dims[4] = {(cuuint64_t)kDim, (cuuint64_t)p.H, (cuuint64_t)p.n_tokens,
+                              (cuuint64_t)lay.L};
+  const cuuint64_t strides[3] = {(cuuint64_t)kDim * 2, (cuuint64_t)p.H * kDim * 2,
+                                 (cuuint64_t)lay.act_stride * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)kDim, 1, (cuuint32_t)Q, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  for (int x = 0; x < 4; ++x) {
+    if (encode(&maps.tok[x], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<uint16_t *>(src[x]), dims, strides, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
+template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN, bool LAYERS = false>
+int launch_ws(const StepParams &p, int n_items, cudaStream_t stream,
+              const LayerBases *bases = nullptr) {
+  auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY, VARLEN, LAYERS>;
   constexpr size_t smem = sizeof(WsSmem<Q, ST, BOUNDARY>);
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -69,10 +94,25 @@ int launch_ws(const StepParams &p, int n_items, cudaStream_t stream) {
   const int sms = device_sm_count(dev);
   const int grid = n_items < sms ? n_items : sms;
   WsMaps maps;
-  const int st = encode_token_maps<Q>(p, maps);
+  WsLayers<LAYERS> lay{};
+  int st;
+  if constexpr (LAYERS) {
+    static_cast<LayerBases &>(lay) = *bases;
+    st = encode_layer_token_maps<Q>(p, *bases, maps);
+  } else {
+    (void)bases;
+    st = encode_token_maps<Q>(p, maps);
+  }
   if (st != KDA_OK) return st;
-  kern<<<grid, kWsThreads, smem, stream>>>(p, maps, n_items);
+  kern<<<grid, kWsThreads, smem, stream>>>(p, maps, lay, n_items);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// The multi-layer replay + verify (persistent kernel, uniform windows).
+template <int Q>
+int launch_step_layers_q(const StepParams &p, const LayerBases &lay, int n_items,
+                         cudaStream_t stream) {
+  return launch_ws<Q, float, true, false, false, true>(p, n_items, stream, &lay);
 }
 
 template <int Q, int SPLIT, bool BOUNDARY, bool VARLEN>

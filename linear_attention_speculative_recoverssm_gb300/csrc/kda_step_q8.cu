@@ -6,4 +6,8 @@ int launch_step_q8(const StepParams &p, int n_items, int variant, int split,
                     cudaStream_t stream) {
   return launch_step_q<8, false>(p, n_items, variant, split, stream);
 }
+int launch_step_layers_q8(const StepParams &p, const LayerBases &lay, int n_items,
+                           cudaStream_t stream) {
+  return launch_step_layers_q<8>(p, lay, n_items, stream);
+}
 }  // namespace kda

@@ -115,6 +115,15 @@ struct WsMaps {
   CUtensorMap tok[4];
 };
 
+// The multi-layer instances take the layers' bases (LayerBases) as a kernel
+// parameter; the others an empty stand-in.
+template <bool LAYERS>
+struct WsLayers {
+  int unused;
+};
+template <>
+struct WsLayers<true> : LayerBases {};
+
 // One item's inputs, staged by tensor / bulk copies one item ahead of the
 // prologue (128-byte aligned: tensor-copy destinations).
 template <int Q>
@@ -376,8 +385,9 @@ __device__ __forceinline__ void ws_dots(const float4 (&s)[4][4], const float *__
 // s > t).  Writes o_t (BF16) and, with a record row, u_t (FP32).
 template <int Q, int NG, bool VARLEN, typename Ops>
 __device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
-                                         const StepParams &p, long long tok0, int qb, int h,
-                                         int rec, int R0, int c, int lane) {
+                                         const StepParams &p, uint16_t *out, float *corr,
+                                         long long corr_row_stride, long long tok0, int qb,
+                                         int h, int rec, int R0, int c, int lane) {
   const int cw = c < Q ? c : Q - 1;  // lanes without a w role compute unused values
   const uint2 vb = *reinterpret_cast<const uint2 *>(&op.vv[cw][R0]);
   const float4 v4 = make_float4(__uint_as_float(vb.x << 16), __uint_as_float(vb.x & 0xffff0000u),
@@ -420,21 +430,27 @@ __device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
     if (hy[g] && (!VARLEN || ty[g] < qb)) {
       const uint2 o2 = make_uint2(pack_bf16x2(oacc[g][0], oacc[g][1]),
                                   pack_bf16x2(oacc[g][2], oacc[g][3]));
-      *reinterpret_cast<uint2 *>(p.out + ((tok0 + ty[g]) * p.H + h) * kDim + R0) = o2;
+      *reinterpret_cast<uint2 *>(out + ((tok0 + ty[g]) * p.H + h) * kDim + R0) = o2;
     }
   }
   if ((VARLEN ? c < qb : c < Q) && rec >= 0) {
-    const long long cbase = (long long)rec * p.corr_row_stride + ((long long)h * p.rq + c) * kDim;
-    stg4(p.corr + cbase + R0, make_float4(bt * res[0], bt * res[1], bt * res[2], bt * res[3]));
+    const long long cbase = (long long)rec * corr_row_stride + ((long long)h * p.rq + c) * kDim;
+    stg4(corr + cbase + R0, make_float4(bt * res[0], bt * res[1], bt * res[2], bt * res[3]));
   }
 }
 
 // VARLEN: windows from query_start_loc (p.qsl, non-null), each of q_b <= Q
 // tokens; otherwise request b's window is tokens b*Q .. b*Q + Q - 1.  The
 // meta words carry b (uniform) or the window's first token and length.
-template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN>
+// LAYERS: items (layer, request, head) over the layers of `lay` (uniform
+// windows, FP32 state, no boundary states); the meta words carry the layer
+// in place of the window length.
+template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN, bool LAYERS>
 __global__ void __launch_bounds__(kWsThreads, 1)
-    kda_step_ws(const StepParams p, const __grid_constant__ WsMaps maps, int n_items) {
+    kda_step_ws(const StepParams p, const __grid_constant__ WsMaps maps,
+                const __grid_constant__ WsLayers<LAYERS> lay, int n_items) {
+  static_assert(!LAYERS || (!VARLEN && !BOUNDARY && REPLAY && sizeof(ST) == 4),
+                "the multi-layer step: uniform windows, FP32 state, no boundary");
   using Smem = WsSmem<Q, ST, BOUNDARY>;
   using Ops = WsOps<Q, BOUNDARY>;
   static_assert(WsLayoutCheck<Q, ST, BOUNDARY>::ok, "layout");
@@ -449,8 +465,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   const int first = blockIdx.x, stride = gridDim.x;
   const int count = first < n_items ? (n_items - first + stride - 1) / stride : 0;
 
+  // item index -> request and layer (layer-major over LAYERS' layers)
+  auto req_of = [&](int idx) { return LAYERS ? (idx / p.H) % p.B : idx / p.H; };
+  auto layer_of = [&](int idx) { return LAYERS ? idx / (p.H * p.B) : 0; };
   auto item_slot = [&](int j) {
-    const int b = (first + j * stride) / p.H;
+    const int b = req_of(first + j * stride);
     const int s = p.state_slots[b];
     return (s > p.null_slot && s < p.n_slots) ? s : -1;
   };
@@ -460,7 +479,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     if (slot >= 0) {
       const int h = (first + j * stride) % p.H;
       mbar_arrive_expect_tx(bar, kPageBytes);
-      bulk_g2s(sm.stage[j % NS], page_ptr<ST>(p, slot, h), kPageBytes, bar);
+      if constexpr (LAYERS) {
+        const int l = layer_of(first + j * stride);
+        const float *page = reinterpret_cast<const float *>(lay.state[l]) +
+                            (long long)slot * lay.slot_stride[l] + (long long)h * (kDim * kDim);
+        bulk_g2s(sm.stage[j % NS], page, kPageBytes, bar);
+      } else {
+        bulk_g2s(sm.stage[j % NS], page_ptr<ST>(p, slot, h), kPageBytes, bar);
+      }
     } else {
       mbar_arrive(bar);
     }
@@ -512,9 +538,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       sm.next_meta[5] = m.bslot;
       sm.next_meta[6] = m.m;
       if constexpr (VARLEN) sm.next_meta[7] = m.qb;
+      if constexpr (LAYERS) sm.next_meta[7] = m.l;
     };
     auto load_raw = [&](int i, Raw &r) {
-      const int b = (first + i * stride) / p.H;
+      const int b = req_of(first + i * stride);
       r.slot = p.state_slots[b];
       r.rec = p.record_rows != nullptr ? p.record_rows[b] : b;
       r.bslot = -1;
@@ -540,8 +567,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const int rs_slot = r.slot, rs_rec = r.rec, rs_bslot = r.bslot, rs_blen = r.blen,
                 rs_pend = r.pend;
       ItemMeta it;
-      it.b = (first + i * stride) / p.H;
-      it.h = (first + i * stride) - it.b * p.H;
+      if constexpr (LAYERS) {
+        it.b = req_of(first + i * stride);
+        it.h = (first + i * stride) % p.H;
+        it.l = layer_of(first + i * stride);
+      } else {
+        it.b = (first + i * stride) / p.H;
+        it.h = (first + i * stride) - it.b * p.H;
+        it.l = 0;
+      }
       int slot = rs_slot;
       if (slot >= p.n_slots) {
         report(p.status, KDA_ERR_ARG);
@@ -594,6 +628,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       m.bslot = sm.next_meta[5];
       m.m = sm.next_meta[6];
       m.qb = VARLEN ? sm.next_meta[7] : Q;
+      m.l = LAYERS ? sm.next_meta[7] : 0;
       WsIn<Q> &in = sm.in[i & 1];
       in.meta[0] = m.b;
       in.meta[1] = m.h;
@@ -603,6 +638,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       in.meta[5] = m.bslot;
       in.meta[6] = m.m;
       if constexpr (VARLEN) in.meta[7] = m.qb;
+      if constexpr (LAYERS) in.meta[7] = m.l;
       uint64_t *bar = &sm.infull[i & 1];
       if (m.slot < 0) {
         mbar_arrive(bar);
@@ -615,14 +651,25 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
       // (rows past the window or the activations arrive as zeros or as other
       // requests' tokens; nothing computed from them is written)
-      for (int x = 0; x < 4; ++x)
-        tma_load_3d(&in.tok[x][0][0], &maps.tok[x], 0, m.h, VARLEN ? m.tok0 : m.b * Q, bar);
+      for (int x = 0; x < 4; ++x) {
+        if constexpr (LAYERS)
+          tma_load_4d(&in.tok[x][0][0], &maps.tok[x], 0, m.h, m.b * Q, m.l, bar);
+        else
+          tma_load_3d(&in.tok[x][0][0], &maps.tok[x], 0, m.h, VARLEN ? m.tok0 : m.b * Q, bar);
+      }
       if (nrec > 0) {
-        bulk_g2s(&in.kg[0][0],
-                 p.kg + (long long)m.rec * p.kg_row_stride + (long long)m.h * p.rq * (2 * kDim),
+        const uint16_t *kg = p.kg;
+        const float *corr = p.corr;
+        long long kgs = p.kg_row_stride, cs = p.corr_row_stride;
+        if constexpr (LAYERS) {
+          kg = reinterpret_cast<const uint16_t *>(lay.kg[m.l]);
+          corr = reinterpret_cast<const float *>(lay.corr[m.l]);
+          kgs = lay.kg_stride[m.l];
+          cs = lay.corr_stride[m.l];
+        }
+        bulk_g2s(&in.kg[0][0], kg + (long long)m.rec * kgs + (long long)m.h * p.rq * (2 * kDim),
                  rec_bytes, bar);
-        bulk_g2s(&in.corr[0][0],
-                 p.corr + (long long)m.rec * p.corr_row_stride + (long long)m.h * p.rq * kDim,
+        bulk_g2s(&in.corr[0][0], corr + (long long)m.rec * cs + (long long)m.h * p.rq * kDim,
                  rec_bytes, bar);
       }
     };
@@ -633,6 +680,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // The window of item i is read from next_meta, which holds item i's
     // resolved chain whenever this runs.
     auto load_small = [&](int i) {
+      if constexpr (LAYERS) {
+        const int idx = first + i * stride;
+        const int b = req_of(idx), h = idx % p.H, l = layer_of(idx);
+        dt_n = p.dt_bias[((long long)l * p.H + h) * kDim + c];
+        alog_n = p.A_log[l * p.H + h];
+        beta_n = 0;
+        if (c < Q) beta_n = p.beta[l * lay.beta_stride + ((long long)b * Q + c) * p.H + h];
+        return;
+      }
       const int b = (first + i * stride) / p.H;
       const int h = (first + i * stride) - b * p.H;
       dt_n = p.dt_bias[h * kDim + c];
@@ -701,6 +757,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       it.bslot = in.meta[5];
       it.m = in.meta[6];
       it.qb = VARLEN ? in.meta[7] : Q;
+      it.l = LAYERS ? in.meta[7] : 0;
       const bool live = it.slot >= 0;
 
       // (inputs are re-read from the stage where needed: fewer live registers)
@@ -768,6 +825,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         op.meta[5] = it.bslot;
         op.meta[6] = it.m;
         if constexpr (VARLEN) op.meta[7] = it.qb;
+        if constexpr (LAYERS) op.meta[7] = it.l;
       }
       if (live) {
 #pragma unroll
@@ -864,13 +922,18 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         // New key / gate records: the old ones were read above.
         if (it.rec >= 0) {
-          const long long kbase = (long long)it.rec * p.kg_row_stride +
-                                  (long long)it.h * p.rq * (2 * kDim) + c;
+          uint16_t *kg = p.kg;
+          long long kgs = p.kg_row_stride;
+          if constexpr (LAYERS) {
+            kg = reinterpret_cast<uint16_t *>(lay.kg[it.l]);
+            kgs = lay.kg_stride[it.l];
+          }
+          const long long kbase = (long long)it.rec * kgs + (long long)it.h * p.rq * (2 * kDim) + c;
 #pragma unroll
           for (int t = 0; t < Q; ++t) {
             if (!VARLEN || t < it.qb) {
-              p.kg[kbase + t * 2 * kDim] = in.tok[1][t][c];
-              p.kg[kbase + t * 2 * kDim + kDim] = in.tok[2][t][c];
+              kg[kbase + t * 2 * kDim] = in.tok[1][t][c];
+              kg[kbase + t * 2 * kDim + kDim] = in.tok[2][t][c];
             }
           }
         }
@@ -918,7 +981,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   };
   // lane 0: the raw slot of item j + NS + 1, loaded an item before its use
   // (the page that may follow item j into its stage is item j + NS's)
-  auto raw_slot = [&](int i) { return p.state_slots[(first + i * stride) / p.H]; };
+  auto raw_slot = [&](int i) { return p.state_slots[req_of(first + i * stride)]; };
   auto valid_slot = [&](int s) { return (s > p.null_slot && s < p.n_slots) ? s : -1; };
   int raw_ahead = -1;
   if (lane == 0 && NS < count) raw_ahead = raw_slot(NS);
@@ -938,6 +1001,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const Ops &op = sm.ops[j % kWsOpsBufs];
     const int h = op.meta[1], slot = op.meta[2], rec = op.meta[3];
     const int n = op.meta[4], bslot = op.meta[5], m = op.meta[6];
+    // the layer's outputs and corrections (the call's own without LAYERS)
+    uint16_t *out_base = p.out;
+    float *corr_base = p.corr;
+    long long corr_stride = p.corr_row_stride;
+    if constexpr (LAYERS) {
+      const int l = op.meta[7];
+      out_base = p.out + l * lay.act_stride;
+      corr_base = reinterpret_cast<float *>(lay.corr[l]);
+      corr_stride = lay.corr_stride[l];
+    }
     // (the window is re-read from the ops buffer where it is used: fewer
     // registers live across the passes)
     auto window = [&](long long &tok0, int &qb) {
@@ -962,7 +1035,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       int qb;
       window(tok0, qb);
       if (c < qb)
-        *reinterpret_cast<uint2 *>(p.out + ((tok0 + c) * p.H + h) * kDim + R0) = make_uint2(0, 0);
+        *reinterpret_cast<uint2 *>(out_base + ((tok0 + c) * p.H + h) * kDim + R0) =
+            make_uint2(0, 0);
       stage_read(j, next_slot);
       warp_arrive(&sm.opempty[j % kWsOpsBufs]);
       consumed = j + 1;
@@ -984,6 +1058,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (n > 0) {
         float *gpage = reinterpret_cast<float *>(p.state) + (long long)slot * p.slot_stride +
                        (long long)h * (kDim * kDim);
+        if constexpr (LAYERS) {
+          const int l = op.meta[7];
+          gpage = reinterpret_cast<float *>(lay.state[l]) + (long long)slot * lay.slot_stride[l] +
+                  (long long)h * (kDim * kDim);
+        }
         float *gbnd = nullptr;
         if (BOUNDARY && bslot >= 0)
           gbnd = reinterpret_cast<float *>(p.state) + (long long)bslot * p.slot_stride +
@@ -1010,7 +1089,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     long long tok0;
     int qb;
     window(tok0, qb);
-    ws_solve<Q, NG, VARLEN>(d, op, p, tok0, qb, h, rec, R0, c, lane);
+    ws_solve<Q, NG, VARLEN>(d, op, p, out_base, corr_base, corr_stride, tok0, qb, h, rec, R0, c,
+                            lane);
     warp_arrive(&sm.opempty[j % kWsOpsBufs]);
   }
   if (failed && lane == 0) report(p.status, KDA_ERR_TIMEOUT);

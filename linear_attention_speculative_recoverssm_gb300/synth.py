@@ -176,6 +176,40 @@ def replay_verify_case(*, B, H, Q, slots, seed, RQ=None, rows=None, K=128,
     return case
 
 
+LAYER_STACKED = ("q", "k", "v", "raw_g", "raw_beta", "A_log", "dt_bias")
+SHARED_INDEX = ("state_slots", "record_rows", "pending")
+
+
+def layers_case(*, L, B, H, Q, slots, seed, **kw):
+    """Operands of one replay + verify step over L layers that share the
+    requests' slots, record rows and pending counts (a request has the same
+    slot and record row in every layer's pool).  ``layers`` holds L cases of
+    ``replay_verify_case`` (layer l drawn with seed + 1000 l, its state
+    drawn on layer 0's slots); the activations, A_log and dt_bias are also
+    given stacked over the layers ([L, ...], the multi-layer call's layout)."""
+    base = replay_verify_case(B=B, H=H, Q=Q, slots=slots, seed=seed, **kw)
+    layers = [base]
+    used = np.sort(base["state_slots"][base["state_slots"] > NULL_SLOT])
+    for l in range(1, L):
+        c = replay_verify_case(B=B, H=H, Q=Q, slots=slots, seed=seed + 1000 * l, **kw)
+        rng = np.random.default_rng(seed + 1000 * l + 17)
+        state = np.zeros_like(c["state"])
+        draw = _normal(rng, (len(used),) + c["state"].shape[1:], 0.05)
+        state[used] = draw if state.dtype == np.float32 else to_bf16_bits(draw)
+        del draw
+        c["state"] = state
+        for key in SHARED_INDEX + ("boundary_slots", "boundary_lens"):
+            c[key] = base[key]
+        layers.append(c)
+    case = {key: np.stack([c[key] for c in layers]) for key in LAYER_STACKED}
+    for key in SHARED_INDEX:
+        case[key] = base[key]
+    case.update(layers=layers, L=L, B=B, H=H, Q=Q, RQ=base["RQ"],
+                lower_bound=base["lower_bound"], q_scale=base["q_scale"],
+                null_slot=base["null_slot"])
+    return case
+
+
 WINDOW_KEYS = ("q", "k", "v", "raw_g", "raw_beta")
 
 

@@ -96,6 +96,37 @@ def test_replay_verify_host_checks(lib):
     assert call(qsl=A, n_tokens=0) == _lib.KDA_OK  # zero tokens: nothing to do
 
 
+def test_replay_verify_layers_host_checks(lib):
+    # host arrays of per-layer addresses / strides (values only read, never
+    # dereferenced: every call below is refused before a launch)
+    def arr(vals, t=ctypes.c_void_p):
+        return (t * len(vals))(*vals)
+
+    def call(L=2, **over):
+        a = dict(q=A, k=A, v=A, g=A, beta=A, A_log=A, dt_bias=A, lb=-5.0, qs=0.088,
+                 pools=arr([A] * L), sstr=arr([2 * 128 * 128] * L, ctypes.c_int64), n_slots=4,
+                 slots=A, rows=A, pending=A, corrs=arr([A] * L), kgs=arr([A] * L),
+                 cstr=arr([2 * 2 * 128] * L, ctypes.c_int64),
+                 kstr=arr([2 * 2 * 256] * L, ctypes.c_int64), n_rows=2, rq=2, out=A, L=L, B=2,
+                 H=2, Q=2, null=0, status=None, stream=None)
+        a.update(over)
+        return lib.kda_replay_verify_layers(*a.values())
+
+    assert call(L=0) == _lib.KDA_ERR_ARG
+    assert call(L=65) == _lib.KDA_ERR_ARG
+    assert call(pools=None) == _lib.KDA_ERR_ARG
+    assert call(pools=arr([A, None])) == _lib.KDA_ERR_ARG
+    assert call(sstr=arr([2 * 128 * 128, 100], ctypes.c_int64)) == _lib.KDA_ERR_ARG
+    assert call(cstr=arr([2 * 2 * 128, -512], ctypes.c_int64)) == _lib.KDA_ERR_ARG
+    assert call(kgs=arr([A, A + 8])) == _lib.KDA_ERR_ALIGN
+    assert call(sstr=arr([2 * 128 * 128, 2 * 128 * 128 + 1], ctypes.c_int64)) == \
+        _lib.KDA_ERR_ALIGN
+    assert call(pending=None) == _lib.KDA_ERR_ARG
+    assert call(lb=-11.0) == _lib.KDA_ERR_UNSUPPORTED
+    assert call(Q=9) == _lib.KDA_ERR_ARG
+    assert call(B=0) == _lib.KDA_OK
+
+
 def test_commit_and_bookkeeping_host_checks(lib):
     P = [A] * 14
     assert lib.kda_commit(*P, 5, -5.0, 0, 1, 2, 2, 2, 4, 2, None, None) == _lib.KDA_ERR_UNSUPPORTED
