@@ -664,20 +664,49 @@ def measure_layer(dev, stream, dt, peak):
         prologue()
         core()
         epilogue()
+
+    # the fused layer entry point: the same prologue into a workspace, then
+    # the step with the gated RMSNorm folded into its row solve
+    from linear_attention_speculative_recoverssm_gb300 import (kda_layer_step,
+                                                               kda_layer_step_workspace_bytes)
+    workspace = torch.empty(kda_layer_step_workspace_bytes(c["B"], c["H"], c["Q"]),
+                            dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def fused_layer():
+        kda_layer_step(d["x"], d["conv_weight"], d["conv_bias"], d["conv_state"], d["f_a"],
+                       d["f_b"], d["raw_beta"], d["A_log"], d["dt_bias"], d["state"],
+                       d["state_slots"], d["record_rows"], d["pending"], d["corr"],
+                       d["key_gate"], d["gate"], d["norm_weight"], out, workspace, Q=c["Q"],
+                       lower_bound=c["lower_bound"], q_scale=c["q_scale"], eps=c["eps"],
+                       status=status, stream=stream)
     for _ in range(3):
         layer()
+        fused_layer()
     ms = {"layer": _event_ms(stream, layer, 20), "prologue": _event_ms(stream, prologue, 20),
-          "step": _event_ms(stream, core, 20), "epilogue": _event_ms(stream, epilogue, 20)}
+          "step": _event_ms(stream, core, 20), "epilogue": _event_ms(stream, epilogue, 20),
+          "fused_layer": _event_ms(stream, fused_layer, 20)}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"fused layer step: device status {int(status.item())}")
     pro_b, epi_b = layer_algorithmic_bytes(c)
     step_b = algorithmic_bytes(c)
     total = pro_b + step_b["total"] + epi_b
     gbs = total / ms["layer"] / 1e6
+    # fused: the epilogue's read of o and write of the output are gone; the
+    # step reads the gate and writes the normed output in place of o
+    fused_b = pro_b + step_b["total"] + c["gate"].nbytes
+    fused_gbs = fused_b / ms["fused_layer"] / 1e6
     return dict(
         workload=name, ms=ms, tok_s=step_b["live_tokens"] / (ms["layer"] / 1e3),
-        bytes_per_launch=dict(prologue=pro_b, step=step_b["total"], epilogue=epi_b),
+        bytes_per_launch=dict(prologue=pro_b, step=step_b["total"], epilogue=epi_b,
+                              fused_layer=fused_b),
         roofline=dict(bound="hbm", achieved=gbs, peak=peak, unit="GB/s", frac=gbs / peak),
         prologue_roofline_frac=pro_b / ms["prologue"] / 1e6 / peak,
-        epilogue_roofline_frac=epi_b / ms["epilogue"] / 1e6 / peak)
+        epilogue_roofline_frac=epi_b / ms["epilogue"] / 1e6 / peak,
+        fused_layer=dict(ms=ms["fused_layer"],
+                         tok_s=step_b["live_tokens"] / (ms["fused_layer"] / 1e3),
+                         roofline=dict(bound="hbm", achieved=fused_gbs, peak=peak, unit="GB/s",
+                                       frac=fused_gbs / peak)))
 
 
 def decode_loop_bytes(c, eager):

@@ -369,6 +369,58 @@ int kda_layer_epilogue(const kda_bf16 *o, const kda_bf16 *gate,
                        const float *norm_weight, float eps, kda_bf16 *out,
                        int n_tokens, int H, void *stream);
 
+/*
+ * kda_layer_step_workspace_bytes -- the workspace kda_layer_step needs for
+ * B requests, H heads and windows of Q tokens: the step's operands q, k, v
+ * and raw_g, 4 * B*Q * H * 128 BF16 values.  -1 for sizes out of range.
+ */
+int64_t kda_layer_step_workspace_bytes(int B, int H, int Q);
+
+/*
+ * kda_layer_step -- one model-layer step of the KDA RecoverSSM ("kda.fused"
+ * page, KdaFused.kernel: the convolution operands, convolution and SiLU,
+ * gate projection, the recurrence, and the gated RMSNorm at the kernel's
+ * end).  Computes what kda_layer_prologue, kda_replay_verify and
+ * kda_layer_epilogue compute one after the other, in two launches: the
+ * prologue writes the step's q, k, v, raw_g into `workspace`, and the step
+ * kernel folds the gated RMSNorm into its row solve, so the recurrence
+ * outputs o never leave the chip:
+ *   out[t, h*128 + r] = BF16(o * rsqrt(sum_r o^2 / 128 + eps) *
+ *                            norm_weight[r] * sigmoid(gate[t, h*128 + r]))
+ * with o the BF16-rounded recurrence output of token t, head h, row r.
+ *   x, conv_weight, conv_bias, conv_state, conv_slot_stride, f_a, f_b  as in
+ *                 kda_layer_prologue (the window is rolled by the pending
+ *                 count and rewritten)
+ *   raw_beta, A_log, dt_bias, lower_bound, q_scale, state_pool,
+ *   slot_stride, n_slots, state_slots, record_rows, pending, corr,
+ *   key_gate, corr_row_stride, kg_row_stride, n_rows, rq  as in
+ *                 kda_replay_verify (uniform windows, no boundary states;
+ *                 records and pending required)
+ *   gate [B*Q, H*128] BF16; norm_weight [128] FP32; eps >= 0
+ *   out  [B*Q, H*128] BF16 (inert requests: zeros)
+ *   workspace  device, 16-byte aligned, at least
+ *              kda_layer_step_workspace_bytes(B, H, Q) bytes, owned by the
+ *              caller; its contents are overwritten (after the call it holds
+ *              the step's q, k, v, raw_g, [B*Q, H, 128] BF16 each, in that
+ *              order)
+ * Returns KDA_ERR_ARG for a missing or short workspace, as well as every
+ * code of the three calls it stands for.
+ */
+int kda_layer_step(const kda_bf16 *x, const kda_bf16 *conv_weight,
+                   const kda_bf16 *conv_bias, kda_bf16 *conv_state,
+                   int64_t conv_slot_stride, const kda_bf16 *f_a,
+                   const kda_bf16 *f_b, const kda_bf16 *raw_beta,
+                   const float *A_log, const float *dt_bias, float lower_bound,
+                   float q_scale, float *state_pool, int64_t slot_stride,
+                   int n_slots, const int32_t *state_slots,
+                   const int32_t *record_rows, const int32_t *pending,
+                   float *corr, kda_bf16 *key_gate, int64_t corr_row_stride,
+                   int64_t kg_row_stride, int n_rows, int rq,
+                   const kda_bf16 *gate, const float *norm_weight, float eps,
+                   kda_bf16 *out, void *workspace, int64_t workspace_bytes,
+                   int B, int H, int Q, int null_slot, int32_t *status,
+                   void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,6 +24,8 @@ from ._lib import (  # noqa: F401
     kda_flush_plan,
     kda_layer_epilogue,
     kda_layer_prologue,
+    kda_layer_step,
+    kda_layer_step_workspace_bytes,
     kda_replay_verify,
     kda_replay_verify_layers,
     kda_selftest_wait_timeout,

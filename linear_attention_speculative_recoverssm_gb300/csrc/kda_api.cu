@@ -188,6 +188,9 @@ kda::StepParams make_params(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16
   p.H = H;
   p.null_slot = null_slot;
   p.status = status;
+  p.gate = nullptr;
+  p.norm_w = nullptr;
+  p.norm_eps = 0.f;
   return p;
 }
 
@@ -343,6 +346,54 @@ int kda_replay_verify_layers(const kda_bf16 *q, const kda_bf16 *k, const kda_bf1
       key_gates[0], corr_row_strides[0], kg_row_strides[0], n_rows, rq, nullptr, nullptr, out, B,
       H, null_slot, status);
   return kda::launch_step_layers(p, lay, L * B * H, Q, static_cast<cudaStream_t>(stream));
+}
+
+int64_t kda_layer_step_workspace_bytes(int B, int H, int Q) {
+  if (B < 0 || H < 1 || Q < 1 || Q > KDA_MAX_WINDOW) return -1;
+  return 4LL * B * Q * H * KDA_HEAD_DIM * (int64_t)sizeof(kda_bf16);
+}
+
+int kda_layer_step(const kda_bf16 *x, const kda_bf16 *conv_weight, const kda_bf16 *conv_bias,
+                   kda_bf16 *conv_state, int64_t conv_slot_stride, const kda_bf16 *f_a,
+                   const kda_bf16 *f_b, const kda_bf16 *raw_beta, const float *A_log,
+                   const float *dt_bias, float lower_bound, float q_scale, float *state_pool,
+                   int64_t slot_stride, int n_slots, const int32_t *state_slots,
+                   const int32_t *record_rows, const int32_t *pending, float *corr,
+                   kda_bf16 *key_gate, int64_t corr_row_stride, int64_t kg_row_stride,
+                   int n_rows, int rq, const kda_bf16 *gate, const float *norm_weight,
+                   float eps, kda_bf16 *out, void *workspace, int64_t workspace_bytes, int B,
+                   int H, int Q, int null_slot, int32_t *status, void *stream) {
+  if (!gate_bound_ok(lower_bound)) return KDA_ERR_UNSUPPORTED;
+  if (!(eps >= 0.0f)) return KDA_ERR_ARG;  // (false for NaN)
+  const int64_t need = kda_layer_step_workspace_bytes(B, H, Q);
+  if (need < 0) return KDA_ERR_ARG;
+  if (B == 0) return KDA_OK;
+  if (!workspace || workspace_bytes < need || !gate || !norm_weight || !record_rows || !pending)
+    return KDA_ERR_ARG;
+  if (!aligned16(workspace) || !aligned16(gate) || !aligned16(norm_weight)) return KDA_ERR_ALIGN;
+  // the step's operands q, k, v, raw_g, made by the prologue in the workspace
+  const int64_t part = need / 4 / (int64_t)sizeof(kda_bf16);
+  kda_bf16 *wq = static_cast<kda_bf16 *>(workspace);
+  kda_bf16 *wk = wq + part, *wv = wk + part, *wg = wv + part;
+  const int n_tokens = B * Q;
+  int rc = check_step_args(wq, wk, wv, wg, raw_beta, A_log, dt_bias, state_pool, 4, slot_stride,
+                           n_slots, state_slots, corr, key_gate, corr_row_stride, kg_row_stride,
+                           n_rows, rq, out, B, H, Q, nullptr, n_tokens);
+  if (rc == kNothingToDo) return KDA_OK;
+  if (rc != KDA_OK) return rc;
+  rc = kda_layer_prologue(x, conv_weight, conv_bias, conv_state, conv_slot_stride, f_a, f_b,
+                          state_slots, record_rows, pending, n_slots, n_rows, rq, wq, wk, wv, wg,
+                          B, H, Q, null_slot, status, stream);
+  if (rc != KDA_OK) return rc;
+  kda::StepParams p = make_params(wq, wk, wv, wg, raw_beta, A_log, dt_bias, lower_bound,
+                                  q_scale, state_pool, slot_stride, n_slots, state_slots, nullptr,
+                                  n_tokens, record_rows, pending, corr, key_gate,
+                                  corr_row_stride, kg_row_stride, n_rows, rq, nullptr, nullptr,
+                                  out, B, H, null_slot, status);
+  p.gate = gate;
+  p.norm_w = norm_weight;
+  p.norm_eps = eps;
+  return kda::launch_step(p, B * H, Q, 4, 1, static_cast<cudaStream_t>(stream));
 }
 
 int kda_commit(const uint64_t *state_ptrs, const uint64_t *corr_ptrs, const uint64_t *kg_ptrs,

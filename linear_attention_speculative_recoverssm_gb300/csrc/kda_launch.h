@@ -16,6 +16,8 @@ int device_sm_count(int dev);
 // The replay / verify step for window Q (1..8).
 //   variant 0: verify only, FP32 pool      1: verify only, BF16 pool
 //           2: replay + verify (FP32)      3: replay + verify + boundary
+//           4: replay + verify with the gated RMSNorm folded in (split 1,
+//              uniform windows)
 //   split   1: persistent CTAs; 2 / 4: cluster of that many CTAs per item.
 int launch_step(const StepParams &p, int n_items, int Q, int variant, int split,
                 cudaStream_t stream);

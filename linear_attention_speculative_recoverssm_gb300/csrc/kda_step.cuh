@@ -35,6 +35,12 @@ struct StepParams {
   uint16_t *out;
   int B, H, null_slot;
   int32_t *status;
+  // the gated RMSNorm folded into the step (the NORM instances only):
+  // out[t, h*128 + r] = BF16(o * rsqrt(mean_r o^2 + norm_eps) * norm_w[r] *
+  // sigmoid(gate[t, h*128 + r])), o the BF16-rounded recurrence output
+  const uint16_t *gate;  // [n_tokens, H*128] BF16 bits
+  const float *norm_w;   // [128]
+  float norm_eps;
 };
 
 // The multi-layer step: one launch over L layers whose items are

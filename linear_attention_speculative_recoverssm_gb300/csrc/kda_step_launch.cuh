@@ -76,10 +76,11 @@ int encode_layer_token_maps(const StepParams &p, const LayerBases &lay, WsMaps &
   return KDA_OK;
 }
 
-template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN, bool LAYERS = false>
+template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN, bool LAYERS = false,
+          bool NORM = false>
 int launch_ws(const StepParams &p, int n_items, cudaStream_t stream,
               const LayerBases *bases = nullptr) {
-  auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY, VARLEN, LAYERS>;
+  auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY, VARLEN, LAYERS, NORM>;
   constexpr size_t smem = sizeof(WsSmem<Q, ST, BOUNDARY>);
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -146,7 +147,8 @@ int launch_cluster(const StepParams &p, int n_items, cudaStream_t stream) {
 }
 
 // The persistent kernel for one variant: 0 verify (FP32 state), 1 verify
-// (BF16 state), 2 replay + verify, 3 replay + verify with boundary states.
+// (BF16 state), 2 replay + verify, 3 replay + verify with boundary states,
+// 4 replay + verify with the gated RMSNorm folded in (uniform windows).
 template <int Q, bool VARLEN>
 int launch_ws_variant(const StepParams &p, int n_items, int variant, cudaStream_t stream) {
   switch (variant) {
@@ -154,6 +156,9 @@ int launch_ws_variant(const StepParams &p, int n_items, int variant, cudaStream_
     case 1: return launch_ws<Q, uint16_t, false, false, VARLEN>(p, n_items, stream);
     case 2: return launch_ws<Q, float, true, false, VARLEN>(p, n_items, stream);
     case 3: return launch_ws<Q, float, true, true, VARLEN>(p, n_items, stream);
+    case 4:
+      if constexpr (VARLEN) return KDA_ERR_UNSUPPORTED;
+      else return launch_ws<Q, float, true, false, false, false, true>(p, n_items, stream);
     default: return KDA_ERR_ARG;
   }
 }
@@ -166,7 +171,7 @@ template <int Q, bool VARLEN>
 int launch_step_q(const StepParams &p, int n_items, int variant, int split,
                   cudaStream_t stream) {
   if (split == 1) return launch_ws_variant<Q, VARLEN>(p, n_items, variant, stream);
-  if (variant != 2 && variant != 3) return KDA_ERR_UNSUPPORTED;
+  if (variant != 2 && variant != 3) return KDA_ERR_UNSUPPORTED;  // (the norm: split 1 only)
   const bool bnd = variant == 3;
   if (split == 2)
     return bnd ? launch_cluster<Q, 2, true, VARLEN>(p, n_items, stream)

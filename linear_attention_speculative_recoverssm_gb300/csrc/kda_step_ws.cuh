@@ -154,6 +154,12 @@ struct WsSmem {
   uint64_t opempty[kWsOpsBufs];
   uint64_t infull[2];
   int next_meta[8];  // resolved index chain of the next item to request
+  // the folded gated RMSNorm: each main warp's sum of squares of its 16 rows
+  // of every token's outputs, per ops buffer, completed on nred[buf] (one
+  // arrival per main warp); the norm weights
+  uint64_t nred[kWsOpsBufs];
+  float nsq[kWsOpsBufs][8][kMaxQ];
+  float norm_w[kDim];
 };
 
 // Every member read or written as float4 (or as a bulk-copy target) must sit
@@ -383,11 +389,14 @@ __device__ __forceinline__ void ws_dots(const float4 (&s)[4][4], const float *__
 // is broadcast to the row group and folded into every lane's residual (the
 // A coefficient is 0 for s >= t) and outputs (the B coefficient is 0 for
 // s > t).  Writes o_t (BF16) and, with a record row, u_t (FP32).
-template <int Q, int NG, bool VARLEN, typename Ops>
+// NORM: the outputs are not stored; the lane's BF16-rounded outputs (at
+// most one token per lane) go to obf / tout (-1: none) for the norm.
+template <int Q, int NG, bool VARLEN, bool NORM, typename Ops>
 __device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
                                          const StepParams &p, uint16_t *out, float *corr,
                                          long long corr_row_stride, long long tok0, int qb,
-                                         int h, int rec, int R0, int c, int lane) {
+                                         int h, int rec, int R0, int c, int lane,
+                                         float (&obf)[4], int &tout) {
   const int cw = c < Q ? c : Q - 1;  // lanes without a w role compute unused values
   const uint2 vb = *reinterpret_cast<const uint2 *>(&op.vv[cw][R0]);
   const float4 v4 = make_float4(__uint_as_float(vb.x << 16), __uint_as_float(vb.x & 0xffff0000u),
@@ -425,12 +434,24 @@ __device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
 #pragma unroll
       for (int r = 0; r < 4; ++r) oacc[g][r] = fmaf(bcoef[g][s2], us[r], oacc[g][r]);
   }
+  if constexpr (NORM) {
+    tout = -1;
 #pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    if (hy[g] && (!VARLEN || ty[g] < qb)) {
-      const uint2 o2 = make_uint2(pack_bf16x2(oacc[g][0], oacc[g][1]),
-                                  pack_bf16x2(oacc[g][2], oacc[g][3]));
-      *reinterpret_cast<uint2 *>(out + ((tok0 + ty[g]) * p.H + h) * kDim + R0) = o2;
+    for (int g = 0; g < NG; ++g) {
+      if (hy[g]) {  // (a lane holds at most one output token)
+        tout = ty[g];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) obf[r] = bf16_bits_to_f32(f32_to_bf16_bits(oacc[g][r]));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      if (hy[g] && (!VARLEN || ty[g] < qb)) {
+        const uint2 o2 = make_uint2(pack_bf16x2(oacc[g][0], oacc[g][1]),
+                                    pack_bf16x2(oacc[g][2], oacc[g][3]));
+        *reinterpret_cast<uint2 *>(out + ((tok0 + ty[g]) * p.H + h) * kDim + R0) = o2;
+      }
     }
   }
   if ((VARLEN ? c < qb : c < Q) && rec >= 0) {
@@ -445,12 +466,19 @@ __device__ __forceinline__ void ws_solve(const float (&d)[NG][4], const Ops &op,
 // LAYERS: items (layer, request, head) over the layers of `lay` (uniform
 // windows, FP32 state, no boundary states); the meta words carry the layer
 // in place of the window length.
-template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN, bool LAYERS>
+// NORM: the model layer's gated RMSNorm folded into the row solve (uniform
+// windows, FP32 state, no boundary states): the main warps exchange their
+// rows' sums of squares per token through shared memory (nred), and write
+// the normed, gated outputs instead of o.
+template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN, bool LAYERS,
+          bool NORM = false>
 __global__ void __launch_bounds__(kWsThreads, 1)
     kda_step_ws(const StepParams p, const __grid_constant__ WsMaps maps,
                 const __grid_constant__ WsLayers<LAYERS> lay, int n_items) {
   static_assert(!LAYERS || (!VARLEN && !BOUNDARY && REPLAY && sizeof(ST) == 4),
                 "the multi-layer step: uniform windows, FP32 state, no boundary");
+  static_assert(!NORM || (!VARLEN && !BOUNDARY && !LAYERS && REPLAY && sizeof(ST) == 4),
+                "the folded norm: uniform windows, FP32 state, one layer, no boundary");
   using Smem = WsSmem<Q, ST, BOUNDARY>;
   using Ops = WsOps<Q, BOUNDARY>;
   static_assert(WsLayoutCheck<Q, ST, BOUNDARY>::ok, "layout");
@@ -504,7 +532,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     }
     mbar_init(&sm.infull[0], 1);  // thread 0's arrival with the copies' byte count
     mbar_init(&sm.infull[1], 1);
+    if constexpr (NORM) {
+      for (int b = 0; b < kWsOpsBufs; ++b) mbar_init(&sm.nred[b], 8);  // one per main warp
+    }
     mbar_init_fence();
+  }
+  if constexpr (NORM) {
+    if (tid < kDim) sm.norm_w[tid] = p.norm_w[tid];
   }
   // the padding dot vectors (rows 2Q .. of x) stay zero in both ops buffers
   constexpr int kPadFloats = (ws_vectors<Q>() - 2 * Q) * kDim;
@@ -1018,6 +1052,20 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       qb = VARLEN ? op.meta[7] : Q;
     };
 
+    // NORM: this lane's output token's gate values, loaded now and used
+    // after the solve (token c - Q or 8 + c - Q of the window; none if
+    // neither is one)
+    uint2 gate_raw = make_uint2(0, 0);
+    if constexpr (NORM) {
+      if (slot >= 0) {
+        const int V = c >= Q ? c : 8 + c;
+        if (V >= Q && V < 2 * Q) {
+          const long long tok = (long long)op.meta[0] * Q + (V - Q);
+          gate_raw = *reinterpret_cast<const uint2 *>(p.gate + (tok * p.H + h) * kDim + R0);
+        }
+      }
+    }
+
     if (slot < 0) {
       // inert item: zero outputs (lane c: token c of its 4 rows).  Its
       // stage phase is an arrival without a copy, made when the item was
@@ -1038,6 +1086,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         *reinterpret_cast<uint2 *>(out_base + ((tok0 + c) * p.H + h) * kDim + R0) =
             make_uint2(0, 0);
       stage_read(j, next_slot);
+      // the norm's barrier phase of this ops buffer completes here too (its
+      // phases follow the items), with nothing to exchange
+      if constexpr (NORM) warp_arrive(&sm.nred[j % kWsOpsBufs]);
       warp_arrive(&sm.opempty[j % kWsOpsBufs]);
       consumed = j + 1;
       continue;
@@ -1089,8 +1140,46 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     long long tok0;
     int qb;
     window(tok0, qb);
-    ws_solve<Q, NG, VARLEN>(d, op, p, out_base, corr_base, corr_stride, tok0, qb, h, rec, R0, c,
-                            lane);
+    float obf[4] = {0.f, 0.f, 0.f, 0.f};
+    int tout = -1;
+    ws_solve<Q, NG, VARLEN, NORM>(d, op, p, out_base, corr_base, corr_stride, tok0, qb, h, rec,
+                                  R0, c, lane, obf, tout);
+    if constexpr (NORM) {
+      // gated RMSNorm over the 128 value rows of each token (page
+      // "...kda.fused", the kernel's end): the warp's 16 rows reduced over
+      // its 4 row sets, exchanged with the other main warps, summed in warp
+      // order (every lane of a token gets the same total)
+      float sq = 0.f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) sq = fmaf(obf[r], obf[r], sq);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 8);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 16);
+      const int mw = mt >> 5;
+      if (lane < 8 && tout >= 0) sm.nsq[j % kWsOpsBufs][mw][tout] = sq;
+      warp_arrive(&sm.nred[j % kWsOpsBufs]);
+      ok = mbar_wait_bounded(&sm.nred[j % kWsOpsBufs], (uint32_t)((j / kWsOpsBufs) & 1));
+      if (__any_sync(0xffffffffu, !ok)) {
+        failed = true;
+        break;
+      }
+      if (tout >= 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < 8; ++w2) tot += sm.nsq[j % kWsOpsBufs][w2][tout];
+        const float rstd = rsqrtf(tot * (1.0f / kDim) + p.norm_eps);
+        const float4 w4 = lds4(&sm.norm_w[R0]);
+        const float g0 = bf16_bits_to_f32(gate_raw.x & 0xffffu);
+        const float g1 = bf16_bits_to_f32(gate_raw.x >> 16);
+        const float g2 = bf16_bits_to_f32(gate_raw.y & 0xffffu);
+        const float g3 = bf16_bits_to_f32(gate_raw.y >> 16);
+        const uint2 o2 = make_uint2(
+            pack_bf16x2(obf[0] * rstd * w4.x * sigmoidf_fast(g0),
+                        obf[1] * rstd * w4.y * sigmoidf_fast(g1)),
+            pack_bf16x2(obf[2] * rstd * w4.z * sigmoidf_fast(g2),
+                        obf[3] * rstd * w4.w * sigmoidf_fast(g3)));
+        *reinterpret_cast<uint2 *>(out_base + ((tok0 + tout) * p.H + h) * kDim + R0) = o2;
+      }
+    }
     warp_arrive(&sm.opempty[j % kWsOpsBufs]);
   }
   if (failed && lane == 0) report(p.status, KDA_ERR_TIMEOUT);

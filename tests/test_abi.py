@@ -24,7 +24,7 @@ def _declared():
     for f in os.listdir(inc):
         if f.endswith(".h"):
             text = open(os.path.join(inc, f)).read()
-            names += re.findall(r"^(?:int|const char \*)\s*(kda_\w+)\s*\(", text, re.M)
+            names += re.findall(r"^(?:int|int64_t|const char \*)\s*(kda_\w+)\s*\(", text, re.M)
     return sorted(set(names))
 
 

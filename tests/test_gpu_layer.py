@@ -197,3 +197,128 @@ def test_layer_prologue_full_size_sampled():
     items = np.sort(rng.choice(case["B"] * case["H"], size=96, replace=False))
     ref, ref_state = _oracle_prologue(case, items=items)
     _compare_prologue(case, d, ref, ref_state, items=items)
+
+
+# --------------------------------------------------------------------------
+# the fused layer step: prologue into a workspace, then the step with the
+# gated RMSNorm folded into its row solve
+# --------------------------------------------------------------------------
+
+def _fused_layer(case, d, step, out, workspace):
+    from linear_attention_speculative_recoverssm_gb300 import kda_layer_step
+    kda_layer_step(d["x"], d["conv_weight"], d["conv_bias"], d["conv_state"], d["f_a"], d["f_b"],
+                   step["raw_beta"], step["A_log"], step["dt_bias"], step["state"],
+                   step["state_slots"], step["record_rows"], step["pending"], step["corr"],
+                   step["key_gate"], d["gate"], d["norm_weight"], out, workspace, Q=case["Q"],
+                   lower_bound=case["lower_bound"], q_scale=case["q_scale"], eps=case["eps"],
+                   status=step["status"])
+
+
+def _check_fused_layer(case, d, step, out, workspace, items=None):
+    """Stage by stage: the workspace's q, k, v, raw_g against the oracle's
+    prologue (one BF16 step), the pool, records and windows against the
+    oracle's step on the GPU's own q, k, v, raw_g, and the layer output
+    against the oracle's gated norm of that step's outputs (rel-L2 <= 2e-3,
+    overall and per (request, head) item)."""
+    B, H, Q = case["B"], case["H"], case["Q"]
+    T = B * Q
+    ws = tu.to_numpy(workspace).reshape(4, T, H, 128)
+    for i, key in enumerate(("q", "k", "v", "raw_g")):
+        d[key] = tu.to_torch(ws[i], "cuda")
+    ref, ref_state = _oracle_prologue(case, items=items)
+    _compare_prologue(case, d, ref, ref_state, items=items)
+    # (on sampled items the oracle may update the case's own arrays: the
+    # whole-pool comparisons below need the copies only without sampling)
+    before = tu.copy_case(case) if items is None else None
+    stage = tu.copy_case(case) if items is None else dict(case)
+    for i, key in enumerate(("q", "k", "v", "raw_g")):
+        a = ws[i].copy()
+        a[a == SENTINEL] = 0
+        stage[key] = a
+    o_ref = np.zeros((T, H, 128), dtype=np.uint16)
+    ko.replay_verify(q=stage["q"], k=stage["k"], v=stage["v"], raw_g=stage["raw_g"],
+                     raw_beta=stage["raw_beta"], A_log=stage["A_log"],
+                     dt_bias=stage["dt_bias"], lower_bound=stage["lower_bound"],
+                     q_scale=stage["q_scale"], state=stage["state"],
+                     state_slots=stage["state_slots"], record_rows=stage["record_rows"],
+                     corr=stage["corr"], key_gate=stage["key_gate"], out=o_ref, B=B, H=H, Q=Q,
+                     pending=stage["pending"], items=items)
+    ref_out = ko.layer_epilogue(o=o_ref, gate=case["gate"], norm_weight=case["norm_weight"],
+                                eps=case["eps"]).reshape(T, H, 128)
+    got_out = tu.to_numpy(out).reshape(T, H, 128)
+    if items is None:
+        tu.assert_out_close(got_out, ref_out, what="layer output", Q=Q)
+        stage["out"] = o_ref
+        # the step's state and records (its outputs were normed in place)
+        view = dict(step, out=tu.to_torch(o_ref, "cuda"))
+        tu.compare_step(stage, view, before)
+    else:
+        for i in items:
+            b, h = divmod(int(i), H)
+            rows = slice(b * Q, (b + 1) * Q)
+            tu.assert_out_close(got_out[rows, h], ref_out[rows, h], what=f"item {i}")
+            s = int(case["state_slots"][b])
+            if s > 0:
+                tu.assert_state_close(tu.to_numpy(step["state"][s, h]), stage["state"][s, h],
+                                      what=f"item {i} state")
+    assert int(tu.to_numpy(step["status"])[0]) == 0
+
+
+@pytest.mark.parametrize("Q,bias,RQ", [(8, True, 8), (4, False, 4), (1, True, 1), (5, True, 7),
+                                       (3, False, 3)])
+def test_fused_layer_step(Q, bias, RQ):
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import kda_layer_step_workspace_bytes
+    case = synth.layer_case(B=12, H=3, Q=Q, slots=32, seed=95 + Q, bias=bias, padding_frac=0.15,
+                            no_record_frac=0.1, RQ=RQ)
+    d = _device_layer(case)
+    step = tu.device_case(case)
+    B, H = case["B"], case["H"]
+    nbytes = kda_layer_step_workspace_bytes(B, H, Q)
+    assert nbytes == 4 * B * Q * H * 128 * 2
+    workspace = tu.to_torch(np.full(nbytes // 2, SENTINEL, dtype=np.uint16), "cuda")
+    out = torch.full((B * Q, H * 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    _fused_layer(case, d, step, out, workspace)
+    torch.cuda.synchronize()
+    _check_fused_layer(case, d, step, out, workspace)
+
+
+def test_fused_layer_step_spread_key_norms_and_back_to_back():
+    """Spread key norms in the step's records; three launches back to back
+    (each reads the pool, records and windows the previous one wrote) against
+    three oracle layer steps."""
+    import torch
+    case = synth.layer_case(B=16, H=4, Q=6, slots=40, seed=120, padding_frac=0.2,
+                            key_norms="spread")
+    d = _device_layer(case)
+    step = tu.device_case(case)
+    from linear_attention_speculative_recoverssm_gb300 import kda_layer_step_workspace_bytes
+    nbytes = kda_layer_step_workspace_bytes(16, 4, 6)
+    workspace = tu.to_torch(np.full(nbytes // 2, SENTINEL, dtype=np.uint16), "cuda")
+    out = torch.zeros((16 * 6, 4 * 128), dtype=torch.bfloat16, device="cuda")
+    for it in range(3):
+        _fused_layer(case, d, step, out, workspace)
+        torch.cuda.synchronize()
+        _check_fused_layer(case, d, step, out, workspace)
+        # the next launch starts from what this one left (the oracle's copy
+        # of the pool, records and windows follows the GPU's)
+        for key in ("state", "corr", "key_gate"):
+            case[key] = tu.to_numpy(step[key]).copy()
+        case["conv_state"] = tu.to_numpy(d["conv_state"]).copy()
+
+
+def test_fused_layer_step_full_size_sampled():
+    """The benchmark's layer workload (H=64, B=512, Q=8) on sampled items."""
+    import torch
+    from linear_attention_speculative_recoverssm_gb300 import kda_layer_step_workspace_bytes
+    case = synth.make("layer-f32-h64-b512-q8")
+    B, H, Q = case["B"], case["H"], case["Q"]
+    d = _device_layer(case)
+    step = tu.device_case(case)
+    workspace = torch.full((kda_layer_step_workspace_bytes(B, H, Q) // 2,), SENTINEL,
+                           dtype=torch.int16, device="cuda")
+    out = torch.zeros((B * Q, H * 128), dtype=torch.bfloat16, device="cuda")
+    _fused_layer(case, d, step, out, workspace)
+    torch.cuda.synchronize()
+    items = np.sort(np.random.default_rng(17).choice(B * H, size=96, replace=False))
+    _check_fused_layer(case, d, step, out, workspace.view(torch.bfloat16), items=items)
