@@ -159,7 +159,7 @@ struct WsSmem {
   // arrival per main warp); the norm weights
   uint64_t nred[kWsOpsBufs];
   float nsq[kWsOpsBufs][8][kMaxQ];
-  float norm_w[kDim];
+  alignas(16) float norm_w[kDim];  // read as float4
 };
 
 // Every member read or written as float4 (or as a bulk-copy target) must sit
@@ -180,7 +180,9 @@ struct WsLayoutCheck {
                 offsetof(WsIn<Q>, tok) % 16 == 0 && offsetof(WsIn<Q>, kg) % 16 == 0 &&
                 offsetof(WsIn<Q>, corr) % 16 == 0, "bulk-copy targets");
   static_assert(offsetof(S, full) % 8 == 0 && offsetof(S, opfull) % 8 == 0 &&
-                offsetof(S, opempty) % 8 == 0 && offsetof(S, infull) % 8 == 0, "mbarriers");
+                offsetof(S, opempty) % 8 == 0 && offsetof(S, infull) % 8 == 0 &&
+                offsetof(S, nred) % 8 == 0, "mbarriers");
+  static_assert(offsetof(S, norm_w) % 16 == 0, "norm weights: float4 reads");
   static_assert(sizeof(S) <= 232448, "shared memory per CTA");
   static constexpr bool ok = true;
 };
