@@ -1022,6 +1022,38 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   int raw_ahead = -1;
   if (lane == 0 && NS < count) raw_ahead = raw_slot(NS);
   bool failed = false;
+  // NORM: a live item's outputs are normed during the next item (after its
+  // replay), so the wait for the other warps' sums of squares overlaps that
+  // work: its BF16-rounded outputs, gates, token, destination and barrier.
+  bool norm_pending = false;
+  float pn_o[4] = {0.f, 0.f, 0.f, 0.f};
+  uint2 pn_gate = make_uint2(0, 0);
+  int pn_tok = -1, pn_buf = 0;
+  uint32_t pn_par = 0;
+  uint16_t *pn_dst = nullptr;
+  auto norm_finish = [&]() -> bool {  // false: the wait gave up
+    if (!NORM || !norm_pending) return true;
+    norm_pending = false;
+    const bool done = mbar_wait_bounded(&sm.nred[pn_buf], pn_par);
+    if (__any_sync(0xffffffffu, !done)) return false;
+    if (pn_tok >= 0) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < 8; ++w2) tot += sm.nsq[pn_buf][w2][pn_tok];
+      const float rstd = rsqrtf(tot * (1.0f / kDim) + p.norm_eps);
+      const float4 w4 = lds4(&sm.norm_w[R0]);
+      const float g0 = bf16_bits_to_f32(pn_gate.x & 0xffffu);
+      const float g1 = bf16_bits_to_f32(pn_gate.x >> 16);
+      const float g2 = bf16_bits_to_f32(pn_gate.y & 0xffffu);
+      const float g3 = bf16_bits_to_f32(pn_gate.y >> 16);
+      *reinterpret_cast<uint2 *>(pn_dst) =
+          make_uint2(pack_bf16x2(pn_o[0] * rstd * w4.x * sigmoidf_fast(g0),
+                                 pn_o[1] * rstd * w4.y * sigmoidf_fast(g1)),
+                     pack_bf16x2(pn_o[2] * rstd * w4.z * sigmoidf_fast(g2),
+                                 pn_o[3] * rstd * w4.w * sigmoidf_fast(g3)));
+    }
+    return true;
+  };
   for (int j = 0; j < count; ++j) {
     int next_slot = -1;
     if (lane == 0 && j + NS < count) {
@@ -1090,7 +1122,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       stage_read(j, next_slot);
       // the norm's barrier phase of this ops buffer completes here too (its
       // phases follow the items), with nothing to exchange
-      if constexpr (NORM) warp_arrive(&sm.nred[j % kWsOpsBufs]);
+      if constexpr (NORM) {
+        if (!norm_finish()) {
+          failed = true;
+          break;
+        }
+        warp_arrive(&sm.nred[j % kWsOpsBufs]);
+      }
       warp_arrive(&sm.opempty[j % kWsOpsBufs]);
       consumed = j + 1;
       continue;
@@ -1134,6 +1172,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
     }
 
+    // the previous item's norm (its sums of squares are in by now)
+    if (!norm_finish()) {
+      failed = true;
+      break;
+    }
+
     // ---------------- pass B: 2Q dots per row ----------------------------
     float d[NG][4];
     ws_dots<NG>(st, &op.x[0][0], c, d);
@@ -1149,8 +1193,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     if constexpr (NORM) {
       // gated RMSNorm over the 128 value rows of each token (page
       // "...kda.fused", the kernel's end): the warp's 16 rows reduced over
-      // its 4 row sets, exchanged with the other main warps, summed in warp
-      // order (every lane of a token gets the same total)
+      // its 4 row sets and published; the other warps' sums are read, in
+      // warp order (every lane of a token gets the same total), when the
+      // next item's replay is done
       float sq = 0.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) sq = fmaf(obf[r], obf[r], sq);
@@ -1159,31 +1204,18 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const int mw = mt >> 5;
       if (lane < 8 && tout >= 0) sm.nsq[j % kWsOpsBufs][mw][tout] = sq;
       warp_arrive(&sm.nred[j % kWsOpsBufs]);
-      ok = mbar_wait_bounded(&sm.nred[j % kWsOpsBufs], (uint32_t)((j / kWsOpsBufs) & 1));
-      if (__any_sync(0xffffffffu, !ok)) {
-        failed = true;
-        break;
-      }
-      if (tout >= 0) {
-        float tot = 0.f;
+      norm_pending = true;
 #pragma unroll
-        for (int w2 = 0; w2 < 8; ++w2) tot += sm.nsq[j % kWsOpsBufs][w2][tout];
-        const float rstd = rsqrtf(tot * (1.0f / kDim) + p.norm_eps);
-        const float4 w4 = lds4(&sm.norm_w[R0]);
-        const float g0 = bf16_bits_to_f32(gate_raw.x & 0xffffu);
-        const float g1 = bf16_bits_to_f32(gate_raw.x >> 16);
-        const float g2 = bf16_bits_to_f32(gate_raw.y & 0xffffu);
-        const float g3 = bf16_bits_to_f32(gate_raw.y >> 16);
-        const uint2 o2 = make_uint2(
-            pack_bf16x2(obf[0] * rstd * w4.x * sigmoidf_fast(g0),
-                        obf[1] * rstd * w4.y * sigmoidf_fast(g1)),
-            pack_bf16x2(obf[2] * rstd * w4.z * sigmoidf_fast(g2),
-                        obf[3] * rstd * w4.w * sigmoidf_fast(g3)));
-        *reinterpret_cast<uint2 *>(out_base + ((tok0 + tout) * p.H + h) * kDim + R0) = o2;
-      }
+      for (int r = 0; r < 4; ++r) pn_o[r] = obf[r];
+      pn_gate = gate_raw;
+      pn_tok = tout;
+      pn_buf = j % kWsOpsBufs;
+      pn_par = (uint32_t)((j / kWsOpsBufs) & 1);
+      pn_dst = out_base + ((tok0 + (tout >= 0 ? tout : 0)) * p.H + h) * kDim + R0;
     }
     warp_arrive(&sm.opempty[j % kWsOpsBufs]);
   }
+  if (!failed && !norm_finish()) failed = true;  // the last item's norm
   if (failed && lane == 0) report(p.status, KDA_ERR_TIMEOUT);
   // After a timeout, pages this warp requested but never read may still be in
   // flight: let them land (bounded) before this CTA's shared memory goes.
