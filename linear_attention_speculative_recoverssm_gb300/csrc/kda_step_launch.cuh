@@ -81,7 +81,7 @@ template <int Q, typename ST, bool REPLAY, bool BOUNDARY, bool VARLEN, bool LAYE
 int launch_ws(const StepParams &p, int n_items, cudaStream_t stream,
               const LayerBases *bases = nullptr) {
   auto kern = kda_step_ws<Q, ST, REPLAY, BOUNDARY, VARLEN, LAYERS, NORM>;
-  constexpr size_t smem = sizeof(WsSmem<Q, ST, BOUNDARY>);
+  constexpr size_t smem = sizeof(WsSmem<Q, ST, BOUNDARY, NORM>);
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;

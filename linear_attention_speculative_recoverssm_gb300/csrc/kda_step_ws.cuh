@@ -55,6 +55,7 @@
 #include <cuda.h>
 
 #include <cstddef>
+#include <type_traits>
 
 #include "kda_step.cuh"
 
@@ -140,7 +141,7 @@ __host__ __device__ constexpr int ws_stages() {
 }
 
 template <int Q, typename ST, bool BOUNDARY>
-struct WsSmem {
+struct WsSmemBase {
   static constexpr int NS = ws_stages<ST>();
   ST stage[NS][kDim * kDim];
   WsOps<Q, BOUNDARY> ops[kWsOpsBufs];
@@ -154,19 +155,28 @@ struct WsSmem {
   uint64_t opempty[kWsOpsBufs];
   uint64_t infull[2];
   int next_meta[8];  // resolved index chain of the next item to request
-  // the folded gated RMSNorm: each main warp's sum of squares of its 16 rows
-  // of every token's outputs, per ops buffer, completed on nred[buf] (one
-  // arrival per main warp); the norm weights
+};
+
+// The NORM instances add the folded gated RMSNorm's exchange: each main
+// warp's sum of squares of its 16 rows of every token's outputs, per ops
+// buffer, completed on nred[buf] (one arrival per main warp); and the norm
+// weights.
+template <int Q, typename ST, bool BOUNDARY>
+struct WsSmemNorm : WsSmemBase<Q, ST, BOUNDARY> {
   uint64_t nred[kWsOpsBufs];
   float nsq[kWsOpsBufs][8][kMaxQ];
   alignas(16) float norm_w[kDim];  // read as float4
 };
 
+template <int Q, typename ST, bool BOUNDARY, bool NORM = false>
+using WsSmem = std::conditional_t<NORM, WsSmemNorm<Q, ST, BOUNDARY>, WsSmemBase<Q, ST, BOUNDARY>>;
+
 // Every member read or written as float4 (or as a bulk-copy target) must sit
 // on a 16-byte boundary; the barriers on 8.
 template <int Q, typename ST, bool BOUNDARY>
 struct WsLayoutCheck {
-  using S = WsSmem<Q, ST, BOUNDARY>;
+  using S = WsSmemBase<Q, ST, BOUNDARY>;
+  using SN = WsSmemNorm<Q, ST, BOUNDARY>;
   using O = WsOps<Q, BOUNDARY>;
   static_assert(sizeof(O) % 16 == 0, "ops buffers must stay 16-byte aligned");
   static_assert(offsetof(S, stage) % 128 == 0 && offsetof(S, ops) % 16 == 0, "stage / ops");
@@ -180,9 +190,9 @@ struct WsLayoutCheck {
                 offsetof(WsIn<Q>, tok) % 16 == 0 && offsetof(WsIn<Q>, kg) % 16 == 0 &&
                 offsetof(WsIn<Q>, corr) % 16 == 0, "bulk-copy targets");
   static_assert(offsetof(S, full) % 8 == 0 && offsetof(S, opfull) % 8 == 0 &&
-                offsetof(S, opempty) % 8 == 0 && offsetof(S, infull) % 8 == 0 &&
-                offsetof(S, nred) % 8 == 0, "mbarriers");
-  static_assert(offsetof(S, norm_w) % 16 == 0, "norm weights: float4 reads");
+                offsetof(S, opempty) % 8 == 0 && offsetof(S, infull) % 8 == 0, "mbarriers");
+  static_assert(offsetof(SN, nred) % 8 == 0 && offsetof(SN, norm_w) % 16 == 0 &&
+                sizeof(SN) <= 232448, "the norm's barriers and float4-read weights");
   static_assert(sizeof(S) <= 232448, "shared memory per CTA");
   static constexpr bool ok = true;
 };
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 "the multi-layer step: uniform windows, FP32 state, no boundary");
   static_assert(!NORM || (!VARLEN && !BOUNDARY && !LAYERS && REPLAY && sizeof(ST) == 4),
                 "the folded norm: uniform windows, FP32 state, one layer, no boundary");
-  using Smem = WsSmem<Q, ST, BOUNDARY>;
+  using Smem = WsSmem<Q, ST, BOUNDARY, NORM>;
   using Ops = WsOps<Q, BOUNDARY>;
   static_assert(WsLayoutCheck<Q, ST, BOUNDARY>::ok, "layout");
   constexpr int NS = Smem::NS;
@@ -1032,7 +1042,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   uint32_t pn_par = 0;
   uint16_t *pn_dst = nullptr;
   auto norm_finish = [&]() -> bool {  // false: the wait gave up
-    if (!NORM || !norm_pending) return true;
+    if constexpr (!NORM) return true;
+    else {
+    if (!norm_pending) return true;
     norm_pending = false;
     const bool done = mbar_wait_bounded(&sm.nred[pn_buf], pn_par);
     if (__any_sync(0xffffffffu, !done)) return false;
@@ -1053,6 +1065,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                                  pn_o[3] * rstd * w4.w * sigmoidf_fast(g3)));
     }
     return true;
+    }
   };
   for (int j = 0; j < count; ++j) {
     int next_slot = -1;
@@ -1069,16 +1082,20 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const Ops &op = sm.ops[j % kWsOpsBufs];
     const int h = op.meta[1], slot = op.meta[2], rec = op.meta[3];
     const int n = op.meta[4], bslot = op.meta[5], m = op.meta[6];
-    // the layer's outputs and corrections (the call's own without LAYERS)
-    uint16_t *out_base = p.out;
-    float *corr_base = p.corr;
-    long long corr_stride = p.corr_row_stride;
-    if constexpr (LAYERS) {
-      const int l = op.meta[7];
-      out_base = p.out + l * lay.act_stride;
-      corr_base = reinterpret_cast<float *>(lay.corr[l]);
-      corr_stride = lay.corr_stride[l];
-    }
+    // the layer's outputs and corrections (the call's own without LAYERS),
+    // formed where they are used
+    auto out_of = [&]() -> uint16_t * {
+      if constexpr (LAYERS) return p.out + op.meta[7] * lay.act_stride;
+      else return p.out;
+    };
+    auto corr_of = [&]() -> float * {
+      if constexpr (LAYERS) return reinterpret_cast<float *>(lay.corr[op.meta[7]]);
+      else return p.corr;
+    };
+    auto corr_stride_of = [&]() -> long long {
+      if constexpr (LAYERS) return lay.corr_stride[op.meta[7]];
+      else return p.corr_row_stride;
+    };
     // (the window is re-read from the ops buffer where it is used: fewer
     // registers live across the passes)
     auto window = [&](long long &tok0, int &qb) {
@@ -1117,7 +1134,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       int qb;
       window(tok0, qb);
       if (c < qb)
-        *reinterpret_cast<uint2 *>(out_base + ((tok0 + c) * p.H + h) * kDim + R0) =
+        *reinterpret_cast<uint2 *>(out_of() + ((tok0 + c) * p.H + h) * kDim + R0) =
             make_uint2(0, 0);
       stage_read(j, next_slot);
       // the norm's barrier phase of this ops buffer completes here too (its
@@ -1188,8 +1205,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     window(tok0, qb);
     float obf[4] = {0.f, 0.f, 0.f, 0.f};
     int tout = -1;
-    ws_solve<Q, NG, VARLEN, NORM>(d, op, p, out_base, corr_base, corr_stride, tok0, qb, h, rec,
-                                  R0, c, lane, obf, tout);
+    ws_solve<Q, NG, VARLEN, NORM>(d, op, p, out_of(), corr_of(), corr_stride_of(), tok0, qb, h,
+                                  rec, R0, c, lane, obf, tout);
     if constexpr (NORM) {
       // gated RMSNorm over the 128 value rows of each token (page
       // "...kda.fused", the kernel's end): the warp's 16 rows reduced over
@@ -1211,7 +1228,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       pn_tok = tout;
       pn_buf = j % kWsOpsBufs;
       pn_par = (uint32_t)((j / kWsOpsBufs) & 1);
-      pn_dst = out_base + ((tok0 + (tout >= 0 ? tout : 0)) * p.H + h) * kDim + R0;
+      pn_dst = out_of() + ((tok0 + (tout >= 0 ? tout : 0)) * p.H + h) * kDim + R0;
     }
     warp_arrive(&sm.opempty[j % kWsOpsBufs]);
   }
