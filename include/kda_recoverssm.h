@@ -73,6 +73,7 @@ extern "C" {
 #define KDA_ERR_UNSUPPORTED (-3)
 #define KDA_ERR_CUDA (-4)
 #define KDA_ERR_TIMEOUT (-5)
+#define KDA_ERR_SCRATCH (-6)
 
 #define KDA_STATE_F32 0
 #define KDA_STATE_BF16 1
@@ -420,6 +421,46 @@ int kda_layer_step(const kda_bf16 *x, const kda_bf16 *conv_weight,
                    kda_bf16 *out, void *workspace, int64_t workspace_bytes,
                    int B, int H, int Q, int null_slot, int32_t *status,
                    void *stream);
+
+/*
+ * kda_layer_step_noalloc -- kda_layer_step for callers that cannot allocate
+ * device memory when they call it (the pages have no counterpart: this is
+ * for this library's users).  A serving runtime that reserves all device
+ * memory in its own pool at start-up, or a plugin whose host framework owns
+ * every device allocation, may not call cudaMalloc on the decode path.
+ * This entry point takes the same arguments as kda_layer_step except the
+ * workspace: the step's operands go to a fixed array of device memory that
+ * belongs to the library, KDA_LAYER_STEP_NOALLOC_MAX_BYTES bytes, held on
+ * every GPU that loads the library until the process exits.  It allocates
+ * and frees nothing.
+ *  - Sizes: kda_layer_step_workspace_bytes(B, H, Q) must not exceed
+ *    KDA_LAYER_STEP_NOALLOC_MAX_BYTES (B * Q * H <= 16384 (token, head)
+ *    rows); larger calls return KDA_ERR_SCRATCH before anything is launched.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address, a runtime query; make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last
+ *    call's contents.  Nothing in it needs clearing (each call writes the
+ *    operands it then reads), but calls whose work overlaps on the GPU (on
+ *    different streams, or from different threads) race on it: order them.
+ *  - Every other argument, result and status code is kda_layer_step's.
+ */
+#define KDA_LAYER_STEP_NOALLOC_MAX_BYTES (16 * 1024 * 1024)
+int kda_layer_step_noalloc(const kda_bf16 *x, const kda_bf16 *conv_weight,
+                           const kda_bf16 *conv_bias, kda_bf16 *conv_state,
+                           int64_t conv_slot_stride, const kda_bf16 *f_a,
+                           const kda_bf16 *f_b, const kda_bf16 *raw_beta,
+                           const float *A_log, const float *dt_bias,
+                           float lower_bound, float q_scale, float *state_pool,
+                           int64_t slot_stride, int n_slots,
+                           const int32_t *state_slots,
+                           const int32_t *record_rows, const int32_t *pending,
+                           float *corr, kda_bf16 *key_gate,
+                           int64_t corr_row_stride, int64_t kg_row_stride,
+                           int n_rows, int rq, const kda_bf16 *gate,
+                           const float *norm_weight, float eps, kda_bf16 *out,
+                           int B, int H, int Q, int null_slot, int32_t *status,
+                           void *stream);
 
 #ifdef __cplusplus
 }

@@ -12,8 +12,10 @@ from ._lib import (  # noqa: F401
     KDA_ERR_ALIGN,
     KDA_ERR_ARG,
     KDA_ERR_CUDA,
+    KDA_ERR_SCRATCH,
     KDA_ERR_TIMEOUT,
     KDA_ERR_UNSUPPORTED,
+    KDA_LAYER_STEP_NOALLOC_MAX_BYTES,
     KDA_OK,
     KDA_STATE_BF16,
     KDA_STATE_F32,
@@ -25,6 +27,7 @@ from ._lib import (  # noqa: F401
     kda_layer_epilogue,
     kda_layer_prologue,
     kda_layer_step,
+    kda_layer_step_noalloc,
     kda_layer_step_workspace_bytes,
     kda_replay_verify,
     kda_replay_verify_layers,

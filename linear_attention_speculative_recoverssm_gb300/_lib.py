@@ -21,6 +21,8 @@ KDA_ERR_ALIGN = -2
 KDA_ERR_UNSUPPORTED = -3
 KDA_ERR_CUDA = -4
 KDA_ERR_TIMEOUT = -5
+KDA_ERR_SCRATCH = -6
+KDA_LAYER_STEP_NOALLOC_MAX_BYTES = 16 * 1024 * 1024
 KDA_STATE_F32 = 0
 KDA_STATE_BF16 = 1
 
@@ -28,7 +30,7 @@ EXPORTS = ("kda_abi_version", "kda_error_string", "kda_check_status", "kda_verif
            "kda_replay_verify", "kda_replay_verify_layers",
            "kda_commit", "kda_defer_commit", "kda_flush_plan", "kda_selftest_wait_timeout",
            "kda_layer_prologue", "kda_layer_epilogue", "kda_layer_step_workspace_bytes",
-           "kda_layer_step")
+           "kda_layer_step", "kda_layer_step_noalloc")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -54,6 +56,9 @@ _SIGS = {
                            + [_I, _I, _I, _I, _P, _P], _I),
     "kda_layer_epilogue": ([_P, _P, _P, _F, _P, _I, _I, _P], _I),
     "kda_layer_step_workspace_bytes": ([_I, _I, _I], _I64),
+    "kda_layer_step_noalloc": ([_P] * 4 + [_I64] + [_P] * 5 + [_F, _F, _P, _I64, _I, _P, _P, _P,
+                                                           _P, _P, _I64, _I64, _I, _I, _P, _P, _F,
+                                                           _P, _I, _I, _I, _I, _P, _P], _I),
     "kda_layer_step": ([_P] * 4 + [_I64] + [_P] * 5 + [_F, _F, _P, _I64, _I, _P, _P, _P, _P, _P,
                                                    _I64, _I64, _I, _I, _P, _P, _F, _P, _P, _I64,
                                                    _I, _I, _I, _I, _P, _P], _I),
@@ -351,3 +356,38 @@ def kda_layer_step(x, conv_weight, conv_bias, conv_state, f_a, f_b, raw_beta, A_
         key_gate.stride(0), corr.shape[0], rq, _ptr(gate), _ptr(norm_weight), eps, _ptr(out),
         _ptr(workspace), nbytes, B, H, Q, null_slot, _ptr(status), _stream(stream))
     return _check("kda_layer_step", rc, raise_on_error)
+
+
+def kda_layer_step_noalloc(x, conv_weight, conv_bias, conv_state, f_a, f_b, raw_beta, A_log,
+                           dt_bias, state_pool, state_slots, record_rows, pending, corr,
+                           key_gate, gate, norm_weight, out, *, Q, lower_bound, q_scale, eps,
+                           rq=None, null_slot=0, status=None, stream=None,
+                           raise_on_error=True):
+    """kda_layer_step without a workspace, for callers that cannot allocate
+    device memory on the decode path: the step's operands go to the
+    library's own fixed array (KDA_LAYER_STEP_NOALLOC_MAX_BYTES per GPU), so
+    nothing is allocated.  Calls larger than that raise KDA_ERR_SCRATCH;
+    calls that overlap on the GPU share the array and must be ordered."""
+    import torch
+    for name, t in (("x", x), ("conv_weight", conv_weight), ("conv_bias", conv_bias),
+                    ("conv_state", conv_state), ("f_a", f_a), ("f_b", f_b),
+                    ("raw_beta", raw_beta), ("key_gate", key_gate), ("gate", gate),
+                    ("out", out)):
+        _expect(t, torch.bfloat16, name)
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias), ("state_pool", state_pool),
+                    ("corr", corr), ("norm_weight", norm_weight)):
+        _expect(t, torch.float32, name)
+    for name, t in (("state_slots", state_slots), ("record_rows", record_rows),
+                    ("pending", pending)):
+        _expect(t, torch.int32, name)
+    rq = corr.shape[2] if rq is None else rq
+    B = state_slots.shape[0]
+    H = A_log.shape[0]
+    rc = load().kda_layer_step_noalloc(
+        _ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state), conv_state.stride(0),
+        _ptr(f_a), _ptr(f_b), _ptr(raw_beta), _ptr(A_log), _ptr(dt_bias), lower_bound, q_scale,
+        _ptr(state_pool), state_pool.stride(0), state_pool.shape[0], _ptr(state_slots),
+        _ptr(record_rows), _ptr(pending), _ptr(corr), _ptr(key_gate), corr.stride(0),
+        key_gate.stride(0), corr.shape[0], rq, _ptr(gate), _ptr(norm_weight), eps, _ptr(out),
+        B, H, Q, null_slot, _ptr(status), _stream(stream))
+    return _check("kda_layer_step_noalloc", rc, raise_on_error)

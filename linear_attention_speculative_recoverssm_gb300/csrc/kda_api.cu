@@ -208,6 +208,7 @@ const char *kda_error_string(int status) {
     case KDA_ERR_UNSUPPORTED: return "unsupported configuration";
     case KDA_ERR_CUDA: return "CUDA launch failed";
     case KDA_ERR_TIMEOUT: return "device wait timed out";
+    case KDA_ERR_SCRATCH: return "call larger than the library's fixed scratch memory";
     default: return "unknown status";
   }
 }
