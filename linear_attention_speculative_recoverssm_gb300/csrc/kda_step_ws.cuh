@@ -879,7 +879,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           op.x[t][c] = gam[t] * kk[t];
           op.x[Q + t][c] = gam[t] * qq[t];
           sm.ex[t][c] = kk[t] * inv[t];
-          op.vv[t][c] = in.tok[3][t][c];
+        }
+        // v rows copied 16 bytes at a time (thread u: 8 values of row u / 16)
+        if (c < 16 * Q) {
+          const int t = c >> 4, q16 = c & 15;
+          *reinterpret_cast<uint4 *>(&op.vv[t][8 * q16]) =
+              *reinterpret_cast<const uint4 *>(&in.tok[3][t][8 * q16]);
         }
         if (c < Q) op.beta[c] = sigmoidf_fast(bf16_bits_to_f32(braw_bits));
         if (REPLAY && it.n > 0) {
@@ -974,13 +979,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             kg = reinterpret_cast<uint16_t *>(lay.kg[it.l]);
             kgs = lay.kg_stride[it.l];
           }
-          const long long kbase = (long long)it.rec * kgs + (long long)it.h * p.rq * (2 * kDim) + c;
+          // 16 bytes per store: unit u of the 32 Q (part, token, 8-channel
+          // chunk) units, part 0 the key row, 1 the raw-gate row
+          const long long kbase = (long long)it.rec * kgs + (long long)it.h * p.rq * (2 * kDim);
 #pragma unroll
-          for (int t = 0; t < Q; ++t) {
-            if (!VARLEN || t < it.qb) {
-              kg[kbase + t * 2 * kDim] = in.tok[1][t][c];
-              kg[kbase + t * 2 * kDim + kDim] = in.tok[2][t][c];
-            }
+          for (int u = c; u < 32 * Q; u += 128) {
+            const int part = u / (16 * Q), t = (u >> 4) % Q, q16 = u & 15;
+            if (!VARLEN || t < it.qb)
+              *reinterpret_cast<uint4 *>(kg + kbase + t * 2 * kDim + part * kDim + 8 * q16) =
+                  *reinterpret_cast<const uint4 *>(&in.tok[1 + part][t][8 * q16]);
           }
         }
       }
