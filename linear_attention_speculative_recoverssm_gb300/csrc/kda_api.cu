@@ -191,6 +191,7 @@ kda::StepParams make_params(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16
   p.gate = nullptr;
   p.norm_w = nullptr;
   p.norm_eps = 0.f;
+  kda::set_head_divisor(p);
   return p;
 }
 

@@ -41,7 +41,31 @@ struct StepParams {
   const uint16_t *gate;  // [n_tokens, H*128] BF16 bits
   const float *norm_w;   // [128]
   float norm_eps;
+  // n / H by a multiply and shifts (set_head_divisor)
+  uint32_t h_mul;
+  int h_sh1, h_sh2;
 };
+
+// Division of an item index by the head count H, an invariant of the call,
+// by a multiply and two shifts (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, the unsigned
+// round-up method): with l = ceil(log2 H) and m = floor(2^32 (2^l - H) / H)
+// + 1, n / H = (t + ((n - t) >> 1)) >> (l - 1) where t = mulhi(m, n), for
+// every 32-bit n (H = 1: m = 1 and both shifts 0).
+inline void set_head_divisor(StepParams &p) {
+  const uint32_t H = (uint32_t)p.H;
+  int l = 0;
+  while ((1ull << l) < H) ++l;
+  p.h_mul = (uint32_t)((((1ull << 32) * ((1ull << l) - H)) / H) + 1);
+  p.h_sh1 = l > 0 ? 1 : 0;
+  p.h_sh2 = l > 0 ? l - 1 : 0;
+}
+
+__device__ __forceinline__ int div_heads(const StepParams &p, int n) {
+  const uint32_t u = (uint32_t)n;
+  const uint32_t t = __umulhi(p.h_mul, u);
+  return (int)((t + ((u - t) >> p.h_sh1)) >> p.h_sh2);
+}
 
 // The multi-layer step: one launch over L layers whose items are
 // (layer, request, head), layer-major.  Every layer has its own state pool,

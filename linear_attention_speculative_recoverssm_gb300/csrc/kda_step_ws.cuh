@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (REPLAY && r.rec >= 0 && r.rec < p.n_rows && r.slot > p.null_slot && r.slot < p.n_slots)
         r.pend = p.pending[r.rec];
       if constexpr (VARLEN) {
-        const int b = (first + i * stride) / p.H;
+        const int b = div_heads(p, first + i * stride);
         r.q0 = p.qsl[b];
         r.q1 = p.qsl[b + 1];
       }
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         it.h = (first + i * stride) % p.H;
         it.l = layer_of(first + i * stride);
       } else {
-        it.b = (first + i * stride) / p.H;
+        it.b = div_heads(p, first + i * stride);
         it.h = (first + i * stride) - it.b * p.H;
         it.l = 0;
       }
@@ -735,7 +735,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (c < Q) beta_n = p.beta[l * lay.beta_stride + ((long long)b * Q + c) * p.H + h];
         return;
       }
-      const int b = (first + i * stride) / p.H;
+      const int b = div_heads(p, first + i * stride);
       const int h = (first + i * stride) - b * p.H;
       dt_n = p.dt_bias[h * kDim + c];
       alog_n = p.A_log[h];

@@ -203,3 +203,23 @@ def test_product_path_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not pattern.search(text), os.path.join(dirpath, f)
+
+
+def test_head_divisor_method():
+    """The step kernels divide item indices by the head count with a multiply
+    and two shifts (Granlund and Montgomery's round-up method for an
+    invariant divisor): m = floor(2^32 (2^l - H) / H) + 1 with l =
+    ceil(log2 H), n / H = (t + ((n - t) >> 1)) >> (l - 1), t = mulhi(m, n)
+    (H = 1: m = 1, both shifts 0).  The method, checked here against exact
+    division for every head count up to 1024 and the 32-bit edge cases."""
+    import random
+    rng = random.Random(3)
+    for H in list(range(1, 1025)) + [4095, 4096, 65535]:
+        l = (H - 1).bit_length()
+        m = ((1 << 32) * ((1 << l) - H)) // H + 1
+        assert 0 < m < (1 << 32)
+        sh1, sh2 = (1, l - 1) if l > 0 else (0, 0)
+        for n in [0, 1, H - 1, H, H + 1, 2 ** 31 - 1, 2 ** 32 - 1] + \
+                [rng.randrange(2 ** 32) for _ in range(40)]:
+            t = (m * n) >> 32
+            assert (t + ((n - t) >> sh1)) >> sh2 == n // H, (H, n)
