@@ -47,13 +47,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // `a` is exp(A_log) of the head, computed once per item.
 // ---------------------------------------------------------------------------
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the hardware's approximate base-2 exponential (ex2.approx.ftz.f32).
+__device__ __forceinline__ float exp2f_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float sigmoidf_fast(float z) {
   return __fdividef(1.0f, 1.0f + __expf(-z));
 }
 
+// Computed as 2^(lb log2(e) / (1 + 2^(-a log2(e) (raw_g + dt)))): two base-2
+// exponentials and one reciprocal, with the products that do not depend on
+// raw_g folded (hoisted out of a caller's loop over tokens).
 __device__ __forceinline__ float gate_decay(float a, float raw_g, float dt,
                                             float lower_bound) {
-  return __expf(lower_bound * sigmoidf_fast(a * (raw_g + dt)));
+  const float al = a * kLog2e;
+  const float e = exp2f_fast(fmaf(-al, raw_g, -al * dt));
+  return exp2f_fast((lower_bound * kLog2e) * __fdividef(1.f, 1.f + e));
 }
 
 // ---------------------------------------------------------------------------

@@ -809,15 +809,26 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       // (inputs are re-read from the stage where needed: fewer live registers)
       float kk[Q], qq[Q], gam[Q], inv[Q];
       float kr[kMaxQ], dr[kMaxQ];
-      const float a = __expf(a_log_h);
+      // the decay d = exp(lb sigmoid(a (g + dt))) as 2^(lb log2(e) / (1 +
+      // 2^(-a log2(e) (g + dt)))), with this channel's constants folded once
+      const float al = __expf(a_log_h) * kLog2e;
+      const float e1 = -al, e0 = -al * dt, lbl = p.lower_bound * kLog2e;
+      auto decay_of = [&](float graw) {
+        const float e = exp2f_fast(fmaf(e1, graw, e0));
+        return exp2f_fast(lbl * __fdividef(1.f, 1.f + e));
+      };
       if (live) {
 #pragma unroll
         for (int t = 0; t < kMaxQ; ++t) {
           kr[t] = 0.f;
           dr[t] = 1.f;
-          if (REPLAY && t < it.n) {
+        }
+        if (REPLAY) {
+#pragma unroll
+          for (int t = 0; t < kMaxQ; ++t) {
+            if (t >= it.n) break;
             kr[t] = bf16_bits_to_f32(in.kg[t][c]);
-            dr[t] = gate_decay(a, bf16_bits_to_f32(in.kg[t][kDim + c]), dt, p.lower_bound);
+            dr[t] = decay_of(bf16_bits_to_f32(in.kg[t][kDim + c]));
           }
         }
         float g = 1.f;
@@ -825,7 +836,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         for (int t = 0; t < Q; ++t) {
           qq[t] = bf16_bits_to_f32(in.tok[0][t][c]);
           kk[t] = bf16_bits_to_f32(in.tok[1][t][c]);
-          g *= gate_decay(a, bf16_bits_to_f32(in.tok[2][t][c]), dt, p.lower_bound);
+          g *= decay_of(bf16_bits_to_f32(in.tok[2][t][c]));
           gam[t] = g;
           inv[t] = __fdividef(1.f, g);
         }
