@@ -76,6 +76,10 @@ constexpr int kBarPro = 1;   // named barrier of the prologue warpgroup
 // may run up to this many items ahead, which absorbs the per-item jitter of
 // either side.
 constexpr int kWsOpsBufs = 3;
+// The index chain runs in lanes 0 .. kWsChain - 1 of the prologue's warp 0,
+// kWsChain items at a time (one per lane), every kWsChain items, into a ring
+// of 2 kWsChain slots of meta words.
+constexpr int kWsChain = 16;
 
 // Reduced over channels by the prologue per item: sum q_t^2 (Q values),
 // then the recorded keys' sums of squares (8 values).
@@ -154,7 +158,8 @@ struct WsSmemBase {
   uint64_t opfull[kWsOpsBufs];
   uint64_t opempty[kWsOpsBufs];
   uint64_t infull[2];
-  int next_meta[8];  // resolved index chain of the next item to request
+  // the resolved index chain of item i in slot i % (2 kWsChain)
+  int meta_ring[2 * kWsChain][8];
 };
 
 // The NORM instances add the folded gated RMSNorm's exchange: each main
@@ -574,17 +579,20 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     struct Raw {
       int slot = -1, rec = -1, bslot = -1, blen = 0, pend = 0, q0 = 0, q1 = 0;
     };
-    Raw r2, r3;  // items j + 2 (row and pending loaded) and j + 3 (row loaded)
-    auto publish_next = [&](const ItemMeta &m) {  // item j + 1, read by thread 0
-      sm.next_meta[0] = VARLEN ? m.tok0 : m.b;
-      sm.next_meta[1] = m.h;
-      sm.next_meta[2] = m.slot;
-      sm.next_meta[3] = m.rec;
-      sm.next_meta[4] = m.n;
-      sm.next_meta[5] = m.bslot;
-      sm.next_meta[6] = m.m;
-      if constexpr (VARLEN) sm.next_meta[7] = m.qb;
-      if constexpr (LAYERS) sm.next_meta[7] = m.l;
+    // Lane l < kWsChain of warp 0 resolves item g kWsChain + l of every
+    // group g: ra holds the row and pending count of its item in the next
+    // group to resolve, rb the row of its item in the group after.
+    Raw ra, rb;
+    auto publish = [&](int i, const ItemMeta &m) {
+      int *w = sm.meta_ring[i % (2 * kWsChain)];
+      w[0] = VARLEN ? m.tok0 : m.b;
+      w[1] = m.h;
+      w[2] = m.slot;
+      w[3] = m.rec;
+      w[4] = m.n;
+      w[5] = m.bslot;
+      w[6] = m.m;
+      w[7] = VARLEN ? m.qb : (LAYERS ? m.l : 0);
     };
     auto load_raw = [&](int i, Raw &r) {
       const int b = req_of(first + i * stride);
@@ -665,16 +673,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // corrections by one bulk copy each, all completing on infull[i & 1].
     auto request_inputs = [&](int i) {
       if (c != 0) return;
+      const int *w = sm.meta_ring[i % (2 * kWsChain)];
       ItemMeta m;
-      m.b = m.tok0 = sm.next_meta[0];
-      m.h = sm.next_meta[1];
-      m.slot = sm.next_meta[2];
-      m.rec = sm.next_meta[3];
-      m.n = sm.next_meta[4];
-      m.bslot = sm.next_meta[5];
-      m.m = sm.next_meta[6];
-      m.qb = VARLEN ? sm.next_meta[7] : Q;
-      m.l = LAYERS ? sm.next_meta[7] : 0;
+      m.b = m.tok0 = w[0];
+      m.h = w[1];
+      m.slot = w[2];
+      m.rec = w[3];
+      m.n = w[4];
+      m.bslot = w[5];
+      m.m = w[6];
+      m.qb = VARLEN ? w[7] : Q;
+      m.l = LAYERS ? w[7] : 0;
       WsIn<Q> &in = sm.in[i & 1];
       in.meta[0] = m.b;
       in.meta[1] = m.h;
@@ -723,8 +732,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // (kept raw: converting here would wait for the loads at once)
     float dt_n = 0.f, alog_n = 0.f;
     uint32_t beta_n = 0;
-    // The window of item i is read from next_meta, which holds item i's
-    // resolved chain whenever this runs.
+    // (with VARLEN item i's window is read from its meta words)
     auto load_small = [&](int i) {
       if constexpr (LAYERS) {
         const int idx = first + i * stride;
@@ -740,9 +748,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       dt_n = p.dt_bias[h * kDim + c];
       alog_n = p.A_log[h];
       if constexpr (VARLEN) {
-        const long long tok = sm.next_meta[0];
+        const int *w = sm.meta_ring[i % (2 * kWsChain)];
+        const long long tok = w[0];
         beta_n = 0;
-        if (c < sm.next_meta[7]) beta_n = p.beta[(tok + c) * p.H + h];
+        if (c < w[7]) beta_n = p.beta[(tok + c) * p.H + h];
       } else {
         if (c < Q) beta_n = p.beta[((long long)b * Q + c) * p.H + h];
       }
@@ -752,29 +761,27 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     int taken = 0;      // items whose inputs were waited for
     if (count > 0) {
       requested = 1;
-      if (c == 0) {
-        Raw r0;
-        load_raw(0, r0);
-        load_pending(0, r0);
-        publish_next(resolve(0, r0));
-      }
-      named_bar(kBarPro, 128);  // next_meta published
-      request_inputs(0);
-      if constexpr (VARLEN) load_small(0);  // item 0's window is in next_meta
-      named_bar(kBarPro, 128);  // next_meta read by every thread
-      if (c == 0 && count > 1) {
-        Raw r1;
-        load_raw(1, r1);
-        load_pending(1, r1);
-        publish_next(resolve(1, r1));
-        if (count > 2) {
-          load_raw(2, r2);
-          load_pending(2, r2);
+      // groups 0 and 1 resolved now; group 2's rows and pending counts and
+      // group 3's rows loaded for the first turns below
+      if (c < kWsChain) {
+        for (int g = 0; g < 2; ++g) {
+          const int i = g * kWsChain + c;
+          if (i < count) {
+            Raw r0;
+            load_raw(i, r0);
+            load_pending(i, r0);
+            publish(i, resolve(i, r0));
+          }
         }
-        if (count > 3) load_raw(3, r3);
+        if (2 * kWsChain + c < count) {
+          load_raw(2 * kWsChain + c, ra);
+          load_pending(2 * kWsChain + c, ra);
+        }
+        if (3 * kWsChain + c < count) load_raw(3 * kWsChain + c, rb);
       }
-      named_bar(kBarPro, 128);  // next_meta published
-      if constexpr (!VARLEN) load_small(0);
+      named_bar(kBarPro, 128);  // groups 0 and 1 published
+      request_inputs(0);
+      load_small(0);
     }
 
     for (int j = 0; j < count; ++j) {
@@ -855,13 +862,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           if (lane < kWsRed) sm.red[warp][lane] = v[0];
         }
       }
-      // thread 0: the index chain of item j + 2, then the row of item j + 3
-      // (each value was loaded at least one item earlier)
-      if (c == 0 && j + 2 < count) {
-        publish_next(resolve(j + 2, r2));
-        r2 = r3;
-        if (j + 3 < count) load_pending(j + 3, r2);
-        if (j + 4 < count) load_raw(j + 4, r3);
+      // lanes 0 .. kWsChain - 1: every kWsChain items, group g = j /
+      // kWsChain + 1 resolved (it is first requested an item before its
+      // first item); then the pending counts of group g + 1 and the rows of
+      // group g + 2 are loaded, each used a whole group later
+      if (c < kWsChain && j >= kWsChain && j % kWsChain == 0) {
+        const int g = j / kWsChain + 1;
+        const int i = g * kWsChain + c;
+        if (i < count) publish(i, resolve(i, ra));
+        ra = rb;
+        if (i + kWsChain < count) load_pending(i + kWsChain, ra);
+        if (i + 2 * kWsChain < count) load_raw(i + 2 * kWsChain, rb);
       }
 
       // ---- the ops buffer of item j - kWsOpsBufs must have been consumed ----
