@@ -438,7 +438,7 @@ ROW_GROUPS = ("commit", "mid_batch", "layers", "varlen", "latency", "bookkeeping
               "layer")
 
 
-def measure_rows(dev, stream, peak, cpu_seconds, only=None):
+def measure_rows(dev, stream, peak, cpu_seconds, only=None, layer_workload=None):
     """Timings of the step's other rows (CUDA events on the launching stream;
     every pool below is larger than L2 except the latency sweep's, which is a
     latency measurement by design).  ``only``: the row groups to run (all
@@ -630,7 +630,9 @@ def measure_rows(dev, stream, peak, cpu_seconds, only=None):
     if want("decode_loop"):
         rows["decode_loop"] = measure_decode_loop(dev, dt, peak)
     if want("layer"):
-        rows["layer"] = measure_layer(dev, stream, dt, peak)
+        rows["layer"] = measure_layer(dev, stream, dt, peak,
+                                      **({} if layer_workload is None else
+                                         dict(name=layer_workload)))
     return rows
 
 
@@ -702,7 +704,7 @@ def layer_algorithmic_bytes(c):
     return prologue, epilogue
 
 
-def measure_layer(dev, stream, dt, peak):
+def measure_layer(dev, stream, dt, peak, name="layer-f32-h64-b512-q8"):
     """The model layer around the large-batch step: the prologue
     (convolution + SiLU, gate projection, window rewrite), the fused
     replay + verify on its outputs, and the gated-norm epilogue."""
@@ -710,7 +712,6 @@ def measure_layer(dev, stream, dt, peak):
     from linear_attention_speculative_recoverssm_gb300 import (kda_layer_epilogue,
                                                                kda_layer_prologue,
                                                                kda_replay_verify, synth)
-    name = "layer-f32-h64-b512-q8"
     c = synth.make(name)
     keys = ("x", "conv_weight", "conv_bias", "conv_state", "f_a", "f_b", "gate", "norm_weight",
             "raw_beta", "A_log", "dt_bias", "state", "state_slots", "record_rows", "pending",
@@ -1038,7 +1039,8 @@ def run_ours(args):
     rows = None
     if rank == 0 and not args.no_rows:
         rows = measure_rows(dev, stream, peak, 0.0 if args.no_cpu_baseline else 3.0,
-                            only=None if args.rows is None else set(args.rows.split(",")))
+                            only=None if args.rows is None else set(args.rows.split(",")),
+                            layer_workload=args.layer_workload)
 
     cpu = None
     if pool is not None:
@@ -1089,6 +1091,8 @@ def main():
     ap.add_argument("--rows", default=None,
                     help="comma-separated row groups to run (default all): "
                          + ", ".join(ROW_GROUPS))
+    ap.add_argument("--layer-workload", default=None,
+                    help="the model-layer row's workload (default layer-f32-h64-b512-q8)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--traffic", type=float, default=None,

@@ -412,6 +412,9 @@ WORKLOADS = {
     "decode-loop-f32-h64-b512-q8": dict(kind="decode_loop", B=512, H=64, Q=8,
                                         slots=1024, steps=8, seed=6, windows=2,
                                         padding_frac=0.05, accept_min=1),
+    # the model layer at a quarter of the requests (profiler captures)
+    "layer-f32-h64-b128-q8": dict(kind="layer", B=128, H=64, Q=8, slots=160,
+                                  seed=10, padding_frac=0.05),
     # the large-batch shape at a quarter of the requests (the same kernel
     # instance, ~0.6 GB of state): small enough for a full profiler capture
     "replay-verify-f32-h64-b128-q8": dict(kind="replay_verify", B=128, H=64,
