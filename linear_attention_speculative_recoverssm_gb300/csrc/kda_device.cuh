@@ -56,6 +56,14 @@ __device__ __forceinline__ float exp2f_fast(float x) {
   return y;
 }
 
+// tanh(x) by the hardware's approximation (tanh.approx.f32, relative error
+// about 2^-11: for values that round to BF16 afterwards).
+__device__ __forceinline__ float tanhf_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float sigmoidf_fast(float z) {
   return __fdividef(1.0f, 1.0f + __expf(-z));
 }

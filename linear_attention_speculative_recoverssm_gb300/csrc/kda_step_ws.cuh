@@ -169,7 +169,7 @@ struct WsSmemBase {
 template <int Q, typename ST, bool BOUNDARY>
 struct WsSmemNorm : WsSmemBase<Q, ST, BOUNDARY> {
   uint64_t nred[kWsOpsBufs];
-  float nsq[kWsOpsBufs][8][kMaxQ];
+  alignas(16) float nsq[kWsOpsBufs][kMaxQ][8];  // [buf][token][main warp]
   alignas(16) float norm_w[kDim];  // read as float4
 };
 
@@ -197,6 +197,7 @@ struct WsLayoutCheck {
   static_assert(offsetof(S, full) % 8 == 0 && offsetof(S, opfull) % 8 == 0 &&
                 offsetof(S, opempty) % 8 == 0 && offsetof(S, infull) % 8 == 0, "mbarriers");
   static_assert(offsetof(SN, nred) % 8 == 0 && offsetof(SN, norm_w) % 16 == 0 &&
+                offsetof(SN, nsq) % 16 == 0 &&
                 sizeof(SN) <= 232448, "the norm's barriers and float4-read weights");
   static_assert(sizeof(S) <= 232448, "shared memory per CTA");
   static constexpr bool ok = true;
@@ -1078,20 +1079,22 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const bool done = mbar_wait_bounded(&sm.nred[pn_buf], pn_par);
     if (__any_sync(0xffffffffu, !done)) return false;
     if (pn_tok >= 0) {
-      float tot = 0.f;
-#pragma unroll
-      for (int w2 = 0; w2 < 8; ++w2) tot += sm.nsq[pn_buf][w2][pn_tok];
-      const float rstd = rsqrtf(tot * (1.0f / kDim) + p.norm_eps);
+      // the eight warps' sums in warp order
+      const float4 s0 = lds4(&sm.nsq[pn_buf][pn_tok][0]);
+      const float4 s1 = lds4(&sm.nsq[pn_buf][pn_tok][4]);
+      const float tot = ((((((s0.x + s0.y) + s0.z) + s0.w) + s1.x) + s1.y) + s1.z) + s1.w;
+      // sigmoid(g) = (1 + tanh(g / 2)) / 2: half of rstd folded into the weight
+      const float hr = 0.5f * rsqrtf(tot * (1.0f / kDim) + p.norm_eps);
       const float4 w4 = lds4(&sm.norm_w[R0]);
       const float g0 = bf16_bits_to_f32(pn_gate.x & 0xffffu);
       const float g1 = bf16_bits_to_f32(pn_gate.x >> 16);
       const float g2 = bf16_bits_to_f32(pn_gate.y & 0xffffu);
       const float g3 = bf16_bits_to_f32(pn_gate.y >> 16);
       *reinterpret_cast<uint2 *>(pn_dst) =
-          make_uint2(pack_bf16x2(pn_o[0] * rstd * w4.x * sigmoidf_fast(g0),
-                                 pn_o[1] * rstd * w4.y * sigmoidf_fast(g1)),
-                     pack_bf16x2(pn_o[2] * rstd * w4.z * sigmoidf_fast(g2),
-                                 pn_o[3] * rstd * w4.w * sigmoidf_fast(g3)));
+          make_uint2(pack_bf16x2(pn_o[0] * (hr * w4.x) * (1.f + tanhf_fast(0.5f * g0)),
+                                 pn_o[1] * (hr * w4.y) * (1.f + tanhf_fast(0.5f * g1))),
+                     pack_bf16x2(pn_o[2] * (hr * w4.z) * (1.f + tanhf_fast(0.5f * g2)),
+                                 pn_o[3] * (hr * w4.w) * (1.f + tanhf_fast(0.5f * g3))));
     }
     return true;
     }
@@ -1105,6 +1108,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     bool ok = mbar_wait_bounded(&sm.opfull[j % kWsOpsBufs], (uint32_t)((j / kWsOpsBufs) & 1));
     if (__any_sync(0xffffffffu, !ok)) {
+      failed = true;
+      break;
+    }
+    // the previous item's norm (its sums of squares are in by now)
+    if (!norm_finish()) {
       failed = true;
       break;
     }
@@ -1218,12 +1226,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
     }
 
-    // the previous item's norm (its sums of squares are in by now)
-    if (!norm_finish()) {
-      failed = true;
-      break;
-    }
-
     // ---------------- pass B: 2Q dots per row ----------------------------
     float d[NG][4];
     ws_dots<NG>(st, &op.x[0][0], c, d);
@@ -1248,7 +1250,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       sq += __shfl_xor_sync(0xffffffffu, sq, 8);
       sq += __shfl_xor_sync(0xffffffffu, sq, 16);
       const int mw = mt >> 5;
-      if (lane < 8 && tout >= 0) sm.nsq[j % kWsOpsBufs][mw][tout] = sq;
+      if (lane < 8 && tout >= 0) sm.nsq[j % kWsOpsBufs][tout][mw] = sq;
       warp_arrive(&sm.nred[j % kWsOpsBufs]);
       norm_pending = true;
 #pragma unroll
