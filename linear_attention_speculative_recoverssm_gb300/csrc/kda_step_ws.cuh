@@ -110,7 +110,7 @@ struct alignas(16) WsOps {
   float rsk[Q];          // rsqrt(|k_t|^2 + eps)
   float fin_a[Q][Q];     // normalised A_ts (s < t), 0 for s >= t
   float fin_b[Q][Q];     // normalised B_ts (s <= t), 0 for s > t
-  int meta[8];  // b (tok0 with VARLEN), h, slot, rec, n, bslot, m, qb (VARLEN)
+  alignas(16) int meta[8];  // b (tok0 with VARLEN), h, slot, rec, n, bslot, m, qb (VARLEN)
 };
 
 // Tensor maps of the four token-major BF16 inputs [B*Q, H, 128], in the
@@ -136,7 +136,7 @@ struct alignas(128) WsIn {
   uint16_t tok[4][Q][kDim];      // q, k, raw_g, v rows of this window (BF16)
   uint16_t kg[kMaxQ][2 * kDim];  // recorded key / raw gate rows (first n)
   float corr[kMaxQ][kDim];       // recorded corrections (first n)
-  int meta[8];                   // as in WsOps
+  alignas(16) int meta[8];       // as in WsOps
 };
 
 template <typename ST>
@@ -159,7 +159,7 @@ struct WsSmemBase {
   uint64_t opempty[kWsOpsBufs];
   uint64_t infull[2];
   // the resolved index chain of item i in slot i % (2 kWsChain)
-  int meta_ring[2 * kWsChain][8];
+  alignas(16) int meta_ring[2 * kWsChain][8];
 };
 
 // The NORM instances add the folded gated RMSNorm's exchange: each main
@@ -674,27 +674,23 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // corrections by one bulk copy each, all completing on infull[i & 1].
     auto request_inputs = [&](int i) {
       if (c != 0) return;
-      const int *w = sm.meta_ring[i % (2 * kWsChain)];
+      // the meta words move 16 bytes at a time: the ring slot and in.meta
+      // have the same layout
+      const int4 *w4 = reinterpret_cast<const int4 *>(sm.meta_ring[i % (2 * kWsChain)]);
+      const int4 w0 = w4[0], w1 = w4[1];
       ItemMeta m;
-      m.b = m.tok0 = w[0];
-      m.h = w[1];
-      m.slot = w[2];
-      m.rec = w[3];
-      m.n = w[4];
-      m.bslot = w[5];
-      m.m = w[6];
-      m.qb = VARLEN ? w[7] : Q;
-      m.l = LAYERS ? w[7] : 0;
+      m.b = m.tok0 = w0.x;
+      m.h = w0.y;
+      m.slot = w0.z;
+      m.rec = w0.w;
+      m.n = w1.x;
+      m.bslot = w1.y;
+      m.m = w1.z;
+      m.qb = VARLEN ? w1.w : Q;
+      m.l = LAYERS ? w1.w : 0;
       WsIn<Q> &in = sm.in[i & 1];
-      in.meta[0] = m.b;
-      in.meta[1] = m.h;
-      in.meta[2] = m.slot;
-      in.meta[3] = m.rec;
-      in.meta[4] = m.n;
-      in.meta[5] = m.bslot;
-      in.meta[6] = m.m;
-      if constexpr (VARLEN) in.meta[7] = m.qb;
-      if constexpr (LAYERS) in.meta[7] = m.l;
+      reinterpret_cast<int4 *>(in.meta)[0] = w0;
+      reinterpret_cast<int4 *>(in.meta)[1] = w1;
       uint64_t *bar = &sm.infull[i & 1];
       if (m.slot < 0) {
         mbar_arrive(bar);
@@ -803,15 +799,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       taken = j + 1;
       ItemMeta it;
-      it.b = in.meta[0];
-      it.h = in.meta[1];
-      it.slot = in.meta[2];
-      it.rec = in.meta[3];
-      it.n = in.meta[4];
-      it.bslot = in.meta[5];
-      it.m = in.meta[6];
-      it.qb = VARLEN ? in.meta[7] : Q;
-      it.l = LAYERS ? in.meta[7] : 0;
+      const int4 im0 = reinterpret_cast<const int4 *>(in.meta)[0];
+      const int4 im1 = reinterpret_cast<const int4 *>(in.meta)[1];
+      it.b = im0.x;
+      it.h = im0.y;
+      it.slot = im0.z;
+      it.rec = im0.w;
+      it.n = im1.x;
+      it.bslot = im1.y;
+      it.m = im1.z;
+      it.qb = VARLEN ? im1.w : Q;
+      it.l = LAYERS ? im1.w : 0;
       const bool live = it.slot >= 0;
 
       // (inputs are re-read from the stage where needed: fewer live registers)
@@ -886,15 +884,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
       }
       if (c == 0) {
-        op.meta[0] = it.b;
-        op.meta[1] = it.h;
-        op.meta[2] = it.slot;
-        op.meta[3] = it.rec;
-        op.meta[4] = it.n;
-        op.meta[5] = it.bslot;
-        op.meta[6] = it.m;
-        if constexpr (VARLEN) op.meta[7] = it.qb;
-        if constexpr (LAYERS) op.meta[7] = it.l;
+        // (the operand buffer's meta words are the input buffer's)
+        reinterpret_cast<int4 *>(op.meta)[0] = im0;
+        reinterpret_cast<int4 *>(op.meta)[1] = im1;
       }
       if (live) {
 #pragma unroll
