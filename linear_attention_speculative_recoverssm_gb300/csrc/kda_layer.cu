@@ -46,8 +46,15 @@ struct LayerParams {
 // windows pass through a thread-private shared-memory block.
 constexpr int kConvCtas = 8;  // CTAs per request
 
-template <int Q>
+// WHOLE (record capacity rq = Q, Q even): the new window is the whole
+// window, so each lane builds a channel pair's new windows (2 (Q + 2) BF16,
+// 8-byte aligned) in registers and stores them 8 bytes at a time, and reads
+// each channel's three taps as two 32-bit words (a lane's block is 8 (Q + 2)
+// BF16 from its neighbour's, so a warp's 2-byte accesses hit each bank up to
+// 8 times).
+template <int Q, bool WHOLE>
 __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams p) {
+  static_assert(!WHOLE || Q % 2 == 0, "whole-window rewrite: an even window");
   __shared__ __align__(16) uint16_t wins[kConvThreads * 8 * (kMaxQ + 2)];
   const int b = blockIdx.x;
   const int slot = p.state_slots[b];
@@ -105,10 +112,30 @@ __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams
       for (int i = 0; i < 4; ++i) wh[i] = reinterpret_cast<const uint16_t *>(&wv[i]);
       const uint16_t *bh = reinterpret_cast<const uint16_t *>(&bv);
       uint32_t res[Q][4];
+      constexpr int kWords = (Q + 2) / 2;  // a channel's window, in 32-bit words (WHOLE)
+      uint32_t nwin[WHOLE ? 2 * kWords : 1];  // the current channel pair's new windows
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         uint16_t *win = mine + j * W;
-        const uint16_t t0 = win[off], t1 = win[off + 1], t2 = win[off + 2];
+        uint16_t t0, t1, t2;
+        if constexpr (WHOLE) {
+          // the taps off .. off + 2 lie in words off / 2 and off / 2 + 1
+          const uint32_t *ww = reinterpret_cast<const uint32_t *>(win);
+          const uint32_t wa = ww[off >> 1], wb = ww[(off >> 1) + 1];
+          if ((off & 1) == 0) {
+            t0 = (uint16_t)(wa & 0xffffu);
+            t1 = (uint16_t)(wa >> 16);
+            t2 = (uint16_t)(wb & 0xffffu);
+          } else {
+            t0 = (uint16_t)(wa >> 16);
+            t1 = (uint16_t)(wb & 0xffffu);
+            t2 = (uint16_t)(wb >> 16);
+          }
+        } else {
+          t0 = win[off];
+          t1 = win[off + 1];
+          t2 = win[off + 2];
+        }
         float seq[Q + 3];
         seq[0] = bf16_bits_to_f32(t0);
         seq[1] = bf16_bits_to_f32(t1);
@@ -127,11 +154,25 @@ __global__ void __launch_bounds__(kConvThreads) kda_layer_conv(const LayerParams
           if (j & 1) res[t][j >> 1] |= bits << 16;
           else res[t][j >> 1] = bits;
         }
-        win[0] = t1;  // entries from 2 + Q on (rq > Q) are kept
-        win[1] = t2;
+        if constexpr (WHOLE) {
+          const int jj = (j & 1) * kWords;
+          nwin[jj] = (uint32_t)t1 | ((uint32_t)t2 << 16);
 #pragma unroll
-        for (int t = 0; t < Q; ++t) win[2 + t] = xh[t][j];
+          for (int w = 1; w < kWords; ++w)
+            nwin[jj + w] = (uint32_t)xh[2 * w - 2][j] | ((uint32_t)xh[2 * w - 1][j] << 16);
+          if (j & 1) {  // channels j - 1 and j: 2 (Q + 2) BF16 from element (j - 1) W
+            uint2 *pair = reinterpret_cast<uint2 *>(mine + (j - 1) * W);
+#pragma unroll
+            for (int w = 0; w < kWords; ++w) pair[w] = make_uint2(nwin[2 * w], nwin[2 * w + 1]);
+          }
+        } else {
+          win[0] = t1;  // entries from 2 + Q on (rq > Q) are kept
+          win[1] = t2;
+#pragma unroll
+          for (int t = 0; t < Q; ++t) win[2 + t] = xh[t][j];
+        }
       }
+
       uint16_t *out = part == 0 ? p.q : (part == 1 ? p.k : p.v);
       const int h = hc / kDim, c0 = hc - h * kDim;
 #pragma unroll
@@ -481,7 +522,14 @@ int launch_prologue_q(const LayerParams &p, int items, cudaStream_t stream) {
   GateMaps maps;
   const int st = encode_gate_maps(p, n_tokens, maps);
   if (st != KDA_OK) return st;
-  kda_layer_conv<Q><<<dim3(p.B, kConvCtas), kConvThreads, 0, stream>>>(p);
+  if constexpr (Q % 2 == 0) {
+    if (p.rq == Q)
+      kda_layer_conv<Q, true><<<dim3(p.B, kConvCtas), kConvThreads, 0, stream>>>(p);
+    else
+      kda_layer_conv<Q, false><<<dim3(p.B, kConvCtas), kConvThreads, 0, stream>>>(p);
+  } else {
+    kda_layer_conv<Q, false><<<dim3(p.B, kConvCtas), kConvThreads, 0, stream>>>(p);
+  }
   const long long units = (long long)((n_tokens + kGateTile - 1) / kGateTile) * p.H;
   if (units > 0x7fffffffLL) return KDA_ERR_ARG;
   const int sms = device_sm_count(dev);
