@@ -302,6 +302,18 @@ __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
   return r != 0;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream, launched
+// with programmatic stream serialization, start before this grid completes.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grids this one depends on programmatically have completed
+// and their memory is visible (returns at once if there are none).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
