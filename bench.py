@@ -424,8 +424,14 @@ def verify_algorithmic_bytes(case):
 
 
 def _event_ms(stream, fn, iters):
+    """Device milliseconds per call of ``fn``, from CUDA events on ``stream``.
+    A device-side sleep is queued first, so the host enqueues all ``iters``
+    calls while it runs and the events bracket back-to-back device work: a
+    short kernel is timed on the device, not at the host's launch rate."""
     import torch
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(_HEAD_START_CYCLES)
     e0.record(stream)
     for _ in range(iters):
         fn()
@@ -433,6 +439,10 @@ def _event_ms(stream, fn, iters):
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / iters
 
+
+# ~5 ms at the SM clock: longer than the host takes to enqueue any timed
+# loop below
+_HEAD_START_CYCLES = 10_000_000
 
 ROW_GROUPS = ("commit", "mid_batch", "layers", "varlen", "latency", "bookkeeping", "decode_loop",
               "layer")
