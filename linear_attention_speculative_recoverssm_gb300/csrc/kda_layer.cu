@@ -395,7 +395,9 @@ __global__ void __launch_bounds__(kGateThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   // unit i of this CTA starts a token tile when its m differs from unit i-1's
-  const auto new_tile = [&](int i) { return i == 0 || (u_begin + i) / p.H != (u_begin + i - 1) / p.H; };
+  const auto new_tile = [&](int i) {
+    return i == 0 || (u_begin + i) / p.H != (u_begin + i - 1) / p.H;
+  };
   if (warp == 4) {
     if (lane == 0) {
       bool ok = true;
@@ -405,7 +407,8 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         const int u = u_begin + i, m = u / p.H, h = u - m * p.H;
         if (new_tile(i)) {
           const int ai = m - m_first, as = ai & 1;
-          if (ai >= kGateASlots) ok = mbar_wait_bounded(&a_free[as], ((uint32_t)(ai >> 1) & 1u) ^ 1u);
+          if (ai >= kGateASlots)
+            ok = mbar_wait_bounded(&a_free[as], ((uint32_t)(ai >> 1) & 1u) ^ 1u);
           if (!ok) break;
           uint8_t *dst = a_tiles + as * kGateTileBytes;
           mbar_arrive_expect_tx(&a_full[as], kGateTileBytes);
