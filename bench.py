@@ -105,16 +105,16 @@ PROFILED = {
     "step": dict(
         sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
                  "kda_step_q8.cu"),
-        sha256="0f2b408c77a0780838e294dc7a5892a379b0e60c8f5801831a1ae4df9bfef9f2",
+        sha256="5a8bd86898b4a9b4af5513496c5008bf84507eb373aae3c7e5235cb87a89f57a",
         workload=WORKLOAD,
-        bytes_per_launch=(608.2 + 464.2) * 1e6 * 31104 / 7808,
+        bytes_per_launch=(608.2 + 464.5) * 1e6 * 31104 / 7808,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
-            "replay-verify-f32-h64-b128-q8 (608.2 + 464.2 MB, 7808 live items), scaled by "
+            "replay-verify-f32-h64-b128-q8 (608.2 + 464.5 MB, 7808 live items), scaled by "
             "live items to this workload's 31104"),
     # one kda_commit_ws launch of the standalone-commit workload itself
     "commit": dict(
         sources=("kda_commit.cu", "kda_device.cuh"),
-        sha256="6a303dbb34b5c4ce6e98b74c4aeeddeb72b140f63249e592ff8443683000fdb7",
+        sha256="70b1471b3c91c16867767ed36da7dd9315f40df30e911fd48f86ac5d8891f448",
         workload="commit-bf16-l4-h32-b64-q4-align",
         bytes_per_launch=(194.8 + 167.1) * 1e6,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_commit_ws launch of "
