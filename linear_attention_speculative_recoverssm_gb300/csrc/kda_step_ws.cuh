@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // =====================================================================
     const int c = tid;
     // The index chain slot / record row -> pending count -> records runs two
-    // items ahead in thread 0; warp 0 requests item j + 1's inputs while
+    // items ahead in thread 0; thread 32 requests item j + 1's inputs while
     // item j is built, so the warpgroup itself never waits on HBM latency.
     // Raw per-request values of an item (no branch on them, so the loads stay
     // in flight) and its pending count, loaded a step later from its row.
@@ -669,11 +669,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       return it;
     };
-    // Thread 0: item i's inputs into in[i & 1]: the window's q, k, raw_g and
-    // v rows by four tensor copies, the first n recorded key / gate rows and
-    // corrections by one bulk copy each, all completing on infull[i & 1].
+    // Thread 32 (warp 1: warp 0's lanes run the index chain): item i's
+    // inputs into in[i & 1]: the window's q, k, raw_g and v rows by four
+    // tensor copies, the first n recorded key / gate rows and corrections by
+    // one bulk copy each, all completing on infull[i & 1].
     auto request_inputs = [&](int i) {
-      if (c != 0) return;
+      if (c != 32) return;
       // the meta words move 16 bytes at a time: the ring slot and in.meta
       // have the same layout
       const int4 *w4 = reinterpret_cast<const int4 *>(sm.meta_ring[i % (2 * kWsChain)]);
@@ -754,7 +755,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
     };
 
-    int requested = 0;  // items whose inputs were requested (warp 0)
+    int requested = 0;  // items whose inputs were requested (thread 32)
     int taken = 0;      // items whose inputs were waited for
     if (count > 0) {
       requested = 1;
