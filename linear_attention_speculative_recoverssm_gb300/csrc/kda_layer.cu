@@ -4,7 +4,9 @@
 // written last; the gated RMSNorm at the kernel's end).  Two kernels bracket
 // the step: the prologue turns the layer's packed projections into the
 // step's q, k, v (the convolution kernel) and raw gates (the projection
-// kernel), and the epilogue normalises its outputs.
+// kernel), and the epilogue normalises its outputs.  The prologue's two
+// kernels run at the same time: the projection first, on half the SMs, and
+// the convolution as its programmatic dependent on the rest and beside it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
