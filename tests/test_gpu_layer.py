@@ -199,6 +199,34 @@ def test_layer_prologue_full_size_sampled():
     _compare_prologue(case, d, ref, ref_state, items=items)
 
 
+@pytest.mark.parametrize("B,H", [(3700, 1), (2900, 3)])
+def test_layer_prologue_many_token_tiles(B, H):
+    """Few heads and long batches: the gate projection's persistent CTAs
+    (on half the SMs) each walk three or more 128-token tiles, so a CTA
+    reloads its resident f_a tile into a slot freed by an earlier tile's last
+    MMA, and the last tile is ragged (B * 8 not a multiple of 128).  One
+    request per (tile, head) is checked against the oracle, so every tile
+    and head is covered; inert requests' rows must stay untouched."""
+    import torch
+    Q = 8
+    case = synth.layer_case(B=B, H=H, Q=Q, slots=B + 64, seed=900 + H, padding_frac=0.1)
+    assert (B * Q) % 128 != 0
+    d = _device_layer(case)
+    _gpu_prologue(case, d)
+    torch.cuda.synchronize()
+    assert int(tu.to_numpy(d["status"])[0]) == 0
+    rng = np.random.default_rng(12 + H)
+    per_tile = 128 // Q  # requests per token tile
+    items = []
+    for r0 in range(0, B, per_tile):
+        for h in range(H):
+            b = int(rng.integers(r0, min(B, r0 + per_tile)))
+            items.append(b * H + h)
+    items = np.array(items)
+    ref, ref_state = _oracle_prologue(case, items=items)
+    _compare_prologue(case, d, ref, ref_state, items=items)
+
+
 # --------------------------------------------------------------------------
 # the fused layer step: prologue into a workspace, then the step with the
 # gated RMSNorm folded into its row solve
