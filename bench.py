@@ -105,7 +105,7 @@ PROFILED = {
     "step": dict(
         sources=("kda_step_ws.cuh", "kda_step.cuh", "kda_device.cuh", "kda_step_launch.cuh",
                  "kda_step_q8.cu"),
-        sha256="5a8bd86898b4a9b4af5513496c5008bf84507eb373aae3c7e5235cb87a89f57a",
+        sha256="620c2da2457db0fec740a53211ff563ccb89fcdc57b68328b2aee8a9961c19eb",
         workload=WORKLOAD,
         bytes_per_launch=(608.2 + 464.5) * 1e6 * 31104 / 7808,
         how="dram__bytes_read.sum + dram__bytes_write.sum of one kda_step_ws launch on "
