@@ -199,6 +199,20 @@ def test_layer_prologue_full_size_sampled():
     _compare_prologue(case, d, ref, ref_state, items=items)
 
 
+def test_layer_prologue_many_heads():
+    """H = 128 on four requests: one token tile, 128 head tiles over the
+    gate projection's CTAs (one or two each), and 384 channel parts per
+    request for the convolution."""
+    import torch
+    case = synth.layer_case(B=4, H=128, Q=8, slots=8, seed=960, padding_frac=0.0)
+    d = _device_layer(case)
+    _gpu_prologue(case, d)
+    torch.cuda.synchronize()
+    assert int(tu.to_numpy(d["status"])[0]) == 0
+    ref, ref_state = _oracle_prologue(case)
+    _compare_prologue(case, d, ref, ref_state)
+
+
 @pytest.mark.parametrize("B,H", [(3700, 1), (2900, 3)])
 def test_layer_prologue_many_token_tiles(B, H):
     """Few heads and long batches: the gate projection's persistent CTAs

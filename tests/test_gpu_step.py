@@ -317,6 +317,16 @@ def test_fewer_items_than_sms_whole_items(B, H, Q):
     _run_and_compare(case, split=1)
 
 
+@pytest.mark.parametrize("H", [128, 100])
+def test_many_heads(H):
+    """Many heads on few requests: the item index is split into request and
+    head by a multiply and shifts (H = 100 is not a power of two), and the
+    pages of one slot span H * 64 KB."""
+    case = synth.replay_verify_case(B=3, H=H, Q=8, slots=7, seed=70 + H, padding_frac=0.0,
+                                    no_record_frac=0.0)
+    _run_and_compare(case, split=1)
+
+
 @pytest.mark.parametrize("lower_bound", [-10.0, 0.0])
 def test_gate_bound_extremes(lower_bound):
     """At the largest supported |lower_bound| the decay products over the
