@@ -77,6 +77,17 @@ def test_commit(Q, dtype, align):
     _compare_pools(got, ref, c["layers"])
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_commit_many_heads(dtype):
+    """H = 128 on few requests and two layers: a layer's slot spans 128
+    pages, and the (layer, request, head) items of one request cover most of
+    the grid."""
+    c = synth.commit_case(L=2, B=3, H=128, Q=4, slots=8, seed=530, state_dtype=dtype,
+                          boundary_frac=0.4)
+    got, ref = _commit_both(c, align=True)
+    _compare_pools(got, ref, c["layers"])
+
+
 def test_commit_with_record_rows():
     c = synth.commit_case(L=2, B=16, H=2, Q=4, slots=64, seed=17, state_dtype="f32")
     rows = np.random.default_rng(1).permutation(16).astype(np.int32)
