@@ -67,6 +67,16 @@ def test_layers_match_single_layer_oracle(L, Q):
     _compare_layers(case, d)
 
 
+def test_layers_many_heads():
+    """H = 128 on three requests over two layers: each layer's slot spans 128
+    pages, and the (layer, request, head) index is split by the layer and
+    head counts at a large head count."""
+    case = synth.layers_case(L=2, B=3, H=128, Q=8, slots=8, seed=870)
+    d = _device(case)
+    _run(case, d)
+    _compare_layers(case, d)
+
+
 def test_layers_spread_key_norms():
     """Per-vector key norms spread over 1e-3 .. 1e2 in every layer."""
     case = synth.layers_case(L=3, B=16, H=4, Q=6, slots=24, seed=830, padding_frac=0.1,
